@@ -1,0 +1,164 @@
+/*
+ * moe.h -- C ABI of libmoe.so: the forward pass of a Mixtral-style sparse
+ * mixture-of-experts feed-forward layer on one NVIDIA B300 (sm_103a).
+ *
+ * What the layer computes (Mixtral of Experts, arXiv 2401.04088, as given on
+ * the paper-graph-ui summary, section 3.4 "MoE Layer Formulation", and the
+ * xyznot reading guide, "Method (with the key equations)"):
+ *
+ *   logits  l = x . W_g                          (router, no bias)
+ *   G(x)    = Softmax(TopK(l))                   (TopK keeps the K largest, -inf elsewhere)
+ *   E_i(x)  = (SiLU(x . W1[i]) (.) (x . W3[i])) . W2[i]     SiLU(z) = z sigma(z)
+ *             ("Expert Network Structure (SwiGLU)", written here in row-vector
+ *             form: W1 is the SiLU branch, W3 the linear branch, W2 the down
+ *             projection)
+ *   y       = sum_i G(x)_i . E_i(x)              (only the K selected experts compute)
+ *
+ * Choices the pages leave open, fixed here:
+ *   - equal logits rank by lower expert index (for every TopK position);
+ *   - slot 0 of a token is its larger logit;
+ *   - router, TopK and the softmax run in fp32; the expert GEMMs take bf16
+ *     operands with fp32 accumulation; the SwiGLU hidden activations are
+ *     stored as bf16; the per-slot expert outputs are fp32 and summed in a
+ *     fixed order (slot 0 then slot 1), so results are bitwise reproducible.
+ *
+ * Conventions for every entry point
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise, on
+ *     the current CUDA device, 16-byte aligned, to a dense row-major tensor.
+ *   - dtype selects the element type shared by x, W_g, W1, W3, W2 and y:
+ *     MOE_BF16 (tensor-core path) or MOE_F32 (exact fp32 SIMT path, no TF32).
+ *   - Every call is asynchronous on `stream` (a cudaStream_t; NULL = legacy
+ *     default stream) except moe_read_status, which synchronises it.
+ *   - The caller owns and allocates every buffer, including the workspace.
+ *     The library allocates no device memory and keeps no per-call state; its
+ *     only global state is a cached device-attribute table.
+ *   - Arguments are validated on the host before anything is enqueued; a
+ *     failed check returns an error code and launches nothing.  Launch
+ *     failures map to MOE_ERR_CUDA.  Errors found on the device (a bounded
+ *     wait that expired, an out-of-range index, non-finite router input under
+ *     MOE_DEBUG_CHECKS) are written to a status word in the workspace and read
+ *     with moe_read_status.  Nothing in the library calls exit() or abort().
+ *   - Inputs must be finite.  NaN or Inf in x or W_g gives unspecified
+ *     routing (reported as MOE_ERR_NONFINITE under MOE_DEBUG_CHECKS).
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#if defined(__GNUC__)
+#define MOE_API __attribute__((visibility("default")))
+#else
+#define MOE_API
+#endif
+
+/* Same type as cudaStream_t. */
+typedef struct CUstream_st *moe_stream_t;
+
+/* Status codes (plain int in every signature). */
+enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,     /* null/misaligned pointer, bad size, aliasing */
+  MOE_ERR_UNSUPPORTED = 2,     /* valid but not implemented (dtype, E, K, device) */
+  MOE_ERR_WORKSPACE = 3,       /* workspace pointer null or smaller than required */
+  MOE_ERR_CUDA = 4,            /* a CUDA runtime call or launch failed */
+  MOE_ERR_DEVICE_TIMEOUT = 5,  /* a bounded device-side wait expired */
+  MOE_ERR_NONFINITE = 6,       /* NaN/Inf router logit (MOE_DEBUG_CHECKS only) */
+  MOE_ERR_DEVICE_BOUNDS = 7    /* device-side index check failed (MOE_DEBUG_CHECKS only) */
+};
+
+/* Element types. */
+enum { MOE_BF16 = 0, MOE_F32 = 1 };
+
+/* moe_forward flags. */
+#define MOE_ACCUMULATE   0x1u  /* y += MoE(x) instead of y = MoE(x) (residual stream) */
+#define MOE_DEBUG_CHECKS 0x2u  /* device-side range and finiteness checks */
+
+/*
+ * Workspace size in bytes for moe_forward / moe_route with these sizes, or 0
+ * if the sizes are invalid or unsupported.  The layout depends only on the
+ * arguments, so one buffer can be reused for every call with the same sizes.
+ * It holds the status word, the routing table, the expert grouping and the
+ * grouped activations; at T = 4096, d = 4096, f = 14336, E = 8, K = 2, bf16
+ * it is about 0.5 GB.
+ */
+MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype);
+
+/*
+ * The MoE layer forward pass: y = sum over the K selected experts of
+ * gate * SwiGLU_expert(x) (section 3.4 "MoE Layer Formulation", output
+ * combination; "Expert Network Structure (SwiGLU)").
+ *
+ *   x   [T, d]      input tokens
+ *   Wg  [d, E]      router weights
+ *   W1  [E, d, f]   SiLU-branch projections
+ *   W3  [E, d, f]   linear-branch projections
+ *   W2  [E, f, d]   down projections
+ *   y   [T, d]      output; must not overlap x.  With MOE_ACCUMULATE, y is
+ *                   read and the layer output is added to it (in fp32, then
+ *                   rounded to dtype).
+ *   T >= 0 (T = 0 returns MOE_OK at once; x, y, workspace may then be NULL),
+ *   1 <= K <= 2, K <= E <= 32,
+ *   d, f >= 1 and multiples of 8 (bf16) or 4 (f32).
+ *   workspace / ws_bytes: device buffer of at least moe_workspace_bytes().
+ *     Calls sharing one workspace must be ordered on the GPU (same stream or
+ *     synchronised); concurrent calls need separate workspaces.
+ *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS.
+ * Returns MOE_OK once every kernel is enqueued.
+ */
+MOE_API int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+                void *y, int T, int d, int f, int E, int K, int dtype,
+                void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * Routing only, for inspection: the router and grouping kernels that
+ * moe_forward runs, with their results copied out in unpadded form
+ * (section 3.4 gating function; "Top-K Gating Mechanism and Routing").
+ *
+ *   idx      [T, K] int32   selected experts, slot 0 = larger logit
+ *   gate     [T, K] float   softmax weights over the selected logits
+ *   perm_tok [T*K]  int32   token id of each row of the expert-grouped order:
+ *                           experts ascending, and within one expert the
+ *                           (token, slot) pairs in ascending t*K+k order
+ *   offsets  [E+1]  int32   start row of each expert in perm_tok; offsets[E] = T*K
+ *   pos      [T, K] int32   row of (t, k) in perm_tok order; may be NULL
+ * Same size limits and workspace as moe_forward (same dtype).  With T = 0
+ * only offsets is written (all zero) and the other pointers may be NULL.
+ */
+MOE_API int moe_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype,
+              int32_t *idx, float *gate, int32_t *perm_tok, int32_t *offsets, int32_t *pos,
+              void *workspace, size_t ws_bytes, moe_stream_t stream);
+
+/*
+ * RMSNorm with unit gain, out = x / sqrt(mean(x^2) + eps) per row, fp32 math
+ * (pre-norm before each MoE block; paper-graph-ui summary, "Architectural
+ * Inheritance from Mistral 7B", layer normalisation).  x, out: [T, d] of
+ * dtype; out may equal x (in place); T >= 0, d >= 1; eps > 0.
+ */
+MOE_API int moe_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, moe_stream_t stream);
+
+/*
+ * Synchronises `stream`, then returns the device status word in `workspace`
+ * (MOE_OK if no device-side error was recorded since the last moe_forward or
+ * moe_route on this workspace cleared it), or MOE_ERR_CUDA if the
+ * synchronisation itself failed.  workspace: the device buffer passed to
+ * moe_forward.
+ */
+MOE_API int moe_read_status(const void *workspace, moe_stream_t stream);
+
+/* Static, NUL-terminated description of a status code. */
+MOE_API const char *moe_status_string(int status);
+
+/* Library version, major * 10000 + minor * 100 + patch. */
+MOE_API int moe_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

@@ -1,0 +1,161 @@
+"""Mixtral-style sparse mixture-of-experts feed-forward layer for NVIDIA B300.
+
+Python binding of libmoe.so (include/moe.h).  These functions only marshal
+arguments: they take torch tensors for device memory and streams and pass raw
+pointers to the C ABI; every step of the layer runs in the library's CUDA
+kernels.  There is no CPU fallback.
+
+    y = moe_forward(x, Wg, W1, W3, W2, K=2)
+
+computes y = sum over the K selected experts of gate * SwiGLU_expert(x), with
+x [T, d], Wg [d, E], W1/W3 [E, d, f], W2 [E, f, d] (bf16 or fp32, all on one
+CUDA device).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from . import _lib
+from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_F32, MoEError,  # noqa: F401
+                   status_string)
+
+__all__ = ["moe_forward", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+           "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
+           "status_string", "library_path"]
+
+_DTYPES = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}
+
+
+def library_path() -> str:
+    return str(_lib.LIB_PATH)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype not in _DTYPES:
+        raise TypeError(f"unsupported dtype {t.dtype}; use bfloat16 or float32")
+    return _DTYPES[t.dtype]
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr()) if t is not None else ctypes.c_void_p(0)
+
+
+def _stream_ptr(stream, device) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream(device)
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _need(t: torch.Tensor, name: str, dtype=None, device=None):
+    if not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must have dtype {dtype}, got {t.dtype}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def moe_workspace_bytes(T: int, d: int, f: int, E: int, K: int, dtype=torch.bfloat16) -> int:
+    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    n = _lib.load().moe_workspace_bytes(T, d, f, E, K, code)
+    if n == 0:
+        raise ValueError(f"unsupported sizes T={T} d={d} f={f} E={E} K={K} dtype={dtype}")
+    return int(n)
+
+
+class Workspace:
+    """A reusable device workspace sized by moe_workspace_bytes (a torch uint8 buffer)."""
+
+    def __init__(self, T, d, f, E, K, dtype=torch.bfloat16, device=None):
+        self.nbytes = moe_workspace_bytes(T, d, f, E, K, dtype)
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        self.key = (T, d, f, E, K, dtype)
+
+    def ptr(self):
+        return ctypes.c_void_p(self.buf.data_ptr())
+
+
+def moe_forward(x, Wg, W1, W3, W2, K: int = 2, y=None, workspace: Workspace | None = None,
+                flags: int = 0, stream=None):
+    """MoE layer forward on the GPU; returns y [T, d] (written in place if given)."""
+    dev = x.device
+    dt = x.dtype
+    for t, n in ((x, "x"), (Wg, "Wg"), (W1, "W1"), (W3, "W3"), (W2, "W2")):
+        _need(t, n, dt, dev)
+    T, d = x.shape
+    E, d1, f = W1.shape
+    if Wg.shape != (d, E) or W3.shape != (E, d, f) or W2.shape != (E, f, d) or d1 != d:
+        raise ValueError("shape mismatch: x [T,d], Wg [d,E], W1/W3 [E,d,f], W2 [E,f,d]")
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", dt, dev)
+    if workspace is None:
+        workspace = Workspace(T, d, f, E, K, dt, dev)
+    rc = _lib.load().moe_forward(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(y), T, d, f, E, K,
+                                 _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
+                                 _stream_ptr(stream, dev))
+    _lib.check("moe_forward", rc)
+    return y
+
+
+def moe_forward_host(x_host, y_host, Wg, W1, W3, W2, K: int = 2, x_dev=None, y_dev=None,
+                     workspace: Workspace | None = None, stream=None):
+    """End-to-end call on host buffers: copy x (pinned host) to the device,
+    run the layer, copy y back.  Weights are device-resident."""
+    dev = W1.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    if x_dev is None:
+        x_dev = torch.empty(x_host.shape, dtype=x_host.dtype, device=dev)
+    if y_dev is None:
+        y_dev = torch.empty_like(x_dev)
+    with torch.cuda.stream(s):
+        x_dev.copy_(x_host, non_blocking=True)
+        moe_forward(x_dev, Wg, W1, W3, W2, K, y=y_dev, workspace=workspace, stream=s)
+        y_host.copy_(y_dev, non_blocking=True)
+    return y_host
+
+
+def moe_route(x, Wg, K: int = 2, workspace: Workspace | None = None, stream=None):
+    """Routing only: returns (idx [T,K] int32, gate [T,K] fp32, perm_tok [T*K] int32,
+    offsets [E+1] int32, pos [T,K] int32), unpadded grouped order."""
+    dev = x.device
+    _need(x, "x", None, dev)
+    _need(Wg, "Wg", x.dtype, dev)
+    T, d = x.shape
+    E = Wg.shape[1]
+    idx = torch.empty((T, K), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, K), dtype=torch.float32, device=dev)
+    perm = torch.empty((T * K,), dtype=torch.int32, device=dev)
+    offsets = torch.empty((E + 1,), dtype=torch.int32, device=dev)
+    pos = torch.empty((T, K), dtype=torch.int32, device=dev)
+    f_min = 8 if x.dtype == torch.bfloat16 else 4
+    if workspace is None:
+        workspace = Workspace(T, d, f_min, E, K, x.dtype, dev)
+    rc = _lib.load().moe_route(_ptr(x), _ptr(Wg), T, d, E, K, _dtype_code(x), _ptr(idx), _ptr(gate), _ptr(perm),
+                               _ptr(offsets), _ptr(pos), workspace.ptr(), workspace.nbytes,
+                               _stream_ptr(stream, dev))
+    _lib.check("moe_route", rc)
+    return idx, gate, perm, offsets, pos
+
+
+def moe_rmsnorm(x, eps: float = 1e-5, out=None, stream=None):
+    """out = x / sqrt(mean(x^2) + eps) per row (unit gain); in place if out is x."""
+    _need(x, "x")
+    if out is None:
+        out = torch.empty_like(x)
+    else:
+        _need(out, "out", x.dtype, x.device)
+    T, d = x.shape
+    rc = _lib.load().moe_rmsnorm(_ptr(x), _ptr(out), T, d, float(eps), _dtype_code(x),
+                                 _stream_ptr(stream, x.device))
+    _lib.check("moe_rmsnorm", rc)
+    return out
+
+
+def moe_read_status(workspace: Workspace, stream=None) -> int:
+    """Synchronise the stream and return the device status word (0 = ok)."""
+    return int(_lib.load().moe_read_status(workspace.ptr(), _stream_ptr(stream, workspace.buf.device)))

@@ -1,0 +1,77 @@
+"""ctypes loader for libmoe.so (the C ABI of include/moe.h).
+
+The library is built in-tree (``python -m sparse_mixture_experts_55_b300.build``).
+There is no fallback: if the shared library is missing or fails to load, every
+call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+import threading
+
+LIB_PATH = pathlib.Path(__file__).resolve().parent / "libmoe.so"
+
+MOE_OK = 0
+MOE_ERR_INVALID_ARG = 1
+MOE_ERR_UNSUPPORTED = 2
+MOE_ERR_WORKSPACE = 3
+MOE_ERR_CUDA = 4
+MOE_ERR_DEVICE_TIMEOUT = 5
+MOE_ERR_NONFINITE = 6
+MOE_ERR_DEVICE_BOUNDS = 7
+
+MOE_BF16 = 0
+MOE_F32 = 1
+
+MOE_ACCUMULATE = 0x1
+MOE_DEBUG_CHECKS = 0x2
+
+# name -> (restype, argtypes), one entry per function declared in include/moe.h
+_vp, _i, _sz, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
+SIGNATURES = {
+    "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "moe_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
+    "moe_route": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "moe_rmsnorm": (_i, [_vp, _vp, _i, _i, ctypes.c_float, _i, _vp]),
+    "moe_read_status": (_i, [_vp, _vp]),
+    "moe_status_string": (ctypes.c_char_p, [_i]),
+    "moe_version": (_i, []),
+}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class MoEError(RuntimeError):
+    """A libmoe entry point returned a non-zero status."""
+
+    def __init__(self, fn: str, code: int):
+        self.code = code
+        super().__init__(f"{fn} failed: status {code} ({status_string(code)})")
+
+
+def load() -> ctypes.CDLL:
+    """Load libmoe.so once and attach the C signatures; raises if it is missing."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not LIB_PATH.exists():
+                raise RuntimeError(
+                    f"{LIB_PATH} is missing: build it with `python -m sparse_mixture_experts_55_b300.build`")
+            lib = ctypes.CDLL(str(LIB_PATH))
+            for name, (res, args) in SIGNATURES.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+def status_string(code: int) -> str:
+    return load().moe_status_string(int(code)).decode()
+
+
+def check(fn: str, code: int) -> None:
+    if code != MOE_OK:
+        raise MoEError(fn, code)

@@ -1,0 +1,72 @@
+// internal.h -- workspace layout and kernel launchers shared by the library's
+// translation units (not part of the public ABI; see include/moe.h).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// Rows of every expert segment in the grouped buffers are padded to a
+// multiple of this, so a 128-row MMA tile never straddles two experts.
+constexpr int kSegPad = 128;
+// Tokens per router block; also the chunk of (token, slot) entries one
+// grouping block ranks.
+constexpr int kRouteTokens = 64;
+constexpr int kMaxE = 32;
+constexpr int kMaxK = 2;
+// Status-word slots at the start of the workspace.
+constexpr int kStatusInts = 8;
+
+struct WsLayout {
+  // byte offsets into the workspace
+  size_t status, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf, obuf;
+  size_t total;
+  int R;         // padded grouped rows (upper bound): T*K + E*(kSegPad-1), rounded up to kSegPad
+  int S;         // split-K count of the down projection
+  int kb_per_split;
+  int n_route_blocks;
+};
+
+// Split-K count for the down projection: enough (expert, n-tile, split) work
+// units to cover the SMs when few tokens are routed.
+int down_splits(int T, int d, int f, int E, int K, int num_sms);
+WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms);
+
+struct Ptrs {
+  int *status;
+  int32_t *idx;
+  float *gate;
+  int32_t *blockcounts, *offsets, *poffsets, *pos, *perm_tok;
+  float *perm_gate;
+  void *xperm, *hbuf;
+  float *obuf;
+};
+Ptrs carve(void *ws, const WsLayout &L);
+
+// -------- routing.cu
+cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
+                         const Ptrs &P, cudaStream_t s);
+cudaError_t launch_group(int T, int E, int K, int n_route_blocks, unsigned flags, const Ptrs &P,
+                         cudaStream_t s);
+cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
+                          cudaStream_t s);
+cudaError_t launch_combine(void *y, int T, int d, int K, int S, int R, int dtype, unsigned flags, const Ptrs &P,
+                           int num_sms, cudaStream_t s);
+cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate,
+                                int32_t *perm_tok, int32_t *offsets, int32_t *pos, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s);
+
+// -------- gemm_tc.cu (bf16 tensor-core path)
+cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
+                                     const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
+                                     cudaStream_t s);
+
+// -------- gemm_simt.cu (exact fp32 path)
+cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,
+                                  const WsLayout &L, const Ptrs &P, cudaStream_t s);
+
+}  // namespace moe

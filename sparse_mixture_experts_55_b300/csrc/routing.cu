@@ -1,0 +1,476 @@
+// routing.cu -- the router (logits, top-K with lower-index ties, softmax over
+// the kept logits), the stable grouping of (token, slot) pairs by expert, the
+// row gather into the grouped activation buffer, the deterministic two-slot
+// combine, and RMSNorm.
+//
+// Method: Mixtral of Experts (arXiv 2401.04088), paper-graph-ui summary,
+// section 3.4 "MoE Layer Formulation" (G(x) = Softmax(TopK(x . W_g)),
+// y = sum_i G(x)_i E_i(x)) and "Top-K Gating Mechanism and Routing" (the
+// three-step Top-2 procedure); grouping tokens by expert follows
+// "Inference and Deployment Infrastructure" (all experts' inputs packed into
+// one matrix).
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <cstdint>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(status, 0, code); }
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename Tin>
+struct Vec;  // one 16-byte vector of inputs
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16 *p, float (&v)[8]) {
+    uint4 u = __ldg(reinterpret_cast<const uint4 *>(p));
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      float2 f = __bfloat1622float2(h[i]);
+      v[2 * i] = f.x;
+      v[2 * i + 1] = f.y;
+    }
+  }
+};
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float *p, float (&v)[4]) {
+    float4 u = __ldg(reinterpret_cast<const float4 *>(p));
+    v[0] = u.x; v[1] = u.y; v[2] = u.z; v[3] = u.w;
+  }
+};
+
+// Accumulate x[j] * Wg[j, :] for the 16-byte vector of x starting at column j0.
+template <typename Tin, int EP>
+__device__ __forceinline__ void accum_vec(const Tin *__restrict__ x_row, const Tin *__restrict__ Wg, int j0, int E,
+                                          float (&acc)[EP]) {
+  constexpr int NV = Vec<Tin>::N;
+  float xv[NV];
+  Vec<Tin>::load(x_row + j0, xv);
+  if (EP == 8 && E == 8) {
+    // Router rows of 8 experts are 16 B (bf16) or 32 B (fp32): vector loads.
+#pragma unroll
+    for (int c = 0; c < NV; ++c) {
+      const Tin *wrow = Wg + static_cast<size_t>(j0 + c) * 8;
+      float w[8];
+      if constexpr (sizeof(Tin) == 2) {
+        Vec<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(wrow), w);
+      } else {
+        float w0[4], w1[4];
+        Vec<float>::load(reinterpret_cast<const float *>(wrow), w0);
+        Vec<float>::load(reinterpret_cast<const float *>(wrow) + 4, w1);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) { w[e] = w0[e]; w[4 + e] = w1[e]; }
+      }
+#pragma unroll
+      for (int e = 0; e < 8; ++e) acc[e] = fmaf(xv[c], w[e], acc[e]);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < NV; ++c) {
+      const Tin *wrow = Wg + static_cast<size_t>(j0 + c) * E;
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+        if (e < E) acc[e] = fmaf(xv[c], to_f(wrow[e]), acc[e]);
+    }
+  }
+}
+
+// Top-K (K <= 2) of the E logits with lower-index tie-break, softmax over the
+// kept logits, and the per-block expert histogram.
+template <int EP>
+__device__ __forceinline__ void select_and_store(const float (&l)[EP], int t, int E, int K, unsigned flags,
+                                                 int32_t *idx, float *gate, int *s_cnt, int *status) {
+  if (flags & MOE_DEBUG_CHECKS) {
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E && !isfinite(l[e])) set_status(status, MOE_ERR_NONFINITE);
+  }
+  int i1 = 0;
+  float v1 = l[0];
+#pragma unroll
+  for (int e = 1; e < EP; ++e)
+    if (e < E && l[e] > v1) { v1 = l[e]; i1 = e; }
+  if (K == 1) {
+    idx[t] = i1;
+    gate[t] = 1.0f;
+    atomicAdd(&s_cnt[i1], 1);
+    return;
+  }
+  int i2 = -1;
+  float v2 = 0.f;
+#pragma unroll
+  for (int e = 0; e < EP; ++e)
+    if (e < E && e != i1 && (i2 < 0 || l[e] > v2)) { v2 = l[e]; i2 = e; }
+  // softmax over {v1, v2}: g1 = e^v1 / (e^v1 + e^v2) = 1 / (1 + e^(v2 - v1)), g2 = 1 - g1
+  const float g1 = 1.0f / (1.0f + expf(v2 - v1));
+  idx[2 * t] = i1;
+  idx[2 * t + 1] = i2;
+  gate[2 * t] = g1;
+  gate[2 * t + 1] = 1.0f - g1;
+  atomicAdd(&s_cnt[i1], 1);
+  atomicAdd(&s_cnt[i2], 1);
+}
+
+// One block routes kRouteTokens tokens with 8 warps.  With at least 8 tokens a
+// warp owns whole tokens; with fewer, the warps of a group split d and sum
+// their partials in a fixed order.
+template <typename Tin, int EP>
+__global__ void __launch_bounds__(256) route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T,
+                                                    int d, int E, int K, unsigned flags, int32_t *__restrict__ idx,
+                                                    float *__restrict__ gate, int32_t *__restrict__ blockcounts,
+                                                    int *status) {
+  constexpr int NV = Vec<Tin>::N;
+  __shared__ float s_part[8][EP];
+  __shared__ int s_cnt[kMaxE];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int t0 = blockIdx.x * kRouteTokens;
+  const int nt = min(kRouteTokens, T - t0);
+  const int nvec = d / NV;
+  if (threadIdx.x < kMaxE) s_cnt[threadIdx.x] = 0;
+  __syncthreads();
+
+  if (nt >= 8) {
+    for (int tl = warp; tl < nt; tl += 8) {
+      const int t = t0 + tl;
+      const Tin *x_row = x + static_cast<size_t>(t) * d;
+      float acc[EP];
+#pragma unroll
+      for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+      for (int v = lane; v < nvec; v += 32) accum_vec<Tin, EP>(x_row, Wg, v * NV, E, acc);
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+      if (lane == 0) select_and_store<EP>(acc, t, E, K, flags, idx, gate, s_cnt, status);
+    }
+  } else {
+    int wpt = 8 / nt;                       // warps per token, rounded down to a power of two
+    wpt = 1 << (31 - __clz(wpt));
+    const int group = warp / wpt, sub = warp % wpt;
+    const bool has_token = group < nt;
+    float acc[EP];
+#pragma unroll
+    for (int e = 0; e < EP; ++e) acc[e] = 0.f;
+    if (has_token) {
+      const Tin *x_row = x + static_cast<size_t>(t0 + group) * d;
+      const int per = (nvec + wpt - 1) / wpt;
+      const int v0 = sub * per, v1 = min(nvec, v0 + per);
+      for (int v = v0 + lane; v < v1; v += 32) accum_vec<Tin, EP>(x_row, Wg, v * NV, E, acc);
+#pragma unroll
+      for (int e = 0; e < EP; ++e)
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
+      if (lane == 0) {
+#pragma unroll
+        for (int e = 0; e < EP; ++e) s_part[warp][e] = acc[e];
+      }
+    }
+    __syncthreads();
+    if (has_token && sub == 0 && lane == 0) {
+      float l[EP];
+#pragma unroll
+      for (int e = 0; e < EP; ++e) {
+        float s = 0.f;
+        for (int w = 0; w < wpt; ++w) s += s_part[warp + w][e];
+        l[e] = s;
+      }
+      select_and_store<EP>(l, t0 + group, E, K, flags, idx, gate, s_cnt, status);
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x < E) blockcounts[blockIdx.x * E + threadIdx.x] = s_cnt[threadIdx.x];
+}
+
+// Stable grouping.  Block b ranks the (token, slot) entries of router block b
+// in flat t*K + k order: rank = entries of that expert in earlier blocks +
+// in earlier warps of this block + in earlier lanes of this warp.  Each
+// expert's segment in the grouped buffers starts at a multiple of kSegPad;
+// pad rows get token -1 and gate 0.
+__global__ void __launch_bounds__(kRouteTokens *kMaxK)
+    group_kernel(int T, int E, int K, int nb, unsigned flags, const int32_t *__restrict__ idx,
+                 const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
+                 int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status) {
+  constexpr int NT = kRouteTokens * kMaxK;
+  constexpr int NW = NT / 32;
+  __shared__ int s_base[kMaxE], s_tot[kMaxE], s_off[kMaxE + 1], s_poff[kMaxE + 1];
+  __shared__ int s_wcnt[NW][kMaxE];
+  const int tid = threadIdx.x, b = blockIdx.x;
+  const int warp = tid >> 5, lane = tid & 31;
+  if (tid < kMaxE) { s_base[tid] = 0; s_tot[tid] = 0; }
+  for (int i = tid; i < NW * kMaxE; i += NT) (&s_wcnt[0][0])[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < nb * E; i += NT) {
+    const int bb = i / E, e = i - bb * E;
+    const int c = blockcounts[i];
+    atomicAdd(&s_tot[e], c);
+    if (bb < b) atomicAdd(&s_base[e], c);
+  }
+  __syncthreads();
+  if (tid == 0) {
+    int off = 0, poff = 0;
+    for (int e = 0; e < E; ++e) {
+      s_off[e] = off;
+      s_poff[e] = poff;
+      off += s_tot[e];
+      poff += (s_tot[e] + kSegPad - 1) / kSegPad * kSegPad;
+    }
+    s_off[E] = off;
+    s_poff[E] = poff;
+  }
+  __syncthreads();
+  if (b == 0 && tid <= E) { offsets[tid] = s_off[tid]; poffsets[tid] = s_poff[tid]; }
+
+  const int flat0 = b * kRouteTokens * K;
+  const int n_entries = min(kRouteTokens, T - b * kRouteTokens) * K;
+  bool active = tid < n_entries;
+  int e = active ? idx[flat0 + tid] : -1;
+  if (active && (e < 0 || e >= E)) {
+    set_status(status, MOE_ERR_DEVICE_BOUNDS);
+    active = false;
+    e = -1;
+  }
+  const unsigned peers = __match_any_sync(0xffffffffu, e);
+  const int rank_w = __popc(peers & ((1u << lane) - 1u));
+  if (active && rank_w == 0) s_wcnt[warp][e] = __popc(peers);
+  __syncthreads();
+  if (active) {
+    int r = s_base[e] + rank_w;
+    for (int w = 0; w < warp; ++w) r += s_wcnt[w][e];
+    const int rp = s_poff[e] + r;
+    perm_tok[rp] = (flat0 + tid) / K;
+    perm_gate[rp] = gate[flat0 + tid];
+    pos[flat0 + tid] = rp;
+  }
+  for (int ee = b; ee < E; ee += nb) {
+    const int start = s_poff[ee] + s_tot[ee], end = s_poff[ee + 1];
+    for (int r = start + tid; r < end; r += NT) {
+      perm_tok[r] = -1;
+      perm_gate[r] = 0.f;
+    }
+  }
+  (void)flags;
+}
+
+// X_perm[r, :] = x[perm_tok[r], :] for every grouped row; pad rows are zeroed.
+// One warp per row, 16-byte vectors.
+__global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x, int T, int vec_per_row,
+                                                     const int32_t *__restrict__ perm_tok,
+                                                     const int32_t *__restrict__ poffsets, int E,
+                                                     uint4 *__restrict__ xperm, int *status) {
+  const int rows = poffsets[E];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  for (int r = gw; r < rows; r += nw) {
+    int tok = perm_tok[r];
+    if (tok >= T) {
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      tok = -1;
+    }
+    uint4 *dst = xperm + static_cast<size_t>(r) * vec_per_row;
+    if (tok >= 0) {
+      const uint4 *src = x + static_cast<size_t>(tok) * vec_per_row;
+      int v = lane;
+      for (; v + 96 < vec_per_row; v += 128) {
+        uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), dd = __ldg(src + v + 96);
+        dst[v] = a; dst[v + 32] = b; dst[v + 64] = c; dst[v + 96] = dd;
+      }
+      for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
+    } else {
+      for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+__device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16 *p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<uint32_t *>(&a);
+  u.y = *reinterpret_cast<uint32_t *>(&b);
+  *reinterpret_cast<uint2 *>(p) = u;
+}
+__device__ __forceinline__ float4 load4(const float *p) { return *reinterpret_cast<const float4 *>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
+  uint2 u = *reinterpret_cast<const uint2 *>(p);
+  float2 a = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u.x));
+  float2 b = __bfloat1622float2(*reinterpret_cast<__nv_bfloat162 *>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+
+// y[t] = sum_k (sum_s O[s][pos[t,k]]): slot 0 then slot 1, splits in order.
+// The gate was applied by the down projection's epilogue.  No atomics.
+template <typename Tout>
+__global__ void __launch_bounds__(256) combine_kernel(Tout *__restrict__ y, int T, int d, int K, int S,
+                                                      long long split_stride, const float *__restrict__ obuf,
+                                                      const int32_t *__restrict__ pos, int rows_bound,
+                                                      unsigned flags, int *status) {
+  const int q = d >> 2;
+  const long long total = static_cast<long long>(T) * q;
+  for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
+       i += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int t = static_cast<int>(i / q);
+    const int c = static_cast<int>(i - static_cast<long long>(t) * q) * 4;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int k = 0; k < K; ++k) {
+      int r = pos[t * K + k];
+      if (r < 0 || r >= rows_bound) {
+        set_status(status, MOE_ERR_DEVICE_BOUNDS);
+        continue;
+      }
+      const float *src = obuf + static_cast<size_t>(r) * d + c;
+      float4 sk = __ldg(reinterpret_cast<const float4 *>(src));
+      for (int s = 1; s < S; ++s) {
+        float4 v = __ldg(reinterpret_cast<const float4 *>(src + s * split_stride));
+        sk.x += v.x; sk.y += v.y; sk.z += v.z; sk.w += v.w;
+      }
+      if (k == 0) {
+        acc = sk;
+      } else {
+        acc.x += sk.x; acc.y += sk.y; acc.z += sk.z; acc.w += sk.w;
+      }
+    }
+    Tout *dst = y + static_cast<size_t>(t) * d + c;
+    if (flags & MOE_ACCUMULATE) {
+      float4 old = load4(dst);
+      acc.x = old.x + acc.x; acc.y = old.y + acc.y; acc.z = old.z + acc.z; acc.w = old.w + acc.w;
+    }
+    store4(dst, acc);
+  }
+}
+
+// Unpadded copies of the routing results for moe_route.
+__global__ void route_export_kernel(int T, int E, int K, const int32_t *__restrict__ idx_ws,
+                                    const float *__restrict__ gate_ws, const int32_t *__restrict__ pos_ws,
+                                    const int32_t *__restrict__ offsets_ws, const int32_t *__restrict__ poffsets_ws,
+                                    int32_t *idx, float *gate, int32_t *perm_tok, int32_t *offsets, int32_t *pos) {
+  const int n = T * K;
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
+    const int e = idx_ws[i];
+    const int ru = offsets_ws[e] + (pos_ws[i] - poffsets_ws[e]);
+    idx[i] = e;
+    gate[i] = gate_ws[i];
+    perm_tok[ru] = i / K;
+    if (pos) pos[i] = ru;
+  }
+  if (blockIdx.x == 0 && threadIdx.x <= E) offsets[threadIdx.x] = offsets_ws[threadIdx.x];
+}
+
+// out = x / sqrt(mean(x^2) + eps) per row; one block per row, fp32 sums.
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T *__restrict__ out, int d, float eps) {
+  __shared__ float s_red[8];
+  const T *row = x + static_cast<size_t>(blockIdx.x) * d;
+  T *orow = out + static_cast<size_t>(blockIdx.x) * d;
+  float ss = 0.f;
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    const float v = to_f(row[j]);
+    ss = fmaf(v, v, ss);
+  }
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += s_red[w];
+  const float inv = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+  __syncthreads();  // every thread has read s_red before any write below (in-place safe)
+  for (int j = threadIdx.x; j < d; j += blockDim.x) {
+    const float v = to_f(row[j]) * inv;
+    if constexpr (sizeof(T) == 2) orow[j] = __float2bfloat16_rn(v);
+    else orow[j] = v;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
+                         const Ptrs &P, cudaStream_t s) {
+  const int nb = (T + kRouteTokens - 1) / kRouteTokens;
+  if (dtype == MOE_BF16) {
+    auto *xx = static_cast<const __nv_bfloat16 *>(x);
+    auto *ww = static_cast<const __nv_bfloat16 *>(Wg);
+    if (E <= 8)
+      route_kernel<__nv_bfloat16, 8><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts,
+                                                         P.status);
+    else
+      route_kernel<__nv_bfloat16, 32><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts,
+                                                          P.status);
+  } else {
+    auto *xx = static_cast<const float *>(x);
+    auto *ww = static_cast<const float *>(Wg);
+    if (E <= 8)
+      route_kernel<float, 8><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts, P.status);
+    else
+      route_kernel<float, 32><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts,
+                                                 P.status);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_group(int T, int E, int K, int nb, unsigned flags, const Ptrs &P, cudaStream_t s) {
+  group_kernel<<<nb, kRouteTokens * kMaxK, 0, s>>>(T, E, K, nb, flags, P.idx, P.gate, P.blockcounts, P.offsets,
+                                                   P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
+                          cudaStream_t s) {
+  const int elem = dtype == MOE_BF16 ? 2 : 4;
+  const int vec_per_row = d * elem / 16;
+  int blocks = (R + 7) / 8;  // 8 warps (rows) per block
+  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  if (blocks < 1) blocks = 1;
+  gather_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), T, vec_per_row, P.perm_tok, P.poffsets, E,
+                                       static_cast<uint4 *>(P.xperm), P.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_combine(void *y, int T, int d, int K, int S, int R, int dtype, unsigned flags, const Ptrs &P,
+                           int num_sms, cudaStream_t s) {
+  const long long total = static_cast<long long>(T) * (d / 4);
+  long long blocks = (total + 255) / 256;
+  if (blocks > num_sms * 16LL) blocks = num_sms * 16LL;
+  if (blocks < 1) blocks = 1;
+  const long long split_stride = static_cast<long long>(R) * d;
+  if (dtype == MOE_BF16)
+    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
+        static_cast<__nv_bfloat16 *>(y), T, d, K, S, split_stride, P.obuf, P.pos, R, flags, P.status);
+  else
+    combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<float *>(y), T, d, K, S,
+                                                                   split_stride, P.obuf, P.pos, R, flags, P.status);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate, int32_t *perm_tok,
+                                int32_t *offsets, int32_t *pos, cudaStream_t s) {
+  int blocks = (T * K + 255) / 256;
+  if (blocks < 1) blocks = 1;
+  if (blocks > 1024) blocks = 1024;
+  route_export_kernel<<<blocks, 256, 0, s>>>(T, E, K, P.idx, P.gate, P.pos, P.offsets, P.poffsets, idx, gate,
+                                             perm_tok, offsets, pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s) {
+  if (T == 0) return cudaSuccess;
+  if (dtype == MOE_BF16)
+    rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
+                                                     static_cast<__nv_bfloat16 *>(out), d, eps);
+  else
+    rmsnorm_kernel<float><<<T, 256, 0, s>>>(static_cast<const float *>(x), static_cast<float *>(out), d, eps);
+  return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -1,0 +1,120 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/moe.h declares, sizes workspaces, and rejects bad
+arguments before touching the device."""
+from __future__ import annotations
+
+import ctypes
+import pathlib
+import re
+
+import pytest
+
+from sparse_mixture_experts_55_b300 import _lib
+
+ROOT = pathlib.Path(__file__).resolve().parents[1]
+
+
+def _header_functions():
+    text = (ROOT / "include" / "moe.h").read_text()
+    return sorted(set(re.findall(r"^MOE_API\s+[\w\s\*]*?\b(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from sparse_mixture_experts_55_b300 import build
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_the_boundary():
+    names = _header_functions()
+    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_route", "moe_rmsnorm",
+                            "moe_read_status", "moe_status_string", "moe_version"])
+
+
+def test_exports_every_declared_symbol(lib):
+    for name in _header_functions():
+        assert hasattr(lib, name), name
+        assert name in _lib.SIGNATURES, name
+
+
+def test_status_strings_and_version(lib):
+    assert lib.moe_version() >= 100
+    for code in range(8):
+        assert lib.moe_status_string(code).decode() not in ("", "unknown status")
+    assert lib.moe_status_string(99).decode() == "unknown status"
+
+
+def test_workspace_bytes(lib):
+    mix = lib.moe_workspace_bytes(4096, 4096, 14336, 8, 2, _lib.MOE_BF16)
+    # grouped rows: 8192 tokens*slots + 8 * 127 pad rows, rounded to 128 -> 9216
+    R = 9216
+    lower = R * 4096 * 2 + R * 14336 * 2 + R * 4096 * 4
+    assert lower <= mix <= lower + 2 * 1024 * 1024
+    assert lib.moe_workspace_bytes(0, 64, 128, 8, 2, _lib.MOE_F32) > 0
+    # invalid shapes -> 0
+    assert lib.moe_workspace_bytes(16, 60, 128, 8, 2, _lib.MOE_BF16) == 0   # d not a multiple of 8
+    assert lib.moe_workspace_bytes(16, 64, 128, 8, 3, _lib.MOE_BF16) == 0   # K > 2
+    assert lib.moe_workspace_bytes(16, 64, 128, 1, 2, _lib.MOE_BF16) == 0   # K > E
+    assert lib.moe_workspace_bytes(16, 64, 128, 33, 2, _lib.MOE_BF16) == 0  # E > 32
+    assert lib.moe_workspace_bytes(16, 64, 128, 8, 2, 7) == 0               # dtype
+    assert lib.moe_workspace_bytes(-1, 64, 128, 8, 2, 0) == 0
+
+
+def _fwd(lib, **kw):
+    a = dict(x=0x1000, Wg=0x2000, W1=0x3000, W3=0x4000, W2=0x5000, y=0x100000, T=16, d=64, f=128, E=8, K=2,
+             dtype=_lib.MOE_BF16, ws=0x200000, ws_bytes=1 << 40, flags=0, stream=0)
+    a.update(kw)
+    vp = ctypes.c_void_p
+    return lib.moe_forward(vp(a["x"]), vp(a["Wg"]), vp(a["W1"]), vp(a["W3"]), vp(a["W2"]), vp(a["y"]), a["T"],
+                           a["d"], a["f"], a["E"], a["K"], a["dtype"], vp(a["ws"]), a["ws_bytes"], a["flags"],
+                           vp(a["stream"]))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(K=3), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(K=0), _lib.MOE_ERR_INVALID_ARG),
+    (dict(E=1, K=2), _lib.MOE_ERR_INVALID_ARG),
+    (dict(E=40), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(d=60), _lib.MOE_ERR_INVALID_ARG),
+    (dict(f=130), _lib.MOE_ERR_INVALID_ARG),
+    (dict(T=-1), _lib.MOE_ERR_INVALID_ARG),
+    (dict(dtype=5), _lib.MOE_ERR_UNSUPPORTED),
+    (dict(x=0), _lib.MOE_ERR_INVALID_ARG),
+    (dict(W2=0), _lib.MOE_ERR_INVALID_ARG),
+    (dict(W1=0x3008), _lib.MOE_ERR_INVALID_ARG),                   # misaligned
+    (dict(y=0x1000 + 16 * 64 * 2 - 16), _lib.MOE_ERR_INVALID_ARG),  # y overlaps x
+    (dict(flags=0x80), _lib.MOE_ERR_INVALID_ARG),
+    (dict(ws=0), _lib.MOE_ERR_WORKSPACE),
+    (dict(ws=0x200008), _lib.MOE_ERR_WORKSPACE),
+    (dict(ws_bytes=1024), _lib.MOE_ERR_WORKSPACE),
+])
+def test_forward_rejects_bad_arguments_on_host(lib, kw, code):
+    # The pointers are never dereferenced: validation happens before any CUDA call.
+    assert _fwd(lib, **kw) == code
+
+
+def test_fp32_multiple_of_4_is_accepted_by_shape_check(lib):
+    # d = 60 is fine for fp32 (16-byte rows); with a 1-byte workspace the call
+    # stops at the workspace check, after the shape checks passed.
+    assert _fwd(lib, d=60, dtype=_lib.MOE_F32, ws_bytes=1) == _lib.MOE_ERR_WORKSPACE
+
+
+def test_route_and_rmsnorm_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    assert lib.moe_route(vp(0x1000), vp(0x2000), 16, 64, 8, 3, 0, vp(16), vp(16), vp(16), vp(16), vp(0),
+                         vp(0x200000), 1 << 40, vp(0)) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_route(vp(0x1000), vp(0x2000), 16, 64, 8, 2, 0, vp(0), vp(16), vp(16), vp(16), vp(0),
+                         vp(0x200000), 1 << 40, vp(0)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_rmsnorm(vp(0x1000), vp(0x1000), 4, 64, 0.0, 0, vp(0)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_rmsnorm(vp(0x1000), vp(0x1000), 4, 64, 1e-5, 9, vp(0)) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_rmsnorm(vp(0), vp(0), 0, 64, 1e-5, 0, vp(0)) == _lib.MOE_OK   # empty input: no-op
+    assert lib.moe_read_status(vp(0), vp(0)) == _lib.MOE_ERR_WORKSPACE
+
+
+def test_binding_has_no_fallback(monkeypatch, tmp_path):
+    """With the shared library missing the binding raises instead of computing anything."""
+    monkeypatch.setattr(_lib, "LIB_PATH", tmp_path / "libmoe.so")
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="missing"):
+        _lib.load()

@@ -1,0 +1,174 @@
+"""GPU parity against the float64 oracle at sizes the oracle finishes in
+seconds: several tiles per GEMM, ragged M/N/K tails, top-1 and top-2, 1 to 32
+experts, the decode split-K path, exact ties, and the edge cases (empty input,
+single token, accumulate into y).  All calls go through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_device):
+    from sparse_mixture_experts_55_b300 import build
+    build.build()
+    import sparse_mixture_experts_55_b300 as m
+    return m
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _run(moe, inp: W.MoEInputs, flags=0, y=None):
+    dev = torch.device("cuda:0")
+    g = inp.to(dev)
+    y_dev = None if y is None else y.to(dev).clone()
+    out = moe.moe_forward(g.x, g.Wg, g.W1, g.W3, g.W2, inp.K, y=y_dev, flags=flags)
+    idx, gate, perm, offs, pos = moe.moe_route(g.x, g.Wg, inp.K)
+    torch.cuda.synchronize()
+    return out, idx, gate, perm, offs, pos
+
+
+def _check_layer(moe, inp, tol_key, flags=0):
+    out, idx, gate, perm, offs, pos = _run(moe, inp, flags)
+    T, d, f, E, K = inp.shape
+    ref = oracle.moe_layer(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K)
+    rep = parity.check_routing(_np(idx), _np(gate), ref.gating, K)
+    assert rep.n_mismatch == 0, rep
+    parity.gate_invariants(_np(idx), _np(gate), E, K)
+    parity.check_grouping(_np(idx), _np(perm), _np(offs), _np(pos), E)
+    if rep.n_exempt_in_out == 0 and rep.n_set_compared == 0:
+        p = oracle.permutation(ref.gating.idx, E)
+        assert np.array_equal(_np(perm), p.perm_tok)
+    err = parity.rel_linf(_np(out.float()), ref.y)
+    assert err <= parity.TOL[tol_key], (err, rep)
+    return err, rep, out
+
+
+# ---------------------------------------------------------------- fp32 path
+def test_tiny_fp32(moe):
+    inp = W.tiny_fp32()
+    err, rep, _ = _check_layer(moe, inp, "f32")
+    dense = oracle.moe_layer_dense(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, inp.K)
+    out, *_ = _run(moe, inp)
+    assert parity.rel_linf(_np(out), dense.y) <= 1e-4
+
+
+@pytest.mark.parametrize("T,d,f,E,K", [(64, 64, 128, 1, 1), (200, 68, 132, 8, 2), (77, 32, 96, 5, 1),
+                                       (130, 64, 128, 32, 2), (1, 64, 128, 8, 2)])
+def test_fp32_shapes(moe, T, d, f, E, K):
+    inp = W.tiny_fp32(T=T, d=d, f=f, E=E, K=K, seed=7 + T)
+    _check_layer(moe, inp, "f32")
+
+
+def test_fp32_k1_e1_is_plain_swiglu(moe):
+    inp = W.tiny_fp32(E=1, K=1)
+    out, *_ = _run(moe, inp)
+    x = oracle.f64(inp.x)
+    want = (oracle.silu(x @ oracle.f64(inp.W1[0])) * (x @ oracle.f64(inp.W3[0]))) @ oracle.f64(inp.W2[0])
+    assert parity.rel_linf(_np(out), want) <= 1e-4
+
+
+# ---------------------------------------------------------------- bf16 tensor-core path
+def _bf16_inputs(T, d, f, E, K, seed):
+    Wg, W1, W3, W2 = W.mixtral_weights(d, f, E, seed=seed, device="cpu")
+    x = W.rms_rows(T, d, seed * 7 + 1, "cpu", torch.bfloat16)
+    return W.MoEInputs(x, Wg, W1, W3, W2, K, {"config": f"bf16-{T}x{d}x{f}x{E}x{K}"})
+
+
+@pytest.mark.parametrize("T,d,f,E,K", [
+    (1000, 512, 1024, 8, 2),    # 2 m-tiles per expert, 8/2 n-tiles, 8/16 k-blocks
+    (257, 520, 1032, 8, 2),     # ragged: N and K tails in both GEMMs
+    (600, 256, 512, 4, 1),      # top-1
+    (129, 256, 384, 32, 2),     # 32 experts, many empty segments
+    (33, 256, 256, 5, 2),       # 5 experts (scalar router path)
+    (1, 512, 1024, 8, 2),       # decode: one token, split-K down projection
+    (8, 512, 1024, 8, 2),
+    (128, 512, 1024, 8, 2),
+    (3000, 256, 256, 8, 2),     # 6 m-tiles per expert, many tiles per CTA
+])
+def test_bf16_shapes(moe, T, d, f, E, K):
+    inp = _bf16_inputs(T, d, f, E, K, seed=100 + T)
+    _check_layer(moe, inp, "bf16")
+
+
+def test_bf16_e1_k1_is_plain_swiglu(moe):
+    inp = _bf16_inputs(300, 256, 512, 1, 1, seed=3)
+    out, *_ = _run(moe, inp)
+    x = oracle.f64(inp.x)
+    want = (oracle.silu(x @ oracle.f64(inp.W1[0])) * (x @ oracle.f64(inp.W3[0]))) @ oracle.f64(inp.W2[0])
+    assert parity.rel_linf(_np(out.float()), want) <= 2e-2
+
+
+def test_bf16_deterministic(moe):
+    inp = _bf16_inputs(700, 512, 1024, 8, 2, seed=5)
+    a, ia, ga, pa, oa, sa = _run(moe, inp)
+    b, ib, gb, pb, ob, sb = _run(moe, inp)
+    assert torch.equal(a, b) and torch.equal(ia, ib) and torch.equal(ga, gb) and torch.equal(pa, pb)
+
+
+def test_accumulate_into_y(moe):
+    inp = _bf16_inputs(200, 256, 512, 8, 2, seed=9)
+    y0 = W.randn((200, 256), 0.5, 1234, "cpu", torch.bfloat16)
+    out, *_ = _run(moe, inp, flags=moe.MOE_ACCUMULATE, y=y0)
+    ref = oracle.moe_layer(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, 2).y + oracle.f64(y0)
+    assert parity.rel_linf(_np(out.float()), ref) <= 2e-2
+
+
+def test_empty_input(moe):
+    dev = torch.device("cuda:0")
+    inp = _bf16_inputs(4, 64, 128, 8, 2, seed=1).to(dev)
+    x0 = inp.x[:0]
+    y = moe.moe_forward(x0, inp.Wg, inp.W1, inp.W3, inp.W2, 2)
+    assert y.shape == (0, 64)
+    idx, gate, perm, offs, pos = moe.moe_route(x0, inp.Wg, 2)
+    torch.cuda.synchronize()
+    assert offs.tolist() == [0] * 9
+
+
+def test_exact_ties_pick_lower_index(moe):
+    inp = W.skew(T=2000, d=512, f=8, E=8, K=2, n_tie=80, weights=(None, None, None, None))
+    dev = torch.device("cuda:0")
+    idx, gate, perm, offs, pos = moe.moe_route(inp.x.to(dev), inp.Wg.to(dev), 2)
+    idx = _np(idx)
+    gate = _np(gate)
+    for t, pat in zip(inp.meta["tie_tokens"], inp.meta["tie_patterns"]):
+        assert tuple(idx[t].tolist()) == W.TIE_EXPECTED[pat]
+    ref = oracle.gating(inp.x, inp.Wg, 2)
+    rep = parity.check_routing(idx, gate, ref, 2)
+    assert rep.n_mismatch == 0
+    parity.check_grouping(idx, _np(perm), _np(offs), _np(pos), 8)
+    shares = np.bincount(idx.ravel(), minlength=8) / idx.size
+    assert shares[0] > 0.3 and shares[7] < 0.08
+
+
+def test_rmsnorm(moe):
+    dev = torch.device("cuda:0")
+    for dt, tol in ((torch.bfloat16, 2 ** -7), (torch.float32, 1e-6)):
+        h = W.randn((33, 4096), 3.0, 77, "cpu", dt)
+        out = moe.moe_rmsnorm(h.to(dev))
+        ref = oracle.rmsnorm(h)
+        assert np.abs(_np(out.float()) - ref).max() <= tol * np.abs(ref).max()
+        hh = h.to(dev)
+        moe.moe_rmsnorm(hh, out=hh)   # in place
+        assert torch.equal(hh, out)
+
+
+def test_debug_checks_report_nonfinite_router_input(moe):
+    dev = torch.device("cuda:0")
+    inp = _bf16_inputs(64, 256, 256, 8, 2, seed=11).to(dev)
+    x = inp.x.clone()
+    x[5, 3] = float("nan")
+    ws = moe.Workspace(64, 256, 256, 8, 2, torch.bfloat16, dev)
+    moe.moe_forward(x, inp.Wg, inp.W1, inp.W3, inp.W2, 2, workspace=ws, flags=moe.MOE_DEBUG_CHECKS)
+    assert moe.moe_read_status(ws) == 6  # MOE_ERR_NONFINITE
+    moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, 2, workspace=ws, flags=moe.MOE_DEBUG_CHECKS)
+    assert moe.moe_read_status(ws) == 0
