@@ -1,0 +1,436 @@
+"""Benchmark of the MoE layer forward on B300: one JSON line on rank 0.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill] [--impl ours|reference]
+
+A step is one full forward pass of the layer (router, grouping, gather,
+gate/up GEMM + SwiGLU, down GEMM x gate, combine) over one batch of seeded
+synthetic tokens, with random-init Mixtral-shaped weights resident in HBM.
+
+  value        tokens/s over all ranks (each rank runs its own replica of the
+               layer on its own batch; no data-path collective), device-timed
+               with CUDA events around K steps, max over ranks
+  e2e          the same metric through the C ABI with host buffers: pinned x
+               copied in, the layer, y copied out, every step
+  roofline     the gate/up expert GEMM (the dominant kernel): algorithmic
+               FLOPs (or bytes at decode sizes) per launch over its average
+               launch time, measured by events recorded around it in the
+               timed region, against MEASURED_PEAKS.json
+  cpu_baseline the float64 oracle on a token sample, timed on the host cores
+  --impl reference   the oracle alone, timed on the host cores (rank 0)
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import pathlib
+import re
+import statistics
+import sys
+import threading
+import time
+
+ROOT = pathlib.Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+import torch  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "MoE layer tokens/s and TFLOP/s (% bf16 peak; % HBM BW at decode) on 1 B300"
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0}
+
+CONFIGS = {
+    "prefill": dict(T=4096, d=4096, f=14336, E=8, K=2),
+    "decode1": dict(T=1, d=4096, f=14336, E=8, K=2),
+    "decode8": dict(T=8, d=4096, f=14336, E=8, K=2),
+    "decode32": dict(T=32, d=4096, f=14336, E=8, K=2),
+    "decode128": dict(T=128, d=4096, f=14336, E=8, K=2),
+    "skew": dict(T=16384, d=4096, f=14336, E=8, K=2),
+    # profiling stand-in: two experts of Mixtral size with ~1024 rows each, the
+    # per-expert GEMM shape of the prefill layer at a quarter of its memory
+    "prefill_e2": dict(T=1024, d=4096, f=14336, E=2, K=2),
+}
+WORKLOAD_TEXT = {
+    "prefill": "Mixtral-shaped MoE layer prefill: T=4096 tokens, d=4096, f=14336, E=8 experts, top-2, bf16, "
+               "fp32 accumulate",
+    "skew": "skewed-routing MoE layer: T=16384, d=4096, f=14336, E=8, top-2, Zipf(1.2) expert loads, bf16",
+}
+WORKLOAD_TEXT["prefill_e2"] = "profiling stand-in: T=1024 tokens, d=4096, f=14336, E=2 experts, top-2, bf16"
+for _t in (1, 8, 32, 128):
+    WORKLOAD_TEXT[f"decode{_t}"] = f"Mixtral-shaped MoE layer decode batch: T={_t} tokens, d=4096, f=14336, " \
+                                   f"E=8, top-2, bf16 (weight-streaming)"
+
+
+# ---------------------------------------------------------------------------
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        try:
+            d = json.loads(p.read_text())
+            return {k: float(d[k]) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained")}, "measured"
+        except Exception:
+            pass
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def traffic_from_profiles(kernel_file: pathlib.Path, key: str):
+    """dram bytes per launch recorded by an ncu capture, if the kernel source is unchanged since."""
+    prof = ROOT / "profiles" / "gate_up_gemm_traffic.md"
+    if not prof.exists():
+        return None
+    text = prof.read_text()
+    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_val = re.search(rf"{key}:\s*([0-9.eE+]+)", text)
+    if not m_sha or not m_val:
+        return None
+    sha = hashlib.sha256(kernel_file.read_bytes()).hexdigest()
+    return float(m_val.group(1)) if sha == m_sha.group(1) else None
+
+
+class ClockSampler:
+    """Samples SM clock, power and clock-event reasons through NVML while running."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown", 0x2: "applications_clocks_setting",
+               0x10: "sync_boost"}
+
+    def __init__(self, device_index: int, period_s: float = 0.005):
+        self.samples = []
+        self.reasons = set()
+        self.ok = False
+        self.max_mhz = None
+        self._stop = threading.Event()
+        self.period = period_s
+        try:
+            import pynvml
+            self.nv = pynvml
+            pynvml.nvmlInit()
+            h = None
+            try:
+                uuid = str(torch.cuda.get_device_properties(device_index).uuid)
+                h = pynvml.nvmlDeviceGetHandleByUUID(("GPU-" + uuid) if not uuid.startswith("GPU-") else uuid)
+            except Exception:
+                h = None
+            if h is None:
+                vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+                idx = int(vis.split(",")[device_index]) if vis and vis.split(",")[0].isdigit() else device_index
+                h = pynvml.nvmlDeviceGetHandleByIndex(idx)
+            self.h = h
+            self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(h, pynvml.NVML_CLOCK_SM)
+            self._reasons_fn = getattr(pynvml, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                getattr(pynvml, "nvmlDeviceGetCurrentClocksThrottleReasons")
+            self.ok = True
+        except Exception as e:  # NVML unavailable: report no clocks rather than guess
+            self.err = repr(e)
+        self._t = threading.Thread(target=self._run, daemon=True)
+
+    def _run(self):
+        while not self._stop.is_set():
+            try:
+                sm = self.nv.nvmlDeviceGetClockInfo(self.h, self.nv.NVML_CLOCK_SM)
+                r = self._reasons_fn(self.h)
+                pw = self.nv.nvmlDeviceGetPowerUsage(self.h) / 1000.0
+                self.samples.append((sm, pw))
+                for bit, name in self.REASONS.items():
+                    if r & bit:
+                        self.reasons.add(name)
+            except Exception:
+                pass
+            time.sleep(self.period)
+
+    def __enter__(self):
+        if self.ok:
+            self._t.start()
+        return self
+
+    def __exit__(self, *a):
+        self._stop.set()
+        if self.ok:
+            self._t.join()
+
+    def summary(self):
+        if not self.ok or not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": [], "samples": 0,
+                    "note": getattr(self, "err", "no samples")}
+        sms = [s for s, _ in self.samples]
+        return {"sm_mhz": statistics.median(sms), "sm_max_mhz": self.max_mhz, "reasons": sorted(self.reasons),
+                "samples": len(sms), "power_w_max": round(max(p for _, p in self.samples), 1)}
+
+
+# ---------------------------------------------------------------------------
+def setup_dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(v: float, world: int, dev) -> float:
+    if world == 1:
+        return v
+    import torch.distributed as dist
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def make_inputs(cfg_name: str, rank: int, dev, weights=None):
+    c = CONFIGS[cfg_name]
+    seed = W.BASE_SEED + 1009 * rank     # replicas: own tokens per rank (same model weights)
+    if weights is None:
+        weights = W.mixtral_weights(c["d"], c["f"], c["E"], seed=W.BASE_SEED, device=dev)
+    if cfg_name in ("prefill", "prefill_e2"):
+        return W.prefill(T=c["T"], seed=seed, device=dev, weights=weights), weights
+    if cfg_name.startswith("decode"):
+        return W.decode(c["T"], seed=seed, device=dev, weights=weights), weights
+    if cfg_name == "skew":
+        return W.skew(T=c["T"], seed=seed, device=dev, weights=weights), weights
+    raise ValueError(cfg_name)
+
+
+def algorithmic(c, n_touched):
+    T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
+    flops = T * K * 6 * d * f + 2 * T * d * E
+    gate_up_flops = T * K * 4 * d * f
+    bytes_step = n_touched * 3 * d * f * 2 + 2 * d * E + 2 * T * d * 2
+    gate_up_bytes = n_touched * 2 * d * f * 2
+    return flops, gate_up_flops, bytes_step, gate_up_bytes
+
+
+# ---------------------------------------------------------------------------
+def f64_banks(inp):
+    """Host float64 copies of the router and expert banks, filled one expert at a time."""
+    import numpy as np
+    E, d, f = inp.W1.shape
+    Wg = inp.Wg.float().cpu().numpy().astype(np.float64)
+    W1 = np.empty((E, d, f)); W3 = np.empty((E, d, f)); W2 = np.empty((E, f, d))
+    for e in range(E):
+        W1[e] = inp.W1[e].float().cpu().numpy()
+        W3[e] = inp.W3[e].float().cpu().numpy()
+        W2[e] = inp.W2[e].float().cpu().numpy()
+    return Wg, W1, W3, W2
+
+
+def blas_threads() -> int:
+    """Threads the oracle's BLAS runs with (threadpoolctl if present, else the CPU affinity set)."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i.get("num_threads", 1) for i in threadpool_info() if i.get("internal_api") == "openblas"]
+        if n:
+            return max(n)
+    except Exception:
+        pass
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        if os.environ.get(var, "").isdigit():
+            return int(os.environ[var])
+    return len(os.sched_getaffinity(0))
+
+
+def cpu_oracle_rate(inp, n_tokens: int):
+    """Time the unchanged float64 oracle on the first n_tokens tokens of the batch.
+    Weights are copied to the host and upcast once, before timing."""
+    import numpy as np
+    import oracle
+    x = inp.x[:n_tokens].float().cpu().numpy().astype(np.float64)
+    Wg, W1, W3, W2 = f64_banks(inp)
+    t0 = time.perf_counter()
+    oracle.moe_layer(x, Wg, W1, W3, W2, inp.K)
+    dt = time.perf_counter() - t0
+    return n_tokens / dt, dt, blas_threads()
+
+
+def run_reference(args, world, rank):
+    """The oracle as the reference arm: host cores only, bounded sample per step."""
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    c = CONFIGS[args.config]
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    inp, _ = make_inputs(args.config, 0, dev)
+    steps, warmup = args.steps, max(args.warmup, 3)
+    # sample per step: bounded so the whole run stays within a few minutes
+    per_step_budget_s = min(2.0, 150.0 / (steps + warmup))
+    n_tok = max(1, min(c["T"], int(per_step_budget_s / 0.02)))
+    x = inp.x.float().cpu().numpy().astype(np.float64)
+    Wg, W1, W3, W2 = f64_banks(inp)
+    del inp
+    times = []
+    for i in range(warmup + steps):
+        lo = (i * n_tok) % max(1, c["T"] - n_tok + 1)
+        t0 = time.perf_counter()
+        oracle.moe_layer(x[lo:lo + n_tok], Wg, W1, W3, W2, c["K"])
+        dt = time.perf_counter() - t0
+        if i >= warmup:
+            times.append(dt)
+    ms = 1e3 * sum(times) / len(times)
+    value = n_tok / (ms / 1e3)
+    threads = blas_threads()
+    sample = f"{n_tok} tokens of the {args.config} batch per step (weights upcast to float64 once, untimed)"
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+            "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.config], **c},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+def run_ours(args, world, rank, local):
+    import sparse_mixture_experts_55_b300 as moe
+    from sparse_mixture_experts_55_b300 import build as _build
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    c = CONFIGS[args.config]
+    T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
+    inp, weights = make_inputs(args.config, rank, dev)
+    ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
+    y = torch.empty_like(inp.x)
+    stream = torch.cuda.current_stream(dev)
+    steps, warmup = args.steps, max(args.warmup, 3)
+
+    # touched experts of this routing (algorithmic bytes at decode sizes)
+    _, _, _, offs, _ = moe.moe_route(inp.x, inp.Wg, K)
+    counts = (offs[1:] - offs[:-1]).cpu()
+    n_touched = int((counts > 0).sum())
+
+    def new_events(n):
+        return [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+
+    wev = new_events(1)[0]
+    for _ in range(warmup):
+        moe.moe_forward_timed(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, wev, y=y, workspace=ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    if moe.moe_read_status(ws) != 0:
+        raise RuntimeError(f"device status {moe.moe_read_status(ws)}")
+
+    evs = new_events(steps)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for i in range(steps):
+            moe.moe_forward_timed(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, evs[i], y=y, workspace=ws,
+                                  stream=stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms_local = start.elapsed_time(end) / steps
+    ms = max_over_ranks(ms_local, world, dev)
+    stage_ms = {}
+    for j, name in enumerate(("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")):
+        stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+    if moe.moe_read_status(ws) != 0:
+        raise RuntimeError("device status set during timed run")
+
+    # end to end through the C ABI with host buffers
+    e2e_steps = max(3, min(steps, 20))
+    x_host = inp.x.cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    x_dev = torch.empty_like(inp.x)
+    for _ in range(2):
+        moe.moe_forward_host(x_host, y_host, inp.Wg, inp.W1, inp.W3, inp.W2, K, x_dev=x_dev, y_dev=y, workspace=ws,
+                             stream=stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        moe.moe_forward_host(x_host, y_host, inp.Wg, inp.W1, inp.W3, inp.W2, K, x_dev=x_dev, y_dev=y, workspace=ws,
+                             stream=stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, dev)
+
+    peaks, peak_src = load_peaks()
+    flops, gu_flops, bytes_step, gu_bytes = algorithmic(c, n_touched)
+    tokens_per_s = world * T / (ms / 1e3)
+    gu_ms = stage_ms["gate_up_gemm"]
+    hbm_bound = args.config.startswith("decode")
+    kernel_file = ROOT / "sparse_mixture_experts_55_b300" / "csrc" / "gemm_tc.cu"
+    if hbm_bound:
+        achieved = gu_bytes / (gu_ms / 1e3) / 1e9
+        roof = {"kernel": "gate_up_gemm", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
+                "traffic": traffic_from_profiles(kernel_file, f"{args.config}_traffic_bytes_per_launch"),
+                "algorithmic_bytes_per_launch": gu_bytes, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
+    else:
+        achieved = gu_flops / (gu_ms / 1e3) / 1e12
+        roof = {"kernel": "gate_up_gemm", "bound": "tensor", "achieved": achieved,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": achieved / peaks["bf16_tflops_sustained"],
+                "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "traffic": traffic_from_profiles(kernel_file, f"{args.config}_traffic_bytes_per_launch"),
+                "algorithmic_flops_per_launch": gu_flops,
+                "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peak_src}; kernel timed inside a "
+                               f"long run of steps)"}
+    line = {
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step" % (
+                       n_touched * 3 * d * f * 2 / 1e9), "touched_experts": n_touched},
+        "tflops": flops / (ms / 1e3) / 1e12 * world,
+        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "hbm_gbs_algorithmic": bytes_step / (ms / 1e3) / 1e9,
+        "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "roofline": roof,
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
+                "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
+        "gpu_launches": 6 * steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        n_tok = min(T, args.cpu_tokens)
+        rate, dt, threads = cpu_oracle_rate(inp, n_tok)
+        line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
+                                "sample": f"first {n_tok} tokens of the batch, float64 oracle ({dt:.1f} s; "
+                                          f"weights upcast once, untimed)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--config", default="prefill", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    world, rank, local = setup_dist()
+    try:
+        if args.impl == "reference":
+            run_reference(args, world, rank)
+        else:
+            run_ours(args, world, rank, local)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

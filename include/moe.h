@@ -116,6 +116,24 @@ MOE_API int moe_forward(const void *x, const void *Wg, const void *W1, const voi
                 void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
 
 /*
+ * moe_forward with per-stage timing: the same work and the same results, and
+ * in addition records caller-created CUDA events on `stream` at the stage
+ * boundaries, for kernel durations measured inside a timed run.
+ *   events: HOST array of MOE_NUM_STAGE_EVENTS cudaEvent_t handles (as void*),
+ *           none NULL, created by the caller (with timing enabled for
+ *           cudaEventElapsedTime).  events[0] is recorded before the router
+ *           and events[i] after stage i: 1 router, 2 grouping, 3 row gather,
+ *           4 gate/up expert GEMM (+SwiGLU), 5 down expert GEMM (x gate),
+ *           6 two-slot combine.  With T = 0 no event is recorded.
+ * Returns MOE_ERR_INVALID_ARG if events or one of its entries is NULL.
+ */
+#define MOE_NUM_STAGE_EVENTS 7
+MOE_API int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+                      void *y, int T, int d, int f, int E, int K, int dtype,
+                      void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                      void *const *events);
+
+/*
  * Routing only, for inspection: the router and grouping kernels that
  * moe_forward runs, with their results copied out in unpadded form
  * (section 3.4 gating function; "Top-K Gating Mechanism and Routing").

@@ -21,7 +21,7 @@ from . import _lib
 from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_F32, MoEError,  # noqa: F401
                    status_string)
 
-__all__ = ["moe_forward", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+__all__ = ["moe_forward", "moe_forward_timed", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
 
@@ -99,6 +99,34 @@ def moe_forward(x, Wg, W1, W3, W2, K: int = 2, y=None, workspace: Workspace | No
                                  _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
                                  _stream_ptr(stream, dev))
     _lib.check("moe_forward", rc)
+    return y
+
+
+def moe_forward_timed(x, Wg, W1, W3, W2, K: int, events, y=None, workspace: Workspace | None = None,
+                      flags: int = 0, stream=None):
+    """moe_forward that also records the seven torch.cuda.Event objects in
+    ``events`` at the stage boundaries (before the router, then after router,
+    grouping, gather, gate/up GEMM, down GEMM and combine)."""
+    if len(events) != _lib.MOE_NUM_STAGE_EVENTS:
+        raise ValueError(f"need {_lib.MOE_NUM_STAGE_EVENTS} events")
+    dev = x.device
+    s = stream if stream is not None else torch.cuda.current_stream(dev)
+    handles = []
+    for ev in events:
+        if ev.cuda_event == 0:      # torch creates the CUDA event on first record
+            ev.record(s)
+        handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    T, d = x.shape
+    E, _, f = W1.shape
+    if y is None:
+        y = torch.empty_like(x)
+    if workspace is None:
+        workspace = Workspace(T, d, f, E, K, x.dtype, dev)
+    rc = _lib.load().moe_forward_timed(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(y), T, d, f, E, K,
+                                       _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
+                                       ctypes.c_void_p(s.cuda_stream), arr)
+    _lib.check("moe_forward_timed", rc)
     return y
 
 

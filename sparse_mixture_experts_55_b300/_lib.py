@@ -25,6 +25,8 @@ MOE_BF16 = 0
 MOE_F32 = 1
 
 MOE_ACCUMULATE = 0x1
+MOE_NUM_STAGE_EVENTS = 7
+STAGES = ("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")
 MOE_DEBUG_CHECKS = 0x2
 
 # name -> (restype, argtypes), one entry per function declared in include/moe.h
@@ -32,6 +34,7 @@ _vp, _i, _sz, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
 SIGNATURES = {
     "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
+    "moe_forward_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp, _vp]),
     "moe_route": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_rmsnorm": (_i, [_vp, _vp, _i, _i, ctypes.c_float, _i, _vp]),
     "moe_read_status": (_i, [_vp, _vp]),

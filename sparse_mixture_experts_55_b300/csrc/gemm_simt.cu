@@ -86,12 +86,13 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float *__restrict__ 
 }  // namespace
 
 cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,
-                                  const WsLayout &L, const Ptrs &P, cudaStream_t s) {
+                                  const WsLayout &L, const Ptrs &P, cudaStream_t s, void *const *mid_event) {
   const dim3 g1((f + TN - 1) / TN, L.R / TM);
   ffn_f32_kernel<true><<<g1, 256, 0, s>>>(static_cast<const float *>(P.xperm), static_cast<const float *>(W1),
                                           static_cast<const float *>(W3), d, f, P.poffsets, E, P.perm_gate,
                                           static_cast<float *>(P.hbuf));
   cudaError_t err = cudaGetLastError();
+  if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
   const dim3 g2((d + TN - 1) / TN, L.R / TM);
   ffn_f32_kernel<false><<<g2, 256, 0, s>>>(static_cast<const float *>(P.hbuf), static_cast<const float *>(W2),

@@ -431,7 +431,7 @@ cudaError_t set_smem_attrs() {
 
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
-                                     cudaStream_t s) {
+                                     cudaStream_t s, void *const *mid_event) {
   (void)flags;
   cudaError_t err = set_smem_attrs();
   if (err != cudaSuccess) return err;
@@ -455,6 +455,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.status = P.status;
   expert_gemm_kernel<MODE_GATE_UP><<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w1, tm_w3, g1);
   err = cudaGetLastError();
+  if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;

@@ -61,12 +61,13 @@ cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx
 cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s);
 
 // -------- gemm_tc.cu (bf16 tensor-core path)
+// mid_event (optional): recorded between the gate/up and the down kernel.
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
-                                     cudaStream_t s);
+                                     cudaStream_t s, void *const *mid_event);
 
 // -------- gemm_simt.cu (exact fp32 path)
 cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,
-                                  const WsLayout &L, const Ptrs &P, cudaStream_t s);
+                                  const WsLayout &L, const Ptrs &P, cudaStream_t s, void *const *mid_event);
 
 }  // namespace moe

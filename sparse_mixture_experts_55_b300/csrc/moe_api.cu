@@ -159,9 +159,9 @@ size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
   return ws_layout(T, d, f, E, K, dtype, sm_count_or_default()).total;
 }
 
-int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y, int T,
-                int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes, unsigned flags,
-                moe_stream_t stream) {
+static int forward_impl(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
+                        int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
+                        unsigned flags, moe_stream_t stream, void *const *events) {
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
   if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS)) return MOE_ERR_INVALID_ARG;
@@ -181,17 +181,42 @@ int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, c
   const Ptrs P = carve(workspace, L);
   if (cudaMemsetAsync(P.status, 0, kStatusInts * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, flags, P, s);
+  // events (optional): one before the router and one after each of the six stages
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  cudaError_t err = mark(0);
+  if (err == cudaSuccess) err = launch_route(x, Wg, T, d, E, K, dtype, flags, P, s);
+  if (err == cudaSuccess) err = mark(1);
   if (err == cudaSuccess) err = launch_group(T, E, K, L.n_route_blocks, flags, P, s);
+  if (err == cudaSuccess) err = mark(2);
   if (err == cudaSuccess) err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
+  if (err == cudaSuccess) err = mark(3);
   if (err == cudaSuccess) {
     if (dtype == MOE_BF16)
-      err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, flags, sms, s);
+      err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, flags, sms, s, events ? events + 4 : nullptr);
     else
-      err = launch_expert_ffn_f32(W1, W3, W2, d, f, E, L, P, s);
+      err = launch_expert_ffn_f32(W1, W3, W2, d, f, E, L, P, s, events ? events + 4 : nullptr);
   }
+  if (err == cudaSuccess) err = mark(5);
   if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, L.R, dtype, flags, P, sms, s);
+  if (err == cudaSuccess) err = mark(6);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y, int T,
+                int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes, unsigned flags,
+                moe_stream_t stream) {
+  return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, nullptr);
+}
+
+int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
+                      int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
+                      unsigned flags, moe_stream_t stream, void *const *events) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, events);
 }
 
 int moe_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, int32_t *idx, float *gate,

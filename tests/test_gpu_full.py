@@ -1,0 +1,84 @@
+"""Parity at the full Mixtral sizes, in the launch configuration bench.py
+times: routing and grouping on every token (bit-exact, near-ties reported),
+layer outputs on a seeded sample of tokens (the oracle evaluates each token
+on its own, so a sample is the full layer restricted to those rows)."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_device):
+    from sparse_mixture_experts_55_b300 import build
+    build.build()
+    import sparse_mixture_experts_55_b300 as m
+    return m
+
+
+@pytest.fixture(scope="module")
+def mixtral(cuda_device):
+    return W.mixtral_weights(device=cuda_device)
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+def _run_and_check(moe, inp: W.MoEInputs, sample, extra_tokens=()):
+    T, d, f, E, K = inp.shape
+    ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, inp.x.device)
+    y = moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, workspace=ws)
+    assert moe.moe_read_status(ws) == 0
+    idx, gate, perm, offs, pos = moe.moe_route(inp.x, inp.Wg, K)
+    x_cpu = inp.x.cpu()
+    Wg_cpu = inp.Wg.cpu()
+    g = oracle.gating(x_cpu, Wg_cpu, K)
+    rep = parity.check_routing(_np(idx), _np(gate), g, K)
+    assert rep.n_mismatch == 0, rep
+    parity.gate_invariants(_np(idx), _np(gate), E, K)
+    parity.check_grouping(_np(idx), _np(perm), _np(offs), _np(pos), E)
+    if rep.n_exempt_in_out == 0 and rep.n_set_compared == 0:
+        assert np.array_equal(_np(perm), oracle.permutation(g.idx, E).perm_tok)
+    rng = np.random.default_rng(1234)
+    toks = np.unique(np.concatenate([rng.choice(T, size=min(sample, T), replace=False),
+                                     np.asarray(extra_tokens, dtype=np.int64)])).astype(np.int64)
+    ref = oracle.moe_layer_tokens(x_cpu, Wg_cpu, inp.W1, inp.W3, inp.W2, K, toks)
+    err = parity.rel_linf(_np(y.float())[toks], ref.y)
+    print(f"\n{inp.meta['config']}: T={T} rel_linf={err:.3e} on {toks.size} tokens; routing {rep}")
+    assert err <= parity.TOL["bf16"], err
+    # the same call again is bitwise identical
+    y2 = moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, workspace=ws)
+    assert torch.equal(y, y2)
+    return idx, rep
+
+
+def test_prefill_full(moe, mixtral, cuda_device):
+    inp = W.prefill(device=cuda_device, weights=mixtral)
+    _run_and_check(moe, inp, sample=48)
+
+
+@pytest.mark.parametrize("T", [1, 8, 32, 128])
+def test_decode_full(moe, mixtral, cuda_device, T):
+    inp = W.decode(T, device=cuda_device, weights=mixtral)
+    _run_and_check(moe, inp, sample=T)
+
+
+def test_skew_full(moe, mixtral, cuda_device):
+    inp = W.skew(device=cuda_device, weights=mixtral)
+    ties = inp.meta["tie_tokens"]
+    idx, rep = _run_and_check(moe, inp, sample=24, extra_tokens=ties[:8])
+    idx = _np(idx)
+    for t, pat in zip(ties, inp.meta["tie_patterns"]):
+        assert tuple(idx[t].tolist()) == W.TIE_EXPECTED[pat]
+    shares = np.bincount(idx.ravel(), minlength=8) / idx.size
+    target = np.array(W.zipf_shares(8))
+    print("skew shares", np.round(shares, 4).tolist(), "target", np.round(target, 4).tolist())
+    assert np.abs(shares - target).max() < 0.02
