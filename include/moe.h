@@ -153,6 +153,29 @@ MOE_API int moe_route(const void *x, const void *Wg, int T, int d, int E, int K,
               void *workspace, size_t ws_bytes, moe_stream_t stream);
 
 /*
+ * moe_route without a workspace, for callers that cannot allocate device
+ * memory: plugin hosts that give a kernel no scratch buffer, code running
+ * while another thread captures a CUDA graph in global mode (cudaMalloc is
+ * not allowed then), or serving loops that must not risk an allocation on
+ * their hot path.  The pages have no counterpart; this is a convenience of
+ * the library.
+ *
+ * Same arguments, outputs and results as moe_route, minus the workspace.  The
+ * scratch is a fixed array of 768 KiB compiled into the library: every GPU
+ * that loads libmoe.so reserves it until the process exits, and all calls on
+ * a GPU share it, so calls that overlap on the GPU (different streams or
+ * host threads) race and must be serialised by the caller.  The first call on
+ * each device looks up the array's device address (cudaGetSymbolAddress, with
+ * that device current); make that first call before any stream capture.
+ * Limits: T <= MOE_ROUTE_NOALLOC_MAX_T, K <= 2, E <= 32; a larger T returns
+ * MOE_ERR_UNSUPPORTED without launching.  Allocates nothing.
+ */
+#define MOE_ROUTE_NOALLOC_MAX_T 16384
+MOE_API int moe_route_noalloc(const void *x, const void *Wg, int T, int d, int E, int K, int dtype,
+                      int32_t *idx, float *gate, int32_t *perm_tok, int32_t *offsets, int32_t *pos,
+                      moe_stream_t stream);
+
+/*
  * RMSNorm with unit gain, out = x / sqrt(mean(x^2) + eps) per row, fp32 math
  * (pre-norm before each MoE block; paper-graph-ui summary, "Architectural
  * Inheritance from Mistral 7B", layer normalisation).  x, out: [T, d] of

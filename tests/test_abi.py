@@ -28,7 +28,8 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _header_functions()
-    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_route", "moe_rmsnorm",
+    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_route",
+                            "moe_route_noalloc", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
 

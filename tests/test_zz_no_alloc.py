@@ -1,0 +1,64 @@
+"""moe_route_noalloc: routing for callers that cannot allocate device memory.
+
+Plugin hosts without a scratch buffer, code running during a global-mode
+graph capture, and allocation-free serving loops cannot pass the library a
+workspace.  moe_route_noalloc serves them from a fixed scratch array inside
+the library.  This test calls it through the C ABI twice in a row (different
+sizes, so the second call runs on the first call's leftovers) and checks that
+its results equal moe_route's bit for bit; it also checks the size limit.
+The file is named so that pytest collects it last.
+"""
+from __future__ import annotations
+
+import ctypes
+
+import pytest
+import torch
+
+import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+def _call_noalloc(lib, x, Wg, K):
+    T, d = x.shape
+    E = Wg.shape[1]
+    dev = x.device
+    idx = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    gate = torch.full((T, K), -7.0, dtype=torch.float32, device=dev)
+    perm = torch.full((T * K,), -7, dtype=torch.int32, device=dev)
+    offs = torch.full((E + 1,), -7, dtype=torch.int32, device=dev)
+    pos = torch.full((T, K), -7, dtype=torch.int32, device=dev)
+    vp = ctypes.c_void_p
+    rc = lib.moe_route_noalloc(vp(x.data_ptr()), vp(Wg.data_ptr()), T, d, E, K, 0 if x.dtype == torch.bfloat16 else 1,
+                               vp(idx.data_ptr()), vp(gate.data_ptr()), vp(perm.data_ptr()), vp(offs.data_ptr()),
+                               vp(pos.data_ptr()), vp(torch.cuda.current_stream(dev).cuda_stream))
+    return rc, (idx, gate, perm, offs, pos)
+
+
+def test_route_noalloc_matches_route_on_consecutive_calls(cuda_device):
+    from sparse_mixture_experts_55_b300 import _lib, build
+    build.build()
+    import sparse_mixture_experts_55_b300 as moe
+    lib = _lib.load()
+    dev = cuda_device
+    cases = [
+        (2000, 4096, 8, 2, torch.bfloat16, 21),
+        (16384, 4096, 8, 2, torch.bfloat16, 22),   # the size limit, after a smaller call
+        (300, 512, 32, 1, torch.float32, 23),
+    ]
+    for T, d, E, K, dt, seed in cases:
+        x = W.rms_rows(T, d, seed, "cpu", dt).to(dev)
+        Wg = W.randn((d, E), d ** -0.5, seed + 100, "cpu", dt).to(dev)
+        rc, got = _call_noalloc(lib, x, Wg, K)
+        assert rc == 0, _lib.status_string(rc)
+        want = moe.moe_route(x, Wg, K)
+        torch.cuda.synchronize(dev)
+        for name, a, b in zip(("idx", "gate", "perm_tok", "offsets", "pos"), got, want):
+            assert torch.equal(a, b), f"{name} differs at T={T} E={E} K={K}"
+    # beyond the fixed scratch: rejected before anything is launched
+    T = 16385
+    x = torch.zeros((T, 64), dtype=torch.bfloat16, device=dev)
+    Wg = torch.zeros((64, 8), dtype=torch.bfloat16, device=dev)
+    rc, _ = _call_noalloc(lib, x, Wg, 2)
+    assert rc == _lib.MOE_ERR_UNSUPPORTED
