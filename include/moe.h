@@ -161,7 +161,7 @@ MOE_API int moe_route(const void *x, const void *Wg, int T, int d, int E, int K,
  * the library.
  *
  * Same arguments, outputs and results as moe_route, minus the workspace.  The
- * scratch is a fixed array of 768 KiB compiled into the library: every GPU
+ * scratch is a fixed array of 1 MiB compiled into the library: every GPU
  * that loads libmoe.so reserves it until the process exits, and all calls on
  * a GPU share it, so calls that overlap on the GPU (different streams or
  * host threads) race and must be serialised by the caller.  The first call on

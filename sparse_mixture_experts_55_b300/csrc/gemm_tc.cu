@@ -153,6 +153,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const int NT = args.num_n_tiles, S = args.splits;
 
   if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      ptx::mbar_init(&c.full[s], 1);
+      ptx::mbar_init(&c.empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      ptx::mbar_init(&c.tfull[a], 1);
+      ptx::mbar_init(&c.tempty[a], 4);  // one arrive per epilogue warp
+    }
+    ptx::mbar_init(&c.drain, 1);
+    ptx::fence_barrier_init();
+  }
+  // Everything above overlaps the previous kernel's tail (programmatic
+  // dependent launch); its outputs are read only after this wait.
+  ptx::grid_dependency_wait();
+  ptx::allow_dependent_launch();
+  if (threadIdx.x == 0) {
     // Tile table from the padded segment offsets written by the grouping kernel.
     int acc = 0;
     bool bad = false;
@@ -174,16 +190,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     c.tstart[args.E] = acc;
     c.total_tiles = acc;
     c.abort = 0;
-    for (int s = 0; s < STAGES; ++s) {
-      ptx::mbar_init(&c.full[s], 1);
-      ptx::mbar_init(&c.empty[s], 1);
-    }
-    for (int a = 0; a < 2; ++a) {
-      ptx::mbar_init(&c.tfull[a], 1);
-      ptx::mbar_init(&c.tempty[a], 4);  // one arrive per epilogue warp
-    }
-    ptx::mbar_init(&c.drain, 1);
-    ptx::fence_barrier_init();
   }
   __syncthreads();
   const int total = c.total_tiles;
@@ -453,8 +459,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.splits = 1;
   g1.kb_per_split = g1.num_kb;
   g1.status = P.status;
-  expert_gemm_kernel<MODE_GATE_UP><<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tm_x, tm_w1, tm_w3, g1);
-  err = cudaGetLastError();
+  err = launch_kernel(expert_gemm_kernel<MODE_GATE_UP>, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, tm_x,
+                      tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
@@ -466,8 +472,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
-  expert_gemm_kernel<MODE_DOWN><<<num_sms, NUM_THREADS, SMEM_BYTES, s>>>(tm_h, tm_w2, tm_w2, g2);
-  return cudaGetLastError();
+  return launch_kernel(expert_gemm_kernel<MODE_DOWN>, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s,
+                       mid_event == nullptr, tm_h, tm_w2, tm_w2, g2);
 }
 
 }  // namespace moe

@@ -13,13 +13,35 @@ namespace moe {
 // Rows of every expert segment in the grouped buffers are padded to a
 // multiple of this, so a 128-row MMA tile never straddles two experts.
 constexpr int kSegPad = 128;
-// Tokens per router block; also the chunk of (token, slot) entries one
-// grouping block ranks.
-constexpr int kRouteTokens = 64;
+// Tokens per router block (each block writes one expert histogram).
+constexpr int kRouteTokens = 16;
+constexpr int kRouteThreads = 512;
+// Tokens whose (token, slot) entries one grouping block ranks; a multiple of kRouteTokens.
+constexpr int kGroupTokens = 256;
+static_assert(kGroupTokens % kRouteTokens == 0, "grouping chunk must cover whole router blocks");
 constexpr int kMaxE = 32;
 constexpr int kMaxK = 2;
 // Status-word slots at the start of the workspace.
 constexpr int kStatusInts = 8;
+
+// Launch `kernel` on stream s; with pdl the launch may begin while the
+// previous kernel in the stream finishes (programmatic dependent launch): the
+// kernel must execute griddepcontrol.wait before it reads that kernel's output.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl,
+                          Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 struct WsLayout {
   // byte offsets into the workspace

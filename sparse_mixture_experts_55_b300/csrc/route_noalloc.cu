@@ -28,8 +28,8 @@ namespace {
 
 // Routing scratch for T <= MOE_ROUTE_NOALLOC_MAX_T tokens, K <= 2, E <= 32:
 // status word, idx, gate, block histograms, offsets, pos and the padded
-// grouped token/gate arrays (about 705 KiB at the limit).
-constexpr size_t kNoAllocBytes = 768 * 1024;
+// grouped token/gate arrays (about 801 KiB at the limit).
+constexpr size_t kNoAllocBytes = 1024 * 1024;
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
 struct ScratchSlot {

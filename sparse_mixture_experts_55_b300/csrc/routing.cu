@@ -22,6 +22,12 @@ namespace {
 
 __device__ __forceinline__ void set_status(int *status, int code) { atomicCAS(status, 0, code); }
 
+// Programmatic dependent launch: wait for the previous kernel in the stream
+// before touching its outputs, and let the next kernel start its prologue.
+// Both are no-ops when the kernel was launched without the attribute.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 __device__ __forceinline__ float to_f(float v) { return v; }
 __device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
 
@@ -50,40 +56,103 @@ struct Vec<float> {
   }
 };
 
-// Accumulate x[j] * Wg[j, :] for the 16-byte vector of x starting at column j0.
+// Router rows of this thread's d-slice: w[c][e] = W_g[j0 + c, e] as fp32.
 template <typename Tin, int EP>
-__device__ __forceinline__ void accum_vec(const Tin *__restrict__ x_row, const Tin *__restrict__ Wg, int j0, int E,
-                                          float (&acc)[EP]) {
+__device__ __forceinline__ void load_router_rows(const Tin *__restrict__ Wg, int j0, int E, bool valid,
+                                                 float (&w)[Vec<Tin>::N][EP]) {
   constexpr int NV = Vec<Tin>::N;
-  float xv[NV];
-  Vec<Tin>::load(x_row + j0, xv);
-  if (EP == 8 && E == 8) {
-    // Router rows of 8 experts are 16 B (bf16) or 32 B (fp32): vector loads.
 #pragma unroll
-    for (int c = 0; c < NV; ++c) {
-      const Tin *wrow = Wg + static_cast<size_t>(j0 + c) * 8;
-      float w[8];
-      if constexpr (sizeof(Tin) == 2) {
-        Vec<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(wrow), w);
-      } else {
-        float w0[4], w1[4];
-        Vec<float>::load(reinterpret_cast<const float *>(wrow), w0);
-        Vec<float>::load(reinterpret_cast<const float *>(wrow) + 4, w1);
+  for (int c = 0; c < NV; ++c)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) { w[e] = w0[e]; w[4 + e] = w1[e]; }
-      }
+    for (int e = 0; e < EP; ++e) w[c][e] = 0.f;
+  if (!valid) return;
+  if (sizeof(Tin) == 2 && EP == 8 && E == 8) {
 #pragma unroll
-      for (int e = 0; e < 8; ++e) acc[e] = fmaf(xv[c], w[e], acc[e]);
+    for (int c = 0; c < NV; ++c) {  // one 16-byte row per d index
+      float r[8];
+      Vec<__nv_bfloat16>::load(reinterpret_cast<const __nv_bfloat16 *>(Wg) + static_cast<size_t>(j0 + c) * 8, r);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) w[c][e] = r[e];
     }
   } else {
 #pragma unroll
-    for (int c = 0; c < NV; ++c) {
-      const Tin *wrow = Wg + static_cast<size_t>(j0 + c) * E;
+    for (int c = 0; c < NV; ++c)
 #pragma unroll
       for (int e = 0; e < EP; ++e)
-        if (e < E) acc[e] = fmaf(xv[c], to_f(wrow[e]), acc[e]);
-    }
+        if (e < E) w[c][e] = to_f(Wg[static_cast<size_t>(j0 + c) * E + e]);
   }
+}
+
+template <typename Tin>
+__device__ __forceinline__ uint4 load_raw(const Tin *p, bool valid) {
+  return valid ? __ldg(reinterpret_cast<const uint4 *>(p)) : make_uint4(0, 0, 0, 0);
+}
+
+template <typename Tin>
+__device__ __forceinline__ void unpack(uint4 raw, float (&xv)[Vec<Tin>::N]) {
+  if constexpr (sizeof(Tin) == 2) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&raw);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      xv[2 * i] = f.x;
+      xv[2 * i + 1] = f.y;
+    }
+  } else {
+    xv[0] = __uint_as_float(raw.x); xv[1] = __uint_as_float(raw.y);
+    xv[2] = __uint_as_float(raw.z); xv[3] = __uint_as_float(raw.w);
+  }
+}
+
+// a[e] += sum_c x[c] * w[c][e] for one 16-byte chunk of x.
+template <typename Tin, int EP>
+__device__ __forceinline__ void dot_chunk(uint4 raw, const float (&w)[Vec<Tin>::N][EP], float (&a)[EP]) {
+  constexpr int NV = Vec<Tin>::N;
+  float xv[NV];
+  unpack<Tin>(raw, xv);
+#pragma unroll
+  for (int c = 0; c < NV; ++c)
+#pragma unroll
+    for (int e = 0; e < EP; ++e) a[e] = fmaf(xv[c], w[c][e], a[e]);
+}
+
+// The same with the W_g rows streamed from L1 one at a time (no register copy).
+template <typename Tin, int EP>
+__device__ __forceinline__ void dot_chunk_streamed(uint4 raw, const Tin *__restrict__ Wg, int j0, int E,
+                                                   float (&a)[EP]) {
+  constexpr int NV = Vec<Tin>::N;
+  float xv[NV];
+  unpack<Tin>(raw, xv);
+#pragma unroll
+  for (int c = 0; c < NV; ++c) {
+    const Tin *row = Wg + static_cast<size_t>(j0 + c) * E;
+#pragma unroll
+    for (int e = 0; e < EP; ++e)
+      if (e < E) a[e] = fmaf(xv[c], to_f(__ldg(row + e)), a[e]);
+  }
+}
+
+// Warp reduce-scatter of EP partial logits: afterwards lane l holds the warp's
+// sum for expert `expert` (32 / EP lanes per expert hold the same value).
+// log2(EP) halving steps, then full reduction over the remaining lane bits.
+template <int EP>
+__device__ __forceinline__ float warp_reduce_scatter(float (&v)[EP], int lane, int &expert) {
+  int base = 0;
+#pragma unroll
+  for (int w = EP, m = 16; w > 1; w >>= 1, m >>= 1) {
+    const bool upper = (lane & m) != 0;
+#pragma unroll
+    for (int i = 0; i < w / 2; ++i) {
+      const float send = upper ? v[i] : v[i + w / 2];
+      const float keep = upper ? v[i + w / 2] : v[i];
+      v[i] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+    }
+    if (upper) base += w / 2;
+  }
+#pragma unroll
+  for (int m = 16 / EP; m > 0; m >>= 1) v[0] += __shfl_xor_sync(0xffffffffu, v[0], m);
+  expert = base;
+  return v[0];
 }
 
 // Top-K (K <= 2) of the E logits with lower-index tie-break, softmax over the
@@ -122,86 +191,87 @@ __device__ __forceinline__ void select_and_store(const float (&l)[EP], int t, in
   atomicAdd(&s_cnt[i2], 1);
 }
 
-// One block routes kRouteTokens tokens with 8 warps.  With at least 8 tokens a
-// warp owns whole tokens; with fewer, the warps of a group split d and sum
-// their partials in a fixed order.
+// One block routes kRouteTokens tokens.  Thread i owns the i-th 16-byte slice
+// of d (8 bf16 or 4 fp32 columns).  With up to 8 experts it keeps its rows of
+// W_g in registers for all the block's tokens; the x slices of the next group
+// of tokens are loaded while the current group is reduced.  Per token, each
+// warp reduce-scatters its partial logits and the warp sums are added in a
+// fixed order, so the logits are deterministic.
 template <typename Tin, int EP>
-__global__ void __launch_bounds__(256) route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T,
-                                                    int d, int E, int K, unsigned flags, int32_t *__restrict__ idx,
-                                                    float *__restrict__ gate, int32_t *__restrict__ blockcounts,
-                                                    int *status) {
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, unsigned flags,
+                 int32_t *__restrict__ idx, float *__restrict__ gate, int32_t *__restrict__ blockcounts,
+                 int *status) {
   constexpr int NV = Vec<Tin>::N;
-  __shared__ float s_part[8][EP];
+  constexpr int NW = kRouteThreads / 32;
+  constexpr int G = 4;  // tokens per reduction group
+  constexpr bool kCached = EP == 8;
+  __shared__ float s_red[G][NW][EP];
+  __shared__ float s_log[G][EP];
   __shared__ int s_cnt[kMaxE];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kRouteTokens;
   const int nt = min(kRouteTokens, T - t0);
-  const int nvec = d / NV;
-  if (threadIdx.x < kMaxE) s_cnt[threadIdx.x] = 0;
-  __syncthreads();
+  const int nchunks = d / NV;
+  if (tid < kMaxE) s_cnt[tid] = 0;
+  pdl_wait();
+  pdl_trigger();
 
-  if (nt >= 8) {
-    for (int tl = warp; tl < nt; tl += 8) {
-      const int t = t0 + tl;
-      const Tin *x_row = x + static_cast<size_t>(t) * d;
-      float acc[EP];
+  const bool own = tid < nchunks;
+  float w[kCached ? NV : 1][kCached ? EP : 1];
+  if constexpr (kCached) load_router_rows<Tin, EP>(Wg, tid * NV, E, own, w);
+  const Tin *xb = x + static_cast<size_t>(t0) * d + tid * NV;
+  uint4 xr[G];
 #pragma unroll
-      for (int e = 0; e < EP; ++e) acc[e] = 0.f;
-      for (int v = lane; v < nvec; v += 32) accum_vec<Tin, EP>(x_row, Wg, v * NV, E, acc);
+  for (int i = 0; i < G; ++i) xr[i] = load_raw(xb + static_cast<size_t>(i) * d, own && i < nt);
+
+  for (int g0 = 0; g0 < nt; g0 += G) {
 #pragma unroll
-      for (int e = 0; e < EP; ++e)
+    for (int i = 0; i < G; ++i) {
+      float a[EP];
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-      if (lane == 0) select_and_store<EP>(acc, t, E, K, flags, idx, gate, s_cnt, status);
-    }
-  } else {
-    int wpt = 8 / nt;                       // warps per token, rounded down to a power of two
-    wpt = 1 << (31 - __clz(wpt));
-    const int group = warp / wpt, sub = warp % wpt;
-    const bool has_token = group < nt;
-    float acc[EP];
-#pragma unroll
-    for (int e = 0; e < EP; ++e) acc[e] = 0.f;
-    if (has_token) {
-      const Tin *x_row = x + static_cast<size_t>(t0 + group) * d;
-      const int per = (nvec + wpt - 1) / wpt;
-      const int v0 = sub * per, v1 = min(nvec, v0 + per);
-      for (int v = v0 + lane; v < v1; v += 32) accum_vec<Tin, EP>(x_row, Wg, v * NV, E, acc);
-#pragma unroll
-      for (int e = 0; e < EP; ++e)
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) acc[e] += __shfl_xor_sync(0xffffffffu, acc[e], off);
-      if (lane == 0) {
-#pragma unroll
-        for (int e = 0; e < EP; ++e) s_part[warp][e] = acc[e];
+      for (int e = 0; e < EP; ++e) a[e] = 0.f;
+      if constexpr (kCached) {
+        dot_chunk<Tin, EP>(xr[i], w, a);
+      } else {
+        if (own) dot_chunk_streamed<Tin, EP>(xr[i], Wg, tid * NV, E, a);
       }
+      // d wider than one slice per thread: further slices with W_g rows from L1
+      for (int c = tid + kRouteThreads; c < nchunks && g0 + i < nt; c += kRouteThreads)
+        dot_chunk_streamed<Tin, EP>(load_raw(x + static_cast<size_t>(t0 + g0 + i) * d + c * NV, true), Wg, c * NV, E,
+                                    a);
+      int e;
+      const float v = warp_reduce_scatter<EP>(a, lane, e);
+      if ((lane & (32 / EP - 1)) == 0) s_red[i][warp][e] = v;
+    }
+    // the next group's x slices load while this group is reduced
+#pragma unroll
+    for (int i = 0; i < G; ++i) xr[i] = load_raw(xb + static_cast<size_t>(g0 + G + i) * d, own && g0 + G + i < nt);
+    __syncthreads();
+    if (tid < G * EP) {
+      const int i = tid / EP, e = tid % EP;
+      float sum = 0.f;
+#pragma unroll
+      for (int ww = 0; ww < NW; ++ww) sum += s_red[i][ww][e];
+      s_log[i][e] = sum;
     }
     __syncthreads();
-    if (has_token && sub == 0 && lane == 0) {
-      float l[EP];
-#pragma unroll
-      for (int e = 0; e < EP; ++e) {
-        float s = 0.f;
-        for (int w = 0; w < wpt; ++w) s += s_part[warp + w][e];
-        l[e] = s;
-      }
-      select_and_store<EP>(l, t0 + group, E, K, flags, idx, gate, s_cnt, status);
-    }
+    if (tid < G && g0 + tid < nt) select_and_store<EP>(s_log[tid], t0 + g0 + tid, E, K, flags, idx, gate, s_cnt, status);
   }
   __syncthreads();
-  if (threadIdx.x < E) blockcounts[blockIdx.x * E + threadIdx.x] = s_cnt[threadIdx.x];
+  if (tid < E) blockcounts[blockIdx.x * E + tid] = s_cnt[tid];
 }
 
-// Stable grouping.  Block b ranks the (token, slot) entries of router block b
-// in flat t*K + k order: rank = entries of that expert in earlier blocks +
-// in earlier warps of this block + in earlier lanes of this warp.  Each
-// expert's segment in the grouped buffers starts at a multiple of kSegPad;
-// pad rows get token -1 and gate 0.
-__global__ void __launch_bounds__(kRouteTokens *kMaxK)
-    group_kernel(int T, int E, int K, int nb, unsigned flags, const int32_t *__restrict__ idx,
+// Stable grouping.  Block b ranks the (token, slot) entries of tokens
+// [b*kGroupTokens, (b+1)*kGroupTokens) in flat t*K + k order: rank = entries of
+// that expert in earlier router blocks + in earlier warps of this block + in
+// earlier lanes of this warp.  Each expert's segment in the grouped buffers
+// starts at a multiple of kSegPad; pad rows get token -1 and gate 0.
+__global__ void __launch_bounds__(kGroupTokens *kMaxK)
+    group_kernel(int T, int E, int K, int nb_route, unsigned flags, const int32_t *__restrict__ idx,
                  const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
                  int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status) {
-  constexpr int NT = kRouteTokens * kMaxK;
+  constexpr int NT = kGroupTokens * kMaxK;
   constexpr int NW = NT / 32;
   __shared__ int s_base[kMaxE], s_tot[kMaxE], s_off[kMaxE + 1], s_poff[kMaxE + 1];
   __shared__ int s_wcnt[NW][kMaxE];
@@ -210,11 +280,14 @@ __global__ void __launch_bounds__(kRouteTokens *kMaxK)
   if (tid < kMaxE) { s_base[tid] = 0; s_tot[tid] = 0; }
   for (int i = tid; i < NW * kMaxE; i += NT) (&s_wcnt[0][0])[i] = 0;
   __syncthreads();
-  for (int i = tid; i < nb * E; i += NT) {
-    const int bb = i / E, e = i - bb * E;
+  pdl_wait();
+  pdl_trigger();
+  const int rb_before = b * (kGroupTokens / kRouteTokens);  // router blocks ahead of this chunk
+  for (int i = tid; i < nb_route * E; i += NT) {
+    const int rb = i / E, e = i - rb * E;
     const int c = blockcounts[i];
     atomicAdd(&s_tot[e], c);
-    if (bb < b) atomicAdd(&s_base[e], c);
+    if (rb < rb_before) atomicAdd(&s_base[e], c);
   }
   __syncthreads();
   if (tid == 0) {
@@ -231,8 +304,8 @@ __global__ void __launch_bounds__(kRouteTokens *kMaxK)
   __syncthreads();
   if (b == 0 && tid <= E) { offsets[tid] = s_off[tid]; poffsets[tid] = s_poff[tid]; }
 
-  const int flat0 = b * kRouteTokens * K;
-  const int n_entries = min(kRouteTokens, T - b * kRouteTokens) * K;
+  const int flat0 = b * kGroupTokens * K;
+  const int n_entries = min(kGroupTokens, T - b * kGroupTokens) * K;
   bool active = tid < n_entries;
   int e = active ? idx[flat0 + tid] : -1;
   if (active && (e < 0 || e >= E)) {
@@ -252,6 +325,7 @@ __global__ void __launch_bounds__(kRouteTokens *kMaxK)
     perm_gate[rp] = gate[flat0 + tid];
     pos[flat0 + tid] = rp;
   }
+  const int nb = gridDim.x;
   for (int ee = b; ee < E; ee += nb) {
     const int start = s_poff[ee] + s_tot[ee], end = s_poff[ee + 1];
     for (int r = start + tid; r < end; r += NT) {
@@ -268,6 +342,8 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x
                                                      const int32_t *__restrict__ perm_tok,
                                                      const int32_t *__restrict__ poffsets, int E,
                                                      uint4 *__restrict__ xperm, int *status) {
+  pdl_wait();
+  pdl_trigger();
   const int rows = poffsets[E];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -316,6 +392,8 @@ __global__ void __launch_bounds__(256) combine_kernel(Tout *__restrict__ y, int 
                                                       long long split_stride, const float *__restrict__ obuf,
                                                       const int32_t *__restrict__ pos, int rows_bound,
                                                       unsigned flags, int *status) {
+  pdl_wait();
+  pdl_trigger();
   const int q = d >> 2;
   const long long total = static_cast<long long>(T) * q;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -355,6 +433,8 @@ __global__ void route_export_kernel(int T, int E, int K, const int32_t *__restri
                                     const float *__restrict__ gate_ws, const int32_t *__restrict__ pos_ws,
                                     const int32_t *__restrict__ offsets_ws, const int32_t *__restrict__ poffsets_ws,
                                     int32_t *idx, float *gate, int32_t *perm_tok, int32_t *offsets, int32_t *pos) {
+  pdl_wait();
+  pdl_trigger();
   const int n = T * K;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const int e = idx_ws[i];
@@ -397,32 +477,31 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T
 
 cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
                          const Ptrs &P, cudaStream_t s) {
-  const int nb = (T + kRouteTokens - 1) / kRouteTokens;
+  // First kernel of a forward pass: an ordinary launch, ordered after all
+  // earlier work in the stream.
+  const dim3 grid((T + kRouteTokens - 1) / kRouteTokens), block(kRouteThreads);
   if (dtype == MOE_BF16) {
     auto *xx = static_cast<const __nv_bfloat16 *>(x);
     auto *ww = static_cast<const __nv_bfloat16 *>(Wg);
     if (E <= 8)
-      route_kernel<__nv_bfloat16, 8><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts,
-                                                         P.status);
-    else
-      route_kernel<__nv_bfloat16, 32><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts,
-                                                          P.status);
-  } else {
-    auto *xx = static_cast<const float *>(x);
-    auto *ww = static_cast<const float *>(Wg);
-    if (E <= 8)
-      route_kernel<float, 8><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts, P.status);
-    else
-      route_kernel<float, 32><<<nb, 256, 0, s>>>(xx, ww, T, d, E, K, flags, P.idx, P.gate, P.blockcounts,
-                                                 P.status);
+      return launch_kernel(route_kernel<__nv_bfloat16, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags,
+                           P.idx, P.gate, P.blockcounts, P.status);
+    return launch_kernel(route_kernel<__nv_bfloat16, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags,
+                         P.idx, P.gate, P.blockcounts, P.status);
   }
-  return cudaGetLastError();
+  auto *xx = static_cast<const float *>(x);
+  auto *ww = static_cast<const float *>(Wg);
+  if (E <= 8)
+    return launch_kernel(route_kernel<float, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags, P.idx,
+                         P.gate, P.blockcounts, P.status);
+  return launch_kernel(route_kernel<float, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags, P.idx,
+                       P.gate, P.blockcounts, P.status);
 }
 
-cudaError_t launch_group(int T, int E, int K, int nb, unsigned flags, const Ptrs &P, cudaStream_t s) {
-  group_kernel<<<nb, kRouteTokens * kMaxK, 0, s>>>(T, E, K, nb, flags, P.idx, P.gate, P.blockcounts, P.offsets,
-                                                   P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status);
-  return cudaGetLastError();
+cudaError_t launch_group(int T, int E, int K, int nb_route, unsigned flags, const Ptrs &P, cudaStream_t s) {
+  const dim3 grid((T + kGroupTokens - 1) / kGroupTokens), block(kGroupTokens * kMaxK);
+  return launch_kernel(group_kernel, grid, block, 0, s, true, T, E, K, nb_route, flags, P.idx, P.gate,
+                       P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status);
 }
 
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
@@ -432,9 +511,9 @@ cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, 
   int blocks = (R + 7) / 8;  // 8 warps (rows) per block
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
-  gather_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4 *>(x), T, vec_per_row, P.perm_tok, P.poffsets, E,
-                                       static_cast<uint4 *>(P.xperm), P.status);
-  return cudaGetLastError();
+  return launch_kernel(gather_kernel, dim3(blocks), dim3(256), 0, s, true, static_cast<const uint4 *>(x), T,
+                       vec_per_row, static_cast<const int32_t *>(P.perm_tok), static_cast<const int32_t *>(P.poffsets),
+                       E, static_cast<uint4 *>(P.xperm), P.status);
 }
 
 cudaError_t launch_combine(void *y, int T, int d, int K, int S, int R, int dtype, unsigned flags, const Ptrs &P,
@@ -444,13 +523,14 @@ cudaError_t launch_combine(void *y, int T, int d, int K, int S, int R, int dtype
   if (blocks > num_sms * 16LL) blocks = num_sms * 16LL;
   if (blocks < 1) blocks = 1;
   const long long split_stride = static_cast<long long>(R) * d;
+  const dim3 grid(static_cast<unsigned>(blocks)), block(256);
   if (dtype == MOE_BF16)
-    combine_kernel<__nv_bfloat16><<<static_cast<int>(blocks), 256, 0, s>>>(
-        static_cast<__nv_bfloat16 *>(y), T, d, K, S, split_stride, P.obuf, P.pos, R, flags, P.status);
-  else
-    combine_kernel<float><<<static_cast<int>(blocks), 256, 0, s>>>(static_cast<float *>(y), T, d, K, S,
-                                                                   split_stride, P.obuf, P.pos, R, flags, P.status);
-  return cudaGetLastError();
+    return launch_kernel(combine_kernel<__nv_bfloat16>, grid, block, 0, s, true, static_cast<__nv_bfloat16 *>(y), T,
+                         d, K, S, split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos),
+                         R, flags, P.status);
+  return launch_kernel(combine_kernel<float>, grid, block, 0, s, true, static_cast<float *>(y), T, d, K, S,
+                       split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos), R, flags,
+                       P.status);
 }
 
 cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate, int32_t *perm_tok,
@@ -458,9 +538,10 @@ cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx
   int blocks = (T * K + 255) / 256;
   if (blocks < 1) blocks = 1;
   if (blocks > 1024) blocks = 1024;
-  route_export_kernel<<<blocks, 256, 0, s>>>(T, E, K, P.idx, P.gate, P.pos, P.offsets, P.poffsets, idx, gate,
-                                             perm_tok, offsets, pos);
-  return cudaGetLastError();
+  return launch_kernel(route_export_kernel, dim3(blocks), dim3(256), 0, s, true, T, E, K,
+                       static_cast<const int32_t *>(P.idx), static_cast<const float *>(P.gate),
+                       static_cast<const int32_t *>(P.pos), static_cast<const int32_t *>(P.offsets),
+                       static_cast<const int32_t *>(P.poffsets), idx, gate, perm_tok, offsets, pos);
 }
 
 cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s) {

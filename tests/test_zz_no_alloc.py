@@ -46,6 +46,7 @@ def test_route_noalloc_matches_route_on_consecutive_calls(cuda_device):
         (2000, 4096, 8, 2, torch.bfloat16, 21),
         (16384, 4096, 8, 2, torch.bfloat16, 22),   # the size limit, after a smaller call
         (300, 512, 32, 1, torch.float32, 23),
+        (16384, 512, 32, 2, torch.bfloat16, 24),   # the limit with the most experts
     ]
     for T, d, E, K, dt, seed in cases:
         x = W.rms_rows(T, d, seed, "cpu", dt).to(dev)
