@@ -8,12 +8,25 @@
 //             section 3.4 "MoE Layer Formulation", Mixtral of Experts summary
 //             pages).
 //
-// One persistent kernel per GEMM, one 192-thread CTA per SM:
-//   warp 0      TMA producer (one elected thread): A tile 128x64 (K-major,
-//               128-byte swizzle) and B tile 64x256 (four 64-column boxes,
-//               N-major since the weights are stored [E, K, N]) per stage;
+// One persistent kernel per GEMM, launched as clusters of two CTAs (one CTA
+// of 192 threads per SM).  Each CTA computes 128x256 output tiles; the two
+// CTAs of a cluster work on a pair of tiles that share an operand, and each
+// loads half of the shared operand and multicasts it to both:
+//   M-pair  tiles (m, n) and (m+1, n) of one expert share the 64x256 weight
+//           tile: each CTA loads its own 128x64 A tile and two of the four
+//           64-column B boxes, multicast (32 KiB per CTA per k-block
+//           instead of 48);
+//   N-pair  for the last m-tile of an expert with an odd count, tiles
+//           (m, n) and (m, n+1) share the A tile: each CTA loads 64 of its
+//           128 rows multicast and its own B tile.
+// Roles per CTA:
+//   warp 0      TMA producer (one elected thread), 4-stage shared-memory ring
+//               (A 128x64 K-major, B 4 x (64x64) N-major since the weights
+//               are stored [E, K, N]; 128-byte swizzle);
 //   warp 1      TMEM allocator + MMA issuer (one thread): 4 x (M128 N256 K16)
 //               per 64-deep k-block into one of two 256-column accumulators;
+//               its commit frees the stage in both CTAs (a stage is refilled
+//               only after both CTAs' MMAs have read it);
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, SwiGLU or gate
 //               scale, global stores; the second accumulator lets the next
 //               tile's MMAs run under this tile's epilogue.
@@ -41,13 +54,16 @@ constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KiB
+constexpr int A_HALF = A_BYTES / 2;     // 64 rows
 constexpr int B_CHUNK = 64 * BK * 2;    // 8 KiB: 64 N-columns x 64 K-rows
 constexpr int B_BYTES = 4 * B_CHUNK;    // 32 KiB
 constexpr int STAGE_TX = A_BYTES + B_BYTES;
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: the whole TMEM of the SM
 constexpr int NUM_THREADS = 192;
-constexpr int GROUP_M = 8;               // m-tiles rastered together (weight reuse in L2)
+constexpr int CLUSTER = 2;
+constexpr uint16_t kBothCtas = 0x3;
+constexpr int GROUP_PAIRS = 4;           // M-pairs rastered together (weight reuse in L2)
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
@@ -73,10 +89,11 @@ struct Ctrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t exit_bar;        // the peer CTA's "done issuing" arrival
   uint32_t tmem_base;
   int abort;
-  int total_tiles;
-  int tstart[kMaxE + 1];
+  int total_units;
+  int ustart[kMaxE + 1];
   int mtiles[kMaxE];
   int poff[kMaxE + 1];
 };
@@ -87,35 +104,52 @@ static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Tile {
   int e, mt, nt, s;
+  bool npair;  // the pair shares A (N-pair) rather than B (M-pair)
 };
 
-// Tiles of expert e are ordered (m-group, split, n-tile, m-tile within group)
-// with the m-tile fastest, so CTAs running together share one weight panel.
-__device__ __forceinline__ Tile decode_tile(int tile, const Ctrl &c, int NT, int S) {
+// Units of expert e: its M-pairs ordered (pair group, split, n-tile, pair in
+// group) with the pair fastest, so clusters running together share weight
+// panels; then, for an odd m-tile count, the N-pairs of its last m-tile.
+__device__ __forceinline__ int units_of(int mt_e, int NT, int S) {
+  return (mt_e >> 1) * NT * S + (mt_e & 1) * ((NT + 1) >> 1) * S;
+}
+
+__device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S, int rank) {
   Tile t;
   int e = 0;
-  while (tile >= c.tstart[e + 1]) ++e;
-  int r = tile - c.tstart[e];
+  while (u >= c.ustart[e + 1]) ++e;
+  int r = u - c.ustart[e];
   const int mt_e = c.mtiles[e];
-  const int per_m = NT * S;
-  const int full_groups = mt_e / GROUP_M;
-  const int group_tiles = GROUP_M * per_m;
-  int g, gs;
-  if (r < full_groups * group_tiles) {
-    g = r / group_tiles;
-    r -= g * group_tiles;
-    gs = GROUP_M;
-  } else {
-    g = full_groups;
-    r -= full_groups * group_tiles;
-    gs = mt_e - full_groups * GROUP_M;
-  }
-  const int mi = r % gs;
-  r /= gs;
+  const int mp = mt_e >> 1;
+  const int per = NT * S;
   t.e = e;
-  t.nt = r % NT;
-  t.s = r / NT;
-  t.mt = g * GROUP_M + mi;
+  if (r < mp * per) {
+    const int full_groups = mp / GROUP_PAIRS;
+    const int group_units = GROUP_PAIRS * per;
+    int g, gs;
+    if (r < full_groups * group_units) {
+      g = r / group_units;
+      r -= g * group_units;
+      gs = GROUP_PAIRS;
+    } else {
+      g = full_groups;
+      r -= full_groups * group_units;
+      gs = mp - full_groups * GROUP_PAIRS;
+    }
+    const int pi = r % gs;
+    r /= gs;
+    t.nt = r % NT;
+    t.s = r / NT;
+    t.mt = 2 * (g * GROUP_PAIRS + pi) + rank;
+    t.npair = false;
+  } else {
+    r -= mp * per;
+    const int ntp = (NT + 1) >> 1;
+    t.nt = 2 * (r % ntp) + rank;  // may equal NT for odd NT: all its loads and stores fall outside
+    t.s = r / ntp;
+    t.mt = mt_e - 1;
+    t.npair = true;
+  }
   return t;
 }
 
@@ -142,8 +176,9 @@ __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)
 
 template <int MODE>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                       const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+    expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_half,
+                       const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                       const GemmArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;
@@ -151,25 +186,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   Ctrl &c = *reinterpret_cast<Ctrl *>(sB + STAGES * B_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = args.num_n_tiles, S = args.splits;
+  const int rank = static_cast<int>(ptx::cluster_ctarank());
+  const int cluster = static_cast<int>(ptx::cluster_id_x());
+  const int nclusters = static_cast<int>(ptx::num_clusters_x());
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&c.full[s], 1);
-      ptx::mbar_init(&c.empty[s], 1);
+      ptx::mbar_init(&c.empty[s], CLUSTER);  // both CTAs' MMAs release a stage
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&c.tfull[a], 1);
       ptx::mbar_init(&c.tempty[a], 4);  // one arrive per epilogue warp
     }
     ptx::mbar_init(&c.drain, 1);
+    ptx::mbar_init(&c.exit_bar, 1);
     ptx::fence_barrier_init();
   }
+  // Barriers must be initialised in both CTAs before either signals the other.
+  ptx::cluster_sync_all();
   // Everything above overlaps the previous kernel's tail (programmatic
   // dependent launch); its outputs are read only after this wait.
   ptx::grid_dependency_wait();
   ptx::allow_dependent_launch();
   if (threadIdx.x == 0) {
-    // Tile table from the padded segment offsets written by the grouping kernel.
+    // Unit table from the padded segment offsets written by the grouping kernel.
     int acc = 0;
     bool bad = false;
     for (int e = 0; e < args.E; ++e) {
@@ -178,22 +219,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int mt = bad ? 0 : (p1 - p0) / BM;
       c.poff[e] = p0;
       c.mtiles[e] = mt;
-      c.tstart[e] = acc;
-      acc += mt * NT * S;
+      c.ustart[e] = acc;
+      acc += units_of(mt, NT, S);
     }
     if (bad) {
       atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
-      for (int e = 0; e < args.E; ++e) { c.mtiles[e] = 0; c.tstart[e] = 0; }
+      for (int e = 0; e < args.E; ++e) { c.mtiles[e] = 0; c.ustart[e] = 0; }
       acc = 0;
     }
     c.poff[args.E] = args.poffsets[args.E];
-    c.tstart[args.E] = acc;
-    c.total_tiles = acc;
+    c.ustart[args.E] = acc;
+    c.total_units = acc;
     c.abort = 0;
   }
   __syncthreads();
-  const int total = c.total_tiles;
-  if (static_cast<int>(blockIdx.x) >= total) return;  // uniform exit, nothing allocated
+  const int total = c.total_units;
+  // Both CTAs of a cluster read the same table, so they leave together.
+  if (cluster >= total) return;
 
   if (warp == 1) {
     ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
@@ -201,6 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
+    ptx::prefetch_tmap(&tmA_half);
     ptx::prefetch_tmap(&tmB0);
     if (MODE == MODE_GATE_UP) ptx::prefetch_tmap(&tmB1);
   }
@@ -208,44 +251,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  // Producer bookkeeping for the abort drain: stages ever filled and the
-  // phase parity of each one's latest fill.
+  // Producer bookkeeping: stages ever filled, the phase parity of each one's
+  // latest fill, and the ring position after the last fill.
   uint32_t issued = 0, last_par = 0;
+  int p_stage = 0;
+  uint32_t p_phase = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       const uint64_t pol_a = ptx::policy_evict_last();
       const uint64_t pol_b = ptx::policy_evict_normal();
-      int stage = 0;
-      uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, c, NT, S);
+      for (int u = cluster; ok && u < total; u += nclusters) {
+        const Tile t = decode_unit(u, c, NT, S, rank);
         const int row0 = c.poff[t.e] + t.mt * BM;
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
-          if (!wait_bounded(&c.empty[stage], phase ^ 1u, c, args.status, true)) { ok = false; break; }
-          uint64_t *bar = &c.full[stage];
-          ptx::mbar_arrive_expect_tx(bar, STAGE_TX);
-          uint8_t *a_dst = sA + stage * A_BYTES;
-          uint8_t *b_dst = sB + stage * B_BYTES;
-          ptx::tma_load_2d(a_dst, &tmA, bar, kb * BK, row0, pol_a);
-          if (MODE == MODE_GATE_UP) {
-            const int n0 = t.nt * (BN / 2);
-            ptx::tma_load_3d(b_dst, &tmB0, bar, n0, kb * BK, t.e, pol_b);
-            ptx::tma_load_3d(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, kb * BK, t.e, pol_b);
-            ptx::tma_load_3d(b_dst + 2 * B_CHUNK, &tmB1, bar, n0, kb * BK, t.e, pol_b);
-            ptx::tma_load_3d(b_dst + 3 * B_CHUNK, &tmB1, bar, n0 + 64, kb * BK, t.e, pol_b);
+          if (!wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, true)) { ok = false; break; }
+          uint64_t *bar = &c.full[p_stage];
+          ptx::mbar_arrive_expect_tx(bar, STAGE_TX);  // own and peer copies together fill the stage
+          uint8_t *a_dst = sA + p_stage * A_BYTES;
+          uint8_t *b_dst = sB + p_stage * B_BYTES;
+          const int k0 = kb * BK;
+          if (!t.npair) {
+            ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);
+            // this CTA's two of the four B boxes, delivered to both CTAs
+            if (MODE == MODE_GATE_UP) {
+              const int n0 = t.nt * (BN / 2);
+              const CUtensorMap *mb = rank == 0 ? &tmB0 : &tmB1;  // W1 boxes from rank 0, W3 boxes from rank 1
+              ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, mb, bar, n0, k0, t.e, kBothCtas, pol_b);
+              ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, mb, bar, n0 + 64, k0, t.e, kBothCtas, pol_b);
+            } else {
+              const int n0 = t.nt * BN;
+              ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank), k0, t.e, kBothCtas,
+                                  pol_b);
+              ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank + 1), k0, t.e,
+                                  kBothCtas, pol_b);
+            }
           } else {
-            const int n0 = t.nt * BN;
+            // this CTA's 64 of the shared 128 A rows, delivered to both CTAs
+            ptx::tma_load_2d_mc(a_dst + rank * A_HALF, &tmA_half, bar, k0, row0 + 64 * rank, kBothCtas, pol_a);
+            if (MODE == MODE_GATE_UP) {
+              const int n0 = t.nt * (BN / 2);
+              ptx::tma_load_3d(b_dst, &tmB0, bar, n0, k0, t.e, pol_b);
+              ptx::tma_load_3d(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, k0, t.e, pol_b);
+              ptx::tma_load_3d(b_dst + 2 * B_CHUNK, &tmB1, bar, n0, k0, t.e, pol_b);
+              ptx::tma_load_3d(b_dst + 3 * B_CHUNK, &tmB1, bar, n0 + 64, k0, t.e, pol_b);
+            } else {
+              const int n0 = t.nt * BN;
 #pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_load_3d(b_dst + j * B_CHUNK, &tmB0, bar, n0 + 64 * j, kb * BK, t.e, pol_b);
+              for (int j = 0; j < 4; ++j) ptx::tma_load_3d(b_dst + j * B_CHUNK, &tmB0, bar, n0 + 64 * j, k0, t.e, pol_b);
+            }
           }
-          issued |= 1u << stage;
-          last_par = (last_par & ~(1u << stage)) | (phase << stage);
-          if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+          issued |= 1u << p_stage;
+          last_par = (last_par & ~(1u << p_stage)) | (p_phase << p_stage);
+          if (++p_stage == STAGES) { p_stage = 0; p_phase ^= 1u; }
         }
       }
     }
@@ -257,8 +319,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, c, NT, S);
+      for (int u = cluster; ok && u < total; u += nclusters) {
+        const Tile t = decode_unit(u, c, NT, S, rank);
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
         const int acc = local & 1;
@@ -279,7 +341,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 2048, B_CHUNK, 1024);
             ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || ks > 0) ? 1u : 0u);
           }
-          ptx::mma_commit(&c.empty[stage]);  // frees the stage once these MMAs have read it
+          // frees the stage in both CTAs once these MMAs have read it
+          ptx::mma_commit_mc(&c.empty[stage], kBothCtas);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -291,8 +354,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     int local = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-      const Tile t = decode_tile(tile, c, NT, S);
+    for (int u = cluster; u < total; u += nclusters) {
+      const Tile t = decode_unit(u, c, NT, S, rank);
       const int acc = local & 1;
       const uint32_t apar = (local >> 1) & 1;
       int ok = 1;
@@ -305,45 +368,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (MODE == MODE_GATE_UP) {
         __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out);
         const int n0 = t.nt * (BN / 2);
+        if (n0 < args.n_out) {
 #pragma unroll 1
-        for (int cc = 0; cc < 4; ++cc) {
-          uint32_t g[32], u[32];
-          ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
-          ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, u);
-          ptx::tmem_wait_ld();
-          uint32_t packed[16];
+          for (int cc = 0; cc < 4; ++cc) {
+            uint32_t g[32], v[32];
+            ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
+            ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, v);
+            ptx::tmem_wait_ld();
+            uint32_t packed[16];
 #pragma unroll
-          for (int j = 0; j < 16; ++j) {
-            const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(u[2 * j]);
-            const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(u[2 * j + 1]);
-            __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
-            packed[j] = *reinterpret_cast<uint32_t *>(&hb);
+            for (int j = 0; j < 16; ++j) {
+              const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(v[2 * j]);
+              const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(v[2 * j + 1]);
+              __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+              packed[j] = *reinterpret_cast<uint32_t *>(&hb);
+            }
+            const int col = n0 + cc * 32;
+            __nv_bfloat16 *dst = H + static_cast<size_t>(row) * args.n_out + col;
+#pragma unroll
+            for (int vv = 0; vv < 4; ++vv)
+              if (col + vv * 8 < args.n_out)
+                *reinterpret_cast<uint4 *>(dst + vv * 8) =
+                    make_uint4(packed[4 * vv], packed[4 * vv + 1], packed[4 * vv + 2], packed[4 * vv + 3]);
           }
-          const int col = n0 + cc * 32;
-          __nv_bfloat16 *dst = H + static_cast<size_t>(row) * args.n_out + col;
-#pragma unroll
-          for (int v = 0; v < 4; ++v)
-            if (col + v * 8 < args.n_out)
-              *reinterpret_cast<uint4 *>(dst + v * 8) =
-                  make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2], packed[4 * v + 3]);
         }
       } else {
         float *O = static_cast<float *>(args.out) + static_cast<size_t>(t.s) * args.out_split_stride;
         const float gsc = args.perm_gate[row];
         const int n0 = t.nt * BN;
+        if (n0 < args.n_out) {
 #pragma unroll 1
-        for (int cc = 0; cc < BN / 32; ++cc) {
-          uint32_t v[32];
-          ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
-          ptx::tmem_wait_ld();
-          const int col = n0 + cc * 32;
-          float *dst = O + static_cast<size_t>(row) * args.n_out + col;
+          for (int cc = 0; cc < BN / 32; ++cc) {
+            uint32_t v[32];
+            ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
+            ptx::tmem_wait_ld();
+            const int col = n0 + cc * 32;
+            float *dst = O + static_cast<size_t>(row) * args.n_out + col;
 #pragma unroll
-          for (int j = 0; j < 8; ++j)
-            if (col + 4 * j < args.n_out)
-              *reinterpret_cast<float4 *>(dst + 4 * j) =
-                  make_float4(__uint_as_float(v[4 * j]) * gsc, __uint_as_float(v[4 * j + 1]) * gsc,
-                              __uint_as_float(v[4 * j + 2]) * gsc, __uint_as_float(v[4 * j + 3]) * gsc);
+            for (int j = 0; j < 8; ++j)
+              if (col + 4 * j < args.n_out)
+                *reinterpret_cast<float4 *>(dst + 4 * j) =
+                    make_float4(__uint_as_float(v[4 * j]) * gsc, __uint_as_float(v[4 * j + 1]) * gsc,
+                                __uint_as_float(v[4 * j + 2]) * gsc, __uint_as_float(v[4 * j + 3]) * gsc);
+          }
         }
       }
       ptx::tc_fence_before();
@@ -353,11 +420,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   }
 
+  // Producer tail: every stage's last release (by both CTAs' MMAs) has
+  // arrived, so no remote arrive can still land in this CTA's barriers.
+  if (warp == 0 && lane == 0) {
+    for (int i = 0; i < STAGES; ++i) {
+      wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, false);
+      if (++p_stage == STAGES) { p_stage = 0; p_phase ^= 1u; }
+    }
+  }
   ptx::tc_fence_before();
   __syncthreads();
   if (*reinterpret_cast<volatile int *>(&c.abort)) {
     // Some role gave up: before TMEM and shared memory are released, wait
-    // (bounded) for this CTA's MMAs and for every copy it issued.
+    // (bounded) for this CTA's MMAs and for every copy it expects.
     if (warp == 1 && lane == 0) {
       ptx::mma_commit(&c.drain);
       wait_bounded(&c.drain, 0, c, args.status, false);
@@ -369,6 +444,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
   }
+  // Neither CTA leaves while its peer may still send it copies or arrivals.
+  if (threadIdx.x == 0) {
+    ptx::mbar_arrive_remote(&c.exit_bar, static_cast<uint32_t>(rank ^ 1));
+    wait_bounded(&c.exit_bar, 0, c, args.status, false);
+  }
+  __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
     ptx::tmem_dealloc(tmem, TMEM_COLS);
@@ -416,21 +497,68 @@ bool tmap_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-cudaError_t set_smem_attrs() {
+// Per device: shared-memory attribute set, and how many 2-CTA clusters of
+// this kernel can be resident at once (the persistent grid size).
+struct DevState {
+  bool ready = false;
+  int clusters = 0;
+};
+
+cudaError_t device_state(int num_sms, int *clusters) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static std::mutex mu;
-  static bool done[64] = {};
+  static DevState st[64];
   std::lock_guard<std::mutex> lock(mu);
-  if (dev >= 0 && dev < 64 && done[dev]) return cudaSuccess;
-  err = cudaFuncSetAttribute(expert_gemm_kernel<MODE_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             SMEM_BYTES);
-  if (err == cudaSuccess)
-    err = cudaFuncSetAttribute(expert_gemm_kernel<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!st[dev].ready) {
+    err = cudaFuncSetAttribute(expert_gemm_kernel<MODE_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                SMEM_BYTES);
-  if (err == cudaSuccess && dev >= 0 && dev < 64) done[dev] = true;
-  return err;
+    if (err == cudaSuccess)
+      err = cudaFuncSetAttribute(expert_gemm_kernel<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 SMEM_BYTES);
+    if (err != cudaSuccess) return err;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((num_sms / CLUSTER) * CLUSTER);
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = SMEM_BYTES;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = CLUSTER;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    err = cudaOccupancyMaxActiveClusters(&n, expert_gemm_kernel<MODE_GATE_UP>, &cfg);
+    if (err != cudaSuccess) return err;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    st[dev].clusters = n;
+    st[dev].ready = true;
+  }
+  *clusters = st[dev].clusters;
+  return cudaSuccess;
+}
+
+template <int MODE>
+cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMap &a, const CUtensorMap &ah,
+                        const CUtensorMap &b0, const CUtensorMap &b1, const GemmArgs &args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(clusters * CLUSTER);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = pdl ? 2 : 1;
+  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE>, a, ah, b0, b1, args);
 }
 
 }  // namespace
@@ -439,11 +567,13 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
                                      cudaStream_t s, void *const *mid_event) {
   (void)flags;
-  cudaError_t err = set_smem_attrs();
+  int clusters = 0;
+  cudaError_t err = device_state(num_sms, &clusters);
   if (err != cudaSuccess) return err;
-  CUtensorMap tm_x, tm_w1, tm_w3, tm_h, tm_w2;
-  if (!tmap_2d(&tm_x, P.xperm, d, L.R, BM) || !tmap_3d(&tm_w1, W1, f, d, E) || !tmap_3d(&tm_w3, W3, f, d, E) ||
-      !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) || !tmap_3d(&tm_w2, W2, d, f, E))
+  CUtensorMap tm_x, tm_xh, tm_w1, tm_w3, tm_h, tm_hh, tm_w2;
+  if (!tmap_2d(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d(&tm_xh, P.xperm, d, L.R, BM / 2) ||
+      !tmap_3d(&tm_w1, W1, f, d, E) || !tmap_3d(&tm_w3, W3, f, d, E) || !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) ||
+      !tmap_2d(&tm_hh, P.hbuf, f, L.R, BM / 2) || !tmap_3d(&tm_w2, W2, d, f, E))
     return cudaErrorInvalidValue;
 
   GemmArgs g1{};
@@ -459,8 +589,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.splits = 1;
   g1.kb_per_split = g1.num_kb;
   g1.status = P.status;
-  err = launch_kernel(expert_gemm_kernel<MODE_GATE_UP>, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s, true, tm_x,
-                      tm_w1, tm_w3, g1);
+  err = launch_gemm<MODE_GATE_UP>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
@@ -472,8 +601,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
-  return launch_kernel(expert_gemm_kernel<MODE_DOWN>, dim3(num_sms), dim3(NUM_THREADS), SMEM_BYTES, s,
-                       mid_event == nullptr, tm_h, tm_w2, tm_w2, g2);
+  return launch_gemm<MODE_DOWN>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2);
 }
 
 }  // namespace moe
