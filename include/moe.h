@@ -85,7 +85,7 @@ enum { MOE_BF16 = 0, MOE_F32 = 1 };
  * arguments, so one buffer can be reused for every call with the same sizes.
  * It holds the status word, the routing table, the expert grouping and the
  * grouped activations; at T = 4096, d = 4096, f = 14336, E = 8, K = 2, bf16
- * it is about 0.5 GB.
+ * it is about 0.5 GB (including a [T, d] buffer for moe_block_forward).
  */
 MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype);
 
@@ -132,6 +132,27 @@ MOE_API int moe_forward_timed(const void *x, const void *Wg, const void *W1, con
                       void *y, int T, int d, int f, int E, int K, int dtype,
                       void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
                       void *const *events);
+
+/*
+ * One pre-norm MoE half-block of the attention-free stack, in place:
+ *
+ *   h <- h + MoE(RMSNorm(h))
+ *
+ * (paper-graph-ui summary: "Architectural Inheritance from Mistral 7B",
+ * RMSNorm before the MoE block; section 3, the MoE output is added to the
+ * residual stream).  RMSNorm has unit gain: x_n = h / sqrt(mean(h^2) + eps)
+ * per row, fp32 math, rounded to dtype; x_n lives in the workspace.  The MoE
+ * part is moe_forward(x_n, ...) with MOE_ACCUMULATE into h, so its results
+ * equal moe_rmsnorm followed by that call bit for bit.
+ *   h   [T, d]  residual stream, read and updated in place; must not overlap
+ *               the workspace.
+ *   Wg, W1, W3, W2, T, d, f, E, K, dtype, workspace, ws_bytes, stream: as for
+ *   moe_forward (the same workspace size).  eps > 0.
+ *   flags: 0 or MOE_DEBUG_CHECKS (accumulation is implied).
+ */
+MOE_API int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2,
+                      int T, int d, int f, int E, int K, int dtype, float eps,
+                      void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
 
 /*
  * Routing only, for inspection: the router and grouping kernels that

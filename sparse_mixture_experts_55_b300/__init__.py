@@ -21,7 +21,7 @@ from . import _lib
 from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_F32, MoEError,  # noqa: F401
                    status_string)
 
-__all__ = ["moe_forward", "moe_forward_timed", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+__all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
 
@@ -100,6 +100,26 @@ def moe_forward(x, Wg, W1, W3, W2, K: int = 2, y=None, workspace: Workspace | No
                                  _stream_ptr(stream, dev))
     _lib.check("moe_forward", rc)
     return y
+
+
+def moe_block_forward(h, Wg, W1, W3, W2, K: int = 2, eps: float = 1e-5, workspace: Workspace | None = None,
+                      flags: int = 0, stream=None):
+    """One pre-norm MoE half-block in place: h <- h + MoE(RMSNorm(h)); returns h."""
+    dev = h.device
+    dt = h.dtype
+    for t, n in ((h, "h"), (Wg, "Wg"), (W1, "W1"), (W3, "W3"), (W2, "W2")):
+        _need(t, n, dt, dev)
+    T, d = h.shape
+    E, d1, f = W1.shape
+    if Wg.shape != (d, E) or W3.shape != (E, d, f) or W2.shape != (E, f, d) or d1 != d:
+        raise ValueError("shape mismatch: h [T,d], Wg [d,E], W1/W3 [E,d,f], W2 [E,f,d]")
+    if workspace is None:
+        workspace = Workspace(T, d, f, E, K, dt, dev)
+    rc = _lib.load().moe_block_forward(_ptr(h), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), T, d, f, E, K,
+                                       _dtype_code(h), float(eps), workspace.ptr(), workspace.nbytes, flags,
+                                       _stream_ptr(stream, dev))
+    _lib.check("moe_block_forward", rc)
+    return h
 
 
 def moe_forward_timed(x, Wg, W1, W3, W2, K: int, events, y=None, workspace: Workspace | None = None,

@@ -2,9 +2,10 @@
 // fp32 FMA, no TF32), for the exact-arithmetic small configurations.
 //
 //   gate/up:  H[r, n] = SiLU(sum_k X[r,k] W1[e,k,n]) * sum_k X[r,k] W3[e,k,n]
-//   down:     O[r, n] = gate[r] * sum_k H[r,k] W2[e,k,n]
+//   down:     O[u, n] = gate[r] * sum_k H[r,k] W2[e,k,n]
 // ("Expert Network Structure (SwiGLU)", Mixtral of Experts summary pages), for
-// every grouped row r of expert e's padded segment.
+// every grouped row r of expert e's padded segment; the down projection stores
+// only real rows, at their unpadded grouped row u (compact output).
 #include <cuda_runtime.h>
 
 #include "internal.h"
@@ -17,7 +18,8 @@ constexpr int TM = 64, TN = 64, TK = 16;
 template <bool GATE_UP>
 __global__ void __launch_bounds__(256) ffn_f32_kernel(const float *__restrict__ A, const float *__restrict__ B0,
                                                       const float *__restrict__ B1, int k_total, int n_out,
-                                                      const int32_t *__restrict__ poffsets, int E,
+                                                      const int32_t *__restrict__ poffsets,
+                                                      const int32_t *__restrict__ offsets, int E,
                                                       const float *__restrict__ perm_gate, float *__restrict__ out) {
   __shared__ float As[TK][TM];
   __shared__ float Bs0[TK][TN];
@@ -66,6 +68,9 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float *__restrict__ 
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
     const int r = row0 + ty * 4 + i;
+    const int seg_row = r - poffsets[e];
+    if (!GATE_UP && seg_row >= offsets[e + 1] - offsets[e]) continue;  // padding row
+    const int r_out = GATE_UP ? r : offsets[e] + seg_row;
     const float gsc = GATE_UP ? 1.f : perm_gate[r];
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
@@ -78,7 +83,7 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float *__restrict__ 
       } else {
         v = acc0[i][j] * gsc;
       }
-      out[static_cast<size_t>(r) * n_out + n] = v;
+      out[static_cast<size_t>(r_out) * n_out + n] = v;
     }
   }
 }
@@ -89,14 +94,14 @@ cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2
                                   const WsLayout &L, const Ptrs &P, cudaStream_t s, void *const *mid_event) {
   const dim3 g1((f + TN - 1) / TN, L.R / TM);
   ffn_f32_kernel<true><<<g1, 256, 0, s>>>(static_cast<const float *>(P.xperm), static_cast<const float *>(W1),
-                                          static_cast<const float *>(W3), d, f, P.poffsets, E, P.perm_gate,
+                                          static_cast<const float *>(W3), d, f, P.poffsets, P.offsets, E, P.perm_gate,
                                           static_cast<float *>(P.hbuf));
   cudaError_t err = cudaGetLastError();
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
   const dim3 g2((d + TN - 1) / TN, L.R / TM);
   ffn_f32_kernel<false><<<g2, 256, 0, s>>>(static_cast<const float *>(P.hbuf), static_cast<const float *>(W2),
-                                           nullptr, f, d, P.poffsets, E, P.perm_gate, P.obuf);
+                                           nullptr, f, d, P.poffsets, P.offsets, E, P.perm_gate, P.obuf);
   return cudaGetLastError();
 }
 

@@ -70,11 +70,15 @@ enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
 
 struct GemmArgs {
   const int32_t *poffsets;  // [E+1] padded segment starts (device)
+  const int32_t *offsets;   // [E+1] unpadded segment starts (device)
   const float *perm_gate;   // [R] gate of each grouped row (down only)
-  void *out;                // gate/up: bf16 H [R, n_out]; down: fp32 O [splits, R, n_out]
+  void *out;                // gate/up: bf16 H [R, n_out]; down: fp32 O [splits, T*K, n_out]
   long long out_split_stride;
+  float *part;              // gate/up with splits > 1: fp32 partial sums [splits, T*K, 2*n_out]
+  int *tile_cnt;            // gate/up with splits > 1: arrivals per (m-tile, n-tile, lane quarter), zero at launch
   int E;
-  int rows_bound;           // R: rows of the grouped buffers
+  int rows_bound;           // R: rows of the padded grouped buffers
+  int tk;                   // T*K: rows of the compact buffers
   int n_out;                // output columns: f (gate/up) or d (down)
   int num_n_tiles;
   int num_kb;               // k-blocks of 64 over the contraction
@@ -96,6 +100,7 @@ struct Ctrl {
   int ustart[kMaxE + 1];
   int mtiles[kMaxE];
   int poff[kMaxE + 1];
+  int uoff[kMaxE + 1];
 };
 
 constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTES) + 1024 /*Ctrl*/;
@@ -218,6 +223,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (p1 < p0 || (p1 - p0) % BM != 0 || p1 > args.rows_bound) bad = true;
       const int mt = bad ? 0 : (p1 - p0) / BM;
       c.poff[e] = p0;
+      c.uoff[e] = args.offsets[e];
       c.mtiles[e] = mt;
       c.ustart[e] = acc;
       acc += units_of(mt, NT, S);
@@ -228,6 +234,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc = 0;
     }
     c.poff[args.E] = args.poffsets[args.E];
+    c.uoff[args.E] = args.offsets[args.E];
     c.ustart[args.E] = acc;
     c.total_units = acc;
     c.abort = 0;
@@ -363,38 +370,146 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
-      const int row = c.poff[t.e] + t.mt * BM + q * 32 + lane;
+      // This thread's accumulator row: padded grouped row `row`; the first
+      // count_e rows of an expert's segment are real, the rest padding.
+      const int seg_row = t.mt * BM + q * 32 + lane;
+      const int row = c.poff[t.e] + seg_row;
+      const bool real = seg_row < c.uoff[t.e + 1] - c.uoff[t.e];
+      const int ru = c.uoff[t.e] + seg_row;  // unpadded grouped row (valid if real)
       const uint32_t tbase = tmem + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       if (MODE == MODE_GATE_UP) {
-        __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out);
         const int n0 = t.nt * (BN / 2);
-        if (n0 < args.n_out) {
+        if (S == 1) {
+          __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out);
+          if (n0 < args.n_out) {
 #pragma unroll 1
-          for (int cc = 0; cc < 4; ++cc) {
-            uint32_t g[32], v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
-            ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, v);
-            ptx::tmem_wait_ld();
-            uint32_t packed[16];
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t g[32], v[32];
+              ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
+              ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, v);
+              ptx::tmem_wait_ld();
+              uint32_t packed[16];
 #pragma unroll
-            for (int j = 0; j < 16; ++j) {
-              const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(v[2 * j]);
-              const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(v[2 * j + 1]);
-              __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
-              packed[j] = *reinterpret_cast<uint32_t *>(&hb);
+              for (int j = 0; j < 16; ++j) {
+                const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(v[2 * j]);
+                const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(v[2 * j + 1]);
+                __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+                packed[j] = *reinterpret_cast<uint32_t *>(&hb);
+              }
+              const int col = n0 + cc * 32;
+              __nv_bfloat16 *dst = H + static_cast<size_t>(row) * args.n_out + col;
+#pragma unroll
+              for (int vv = 0; vv < 4; ++vv)
+                if (col + vv * 8 < args.n_out)
+                  *reinterpret_cast<uint4 *>(dst + vv * 8) =
+                      make_uint4(packed[4 * vv], packed[4 * vv + 1], packed[4 * vv + 2], packed[4 * vv + 3]);
             }
-            const int col = n0 + cc * 32;
-            __nv_bfloat16 *dst = H + static_cast<size_t>(row) * args.n_out + col;
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
+        } else {
+          // Split contraction: store this split's fp32 sums of the real rows,
+          // release the accumulator, and let the CTA that completes the tile
+          // (the last of its S splits to arrive) add the S partials in split
+          // order and apply SwiGLU -- deterministic whatever the arrival order.
+          const size_t pstride = 2 * static_cast<size_t>(args.n_out);
+          float *P = args.part + static_cast<size_t>(t.s) * args.tk * pstride;
+          if (n0 < args.n_out) {
+#pragma unroll 1
+            for (int cc = 0; cc < 4; ++cc) {
+              uint32_t g[32], v[32];
+              ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
+              ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, v);
+              ptx::tmem_wait_ld();
+              const int col = n0 + cc * 32;
+              if (real) {
+                float *pg = P + static_cast<size_t>(ru) * pstride + col;
+                float *pv = pg + args.n_out;
 #pragma unroll
-            for (int vv = 0; vv < 4; ++vv)
-              if (col + vv * 8 < args.n_out)
-                *reinterpret_cast<uint4 *>(dst + vv * 8) =
-                    make_uint4(packed[4 * vv], packed[4 * vv + 1], packed[4 * vv + 2], packed[4 * vv + 3]);
+                for (int j = 0; j < 8; ++j)
+                  if (col + 4 * j < args.n_out) {
+                    __stcg(reinterpret_cast<float4 *>(pg + 4 * j),
+                           make_float4(__uint_as_float(g[4 * j]), __uint_as_float(g[4 * j + 1]),
+                                       __uint_as_float(g[4 * j + 2]), __uint_as_float(g[4 * j + 3])));
+                    __stcg(reinterpret_cast<float4 *>(pv + 4 * j),
+                           make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
+                                       __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3])));
+                  }
+              }
+            }
+          }
+          ptx::tc_fence_before();
+          __syncwarp();
+          if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
+          if (n0 < args.n_out) {
+            // One arrival counter per (m-tile, n-tile, lane quarter): each
+            // epilogue warp completes its own 32 rows, with no cross-warp wait.
+            int *cnt = args.tile_cnt + (static_cast<size_t>(row / BM) * NT + t.nt) * 4 + q;
+            __syncwarp();  // the warp's partial stores precede its arrival
+            int last = 0;
+            if (lane == 0) {
+              __threadfence();
+              last = atomicAdd(cnt, 1) == S - 1 ? 1 : 0;
+            }
+            last = __shfl_sync(0xffffffffu, last, 0);
+            if (last) {
+              __threadfence();  // the other splits' partials are visible to every lane
+              // The warp completes its real rows four at a time, lane l taking
+              // columns [4l, 4l + 4) of the tile's 128, so the partial loads
+              // are coalesced and those of four rows are in flight together.
+              // Each sum runs over the splits in order.
+              const int col = n0 + 4 * lane;
+              const size_t sstride = static_cast<size_t>(args.tk) * pstride;
+              unsigned m = __ballot_sync(0xffffffffu, real);
+              while (m) {
+                int src[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                  src[j] = m ? __ffs(m) - 1 : -1;
+                  m &= m - 1;
+                }
+                if (col < args.n_out) {
+                  const float *pg[4];
+                  float4 a[4], b[4];
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    pg[j] = args.part + static_cast<size_t>(ru - lane + (src[j] < 0 ? lane : src[j])) * pstride + col;
+                    a[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+                    b[j] = a[j];
+                  }
+#pragma unroll 2
+                  for (int sp = 0; sp < S; ++sp) {
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      if (src[j] < 0) continue;
+                      const float4 ga = __ldcg(reinterpret_cast<const float4 *>(pg[j] + sp * sstride));
+                      const float4 gb = __ldcg(reinterpret_cast<const float4 *>(pg[j] + sp * sstride + args.n_out));
+                      a[j].x += ga.x; a[j].y += ga.y; a[j].z += ga.z; a[j].w += ga.w;
+                      b[j].x += gb.x; b[j].y += gb.y; b[j].z += gb.z; b[j].w += gb.w;
+                    }
+                  }
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    if (src[j] < 0) continue;
+                    __nv_bfloat162 h01 = __floats2bfloat162_rn(silu_f(a[j].x) * b[j].x, silu_f(a[j].y) * b[j].y);
+                    __nv_bfloat162 h23 = __floats2bfloat162_rn(silu_f(a[j].z) * b[j].z, silu_f(a[j].w) * b[j].w);
+                    uint2 packed;
+                    packed.x = *reinterpret_cast<uint32_t *>(&h01);
+                    packed.y = *reinterpret_cast<uint32_t *>(&h23);
+                    __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out) +
+                                       static_cast<size_t>(row - lane + src[j]) * args.n_out + col;
+                    *reinterpret_cast<uint2 *>(H) = packed;
+                  }
+                }
+              }
+            }
           }
         }
       } else {
+        // gate-scaled rows into the compact output; padding rows are dropped
         float *O = static_cast<float *>(args.out) + static_cast<size_t>(t.s) * args.out_split_stride;
-        const float gsc = args.perm_gate[row];
+        const float gsc = real ? args.perm_gate[row] : 0.f;
         const int n0 = t.nt * BN;
         if (n0 < args.n_out) {
 #pragma unroll 1
@@ -403,19 +518,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
             ptx::tmem_wait_ld();
             const int col = n0 + cc * 32;
-            float *dst = O + static_cast<size_t>(row) * args.n_out + col;
+            if (real) {
+              float *dst = O + static_cast<size_t>(ru) * args.n_out + col;
 #pragma unroll
-            for (int j = 0; j < 8; ++j)
-              if (col + 4 * j < args.n_out)
-                *reinterpret_cast<float4 *>(dst + 4 * j) =
-                    make_float4(__uint_as_float(v[4 * j]) * gsc, __uint_as_float(v[4 * j + 1]) * gsc,
-                                __uint_as_float(v[4 * j + 2]) * gsc, __uint_as_float(v[4 * j + 3]) * gsc);
+              for (int j = 0; j < 8; ++j)
+                if (col + 4 * j < args.n_out)
+                  *reinterpret_cast<float4 *>(dst + 4 * j) =
+                      make_float4(__uint_as_float(v[4 * j]) * gsc, __uint_as_float(v[4 * j + 1]) * gsc,
+                                  __uint_as_float(v[4 * j + 2]) * gsc, __uint_as_float(v[4 * j + 3]) * gsc);
+            }
           }
         }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
       }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
       ++local;
     }
   }
@@ -578,16 +695,20 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
 
   GemmArgs g1{};
   g1.poffsets = P.poffsets;
+  g1.offsets = P.offsets;
   g1.perm_gate = P.perm_gate;
   g1.out = P.hbuf;
   g1.out_split_stride = 0;
+  g1.part = P.gu_part;
+  g1.tile_cnt = P.tile_cnt;
   g1.E = E;
   g1.rows_bound = L.R;
+  g1.tk = L.TK;
   g1.n_out = f;
   g1.num_n_tiles = (f + BN / 2 - 1) / (BN / 2);
   g1.num_kb = (d + BK - 1) / BK;
-  g1.splits = 1;
-  g1.kb_per_split = g1.num_kb;
+  g1.splits = L.S_gu;
+  g1.kb_per_split = L.kb_per_split_gu;
   g1.status = P.status;
   err = launch_gemm<MODE_GATE_UP>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
@@ -595,7 +716,9 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
 
   GemmArgs g2 = g1;
   g2.out = P.obuf;
-  g2.out_split_stride = static_cast<long long>(L.R) * d;
+  g2.out_split_stride = static_cast<long long>(g1.tk) * d;
+  g2.part = nullptr;
+  g2.tile_cnt = nullptr;
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + BK - 1) / BK;

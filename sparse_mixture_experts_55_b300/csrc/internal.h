@@ -45,27 +45,44 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 struct WsLayout {
   // byte offsets into the workspace
-  size_t status, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf, obuf;
+  size_t status, tile_cnt, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf, obuf,
+      gu_part, xnorm;
   size_t total;
-  int R;         // padded grouped rows (upper bound): T*K + E*(kSegPad-1), rounded up to kSegPad
-  int S;         // split-K count of the down projection
+  size_t zero_bytes;  // bytes from `status` that every call clears (status word + split counters)
+  int TK;             // T*K: rows of the compact grouped buffers
+  int R;              // padded grouped rows (upper bound): T*K + E*(kSegPad-1), rounded up to kSegPad
+  int S;              // split count over the contraction of the down projection
   int kb_per_split;
+  int S_gu;           // split count over the contraction of the gate/up projection
+  int kb_per_split_gu;
   int n_route_blocks;
 };
 
-// Split-K count for the down projection: enough (expert, n-tile, split) work
-// units to cover the SMs when few tokens are routed.
-int down_splits(int T, int d, int f, int E, int K, int num_sms);
+// Split of one grouped GEMM's contraction into S ranges of kb_per_split
+// 64-deep k-blocks.
+struct SplitPlan {
+  int S, kb_per_split;
+};
+// Chooses the split from a makespan model of the persistent GEMM: cluster
+// units of work (an expert's tile pairs times S) spread over `clusters`
+// co-resident 2-CTA clusters, each unit costing its k-blocks plus a fixed
+// overhead, inflated by the fp32 partial-sum traffic a split adds
+// (part_ratio = partial bytes per split / weight bytes).  S = 1 unless a
+// split shortens the modelled time by at least 3%.
+SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, double part_ratio);
 WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms);
 
 struct Ptrs {
   int *status;
+  int *tile_cnt;  // arrival counters of split gate/up tiles
   int32_t *idx;
   float *gate;
   int32_t *blockcounts, *offsets, *poffsets, *pos, *perm_tok;
   float *perm_gate;
   void *xperm, *hbuf;
-  float *obuf;
+  float *obuf;    // [S, T*K, d] gate-scaled expert outputs, unpadded grouped rows
+  float *gu_part; // [S_gu, T*K, 2f] fp32 partial sums of the split gate/up projection
+  void *xnorm;  // [T, d] normalised block input (moe_block_forward)
 };
 Ptrs carve(void *ws, const WsLayout &L);
 
@@ -76,7 +93,7 @@ cudaError_t launch_group(int T, int E, int K, int n_route_blocks, unsigned flags
                          cudaStream_t s);
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
                           cudaStream_t s);
-cudaError_t launch_combine(void *y, int T, int d, int K, int S, int R, int dtype, unsigned flags, const Ptrs &P,
+cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsigned flags, const Ptrs &P,
                            int num_sms, cudaStream_t s);
 cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate,
                                 int32_t *perm_tok, int32_t *offsets, int32_t *pos, cudaStream_t s);

@@ -82,19 +82,33 @@ int check_device() {
 
 }  // namespace
 
-int down_splits(int T, int d, int f, int E, int K, int num_sms) {
-  const int n_tiles = (d + 255) / 256;
-  const long long rows = static_cast<long long>(T) * K;
-  const long long touched = rows < E ? rows : E;
-  // upper bound on the number of 128-row tiles over all experts
-  const long long m_tiles = (rows + kSegPad - 1) / kSegPad + (touched > 0 ? touched - 1 : 0);
-  const long long units = m_tiles * n_tiles;
-  if (units <= 0 || units >= num_sms) return 1;
-  int S = static_cast<int>(num_sms / units);
-  const int kb = (f + 63) / 64;
-  if (S > 16) S = 16;
-  if (S > kb) S = kb;
-  return S < 1 ? 1 : S;
+SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, double part_ratio) {
+  SplitPlan best{1, kb};
+  if (TK <= 0 || kb <= 1 || clusters <= 0) return best;
+  const long long touched = TK < E ? TK : E;
+  const long long rows_per = (TK + touched - 1) / touched;
+  const long long mt = (rows_per + kSegPad - 1) / kSegPad;  // m-tiles per touched expert
+  // cluster units per split: pairs of m-tiles sharing the weight tile, and
+  // for an odd m-tile count, pairs of n-tiles sharing the activation tile
+  const long long per_split = touched * ((mt >> 1) * n_tiles + (mt & 1) * ((n_tiles + 1) / 2));
+  constexpr double kUnitOverheadKb = 0.5;
+  auto cost = [&](int S, int kps) {
+    const long long waves = (per_split * S + clusters - 1) / clusters;
+    return static_cast<double>(waves) * (kps + kUnitOverheadKb) * (1.0 + part_ratio * (S > 1 ? S : 0));
+  };
+  const double base = cost(1, kb);
+  double best_cost = base;
+  for (int s = 2; s <= 32 && s <= kb; ++s) {
+    const int kps = (kb + s - 1) / s;
+    const int S = (kb + kps - 1) / kps;  // every split owns >= 1 k-block
+    const double c = cost(S, kps);
+    if (c < best_cost) {
+      best_cost = c;
+      best = SplitPlan{S, kps};
+    }
+  }
+  if (best_cost > 0.97 * base) best = SplitPlan{1, kb};
+  return best;
 }
 
 WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
@@ -102,10 +116,28 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   const size_t eb = elem_bytes(dtype);
   L.R = static_cast<int>(align_up(static_cast<size_t>(T) * K + static_cast<size_t>(E) * (kSegPad - 1), kSegPad));
   L.n_route_blocks = (T + kRouteTokens - 1) / kRouteTokens;
-  const int kb = (f + 63) / 64;
-  int S = dtype == MOE_BF16 ? down_splits(T, d, f, E, K, num_sms) : 1;
-  L.kb_per_split = (kb + S - 1) / S;
-  L.S = (kb + L.kb_per_split - 1) / L.kb_per_split;  // every split owns >= 1 k-block
+  const long long TKl = static_cast<long long>(T) * K;
+  L.TK = static_cast<int>(TKl);
+  const long long touched = TKl < E ? TKl : E;
+  SplitPlan down{1, (f + 63) / 64}, gu{1, (d + 63) / 64};
+  if (dtype == MOE_BF16 && touched > 0) {
+    const int clusters = num_sms / 2;
+    // partial-sum bytes (written once, read once, fp32) per split over the
+    // weight bytes each projection streams
+    down = plan_splits(TKl, E, (d + 255) / 256, (f + 63) / 64, clusters,
+                       4.0 * static_cast<double>(TKl) / (static_cast<double>(touched) * f));
+    // The split gate/up tile is completed inside the GEMM by the last split's
+    // epilogue warp, whose latency grows with the real rows it owns; beyond
+    // about four rows per expert it stalls the MMA pipeline more than the
+    // balanced split saves, so larger batches keep one split.
+    if (TKl <= 4 * touched)
+      gu = plan_splits(TKl, E, (f + 127) / 128, (d + 63) / 64, clusters,
+                       4.0 * static_cast<double>(TKl) / (static_cast<double>(touched) * d));
+  }
+  L.S = down.S;
+  L.kb_per_split = down.kb_per_split;
+  L.S_gu = gu.S;
+  L.kb_per_split_gu = gu.kb_per_split;
   const size_t TK = static_cast<size_t>(T) * K;
   const size_t R = static_cast<size_t>(L.R);
   size_t o = 0;
@@ -115,6 +147,10 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
     return at;
   };
   L.status = take(kStatusInts * sizeof(int));
+  // one arrival counter per (128-row m-tile, n-tile, 32-row quarter) of the split gate/up GEMM
+  const size_t n_cnt = L.S_gu > 1 ? (R / kSegPad) * static_cast<size_t>((f + 127) / 128) * 4 : 0;
+  L.tile_cnt = take(n_cnt * sizeof(int));
+  L.zero_bytes = o - L.status;
   L.idx = take(TK * 4);
   L.gate = take(TK * 4);
   L.blockcounts = take(static_cast<size_t>(L.n_route_blocks > 0 ? L.n_route_blocks : 1) * E * 4);
@@ -125,7 +161,9 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   L.perm_gate = take(R * 4);
   L.xperm = take(R * d * eb);
   L.hbuf = take(R * f * eb);
-  L.obuf = take(static_cast<size_t>(L.S) * R * d * 4);
+  L.obuf = take(static_cast<size_t>(L.S) * TK * d * 4);
+  L.gu_part = take(L.S_gu > 1 ? static_cast<size_t>(L.S_gu) * TK * 2 * f * 4 : 0);
+  L.xnorm = take(static_cast<size_t>(T) * d * eb);
   L.total = o;
   return L;
 }
@@ -134,6 +172,7 @@ Ptrs carve(void *ws, const WsLayout &L) {
   char *b = static_cast<char *>(ws);
   Ptrs P;
   P.status = reinterpret_cast<int *>(b + L.status);
+  P.tile_cnt = reinterpret_cast<int *>(b + L.tile_cnt);
   P.idx = reinterpret_cast<int32_t *>(b + L.idx);
   P.gate = reinterpret_cast<float *>(b + L.gate);
   P.blockcounts = reinterpret_cast<int32_t *>(b + L.blockcounts);
@@ -145,6 +184,8 @@ Ptrs carve(void *ws, const WsLayout &L) {
   P.xperm = b + L.xperm;
   P.hbuf = b + L.hbuf;
   P.obuf = reinterpret_cast<float *>(b + L.obuf);
+  P.gu_part = reinterpret_cast<float *>(b + L.gu_part);
+  P.xnorm = b + L.xnorm;
   return P;
 }
 
@@ -179,7 +220,8 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   if (st != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Ptrs P = carve(workspace, L);
-  if (cudaMemsetAsync(P.status, 0, kStatusInts * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
+  // status word and split-tile counters start at zero
+  if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   // events (optional): one before the router and one after each of the six stages
   auto mark = [&](int i) -> cudaError_t {
@@ -199,7 +241,7 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
       err = launch_expert_ffn_f32(W1, W3, W2, d, f, E, L, P, s, events ? events + 4 : nullptr);
   }
   if (err == cudaSuccess) err = mark(5);
-  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, L.R, dtype, flags, P, sms, s);
+  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
   if (err == cudaSuccess) err = mark(6);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -208,6 +250,29 @@ int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, c
                 int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes, unsigned flags,
                 moe_stream_t stream) {
   return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, nullptr);
+}
+
+int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d, int f,
+                      int E, int K, int dtype, float eps, void *workspace, size_t ws_bytes, unsigned flags,
+                      moe_stream_t stream) {
+  int st = check_shape(T, d, f, E, K, dtype);
+  if (st != MOE_OK) return st;
+  if (flags & ~MOE_DEBUG_CHECKS) return MOE_ERR_INVALID_ARG;
+  if (!(eps > 0.f)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!h || !aligned16(h)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  const WsLayout L = ws_layout(T, d, f, E, K, dtype, sm_count_or_default());
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  if (overlaps(h, static_cast<size_t>(T) * d * elem_bytes(dtype), workspace, L.total)) return MOE_ERR_INVALID_ARG;
+  st = check_device();
+  if (st != MOE_OK) return st;
+  const Ptrs P = carve(workspace, L);
+  // x_n = RMSNorm(h) into the workspace, then h += MoE(x_n)
+  if (launch_rmsnorm(h, P.xnorm, T, d, eps, dtype, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return forward_impl(P.xnorm, Wg, W1, W3, W2, h, T, d, f, E, K, dtype, workspace, ws_bytes, flags | MOE_ACCUMULATE,
+                      stream, nullptr);
 }
 
 int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,

@@ -265,8 +265,10 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // Stable grouping.  Block b ranks the (token, slot) entries of tokens
 // [b*kGroupTokens, (b+1)*kGroupTokens) in flat t*K + k order: rank = entries of
 // that expert in earlier router blocks + in earlier warps of this block + in
-// earlier lanes of this warp.  Each expert's segment in the grouped buffers
-// starts at a multiple of kSegPad; pad rows get token -1 and gate 0.
+// earlier lanes of this warp.  Each expert's segment in the padded grouped
+// buffers (X_perm, H) starts at a multiple of kSegPad; pad rows get token -1
+// and gate 0.  pos[t, k] is the entry's row in the unpadded grouped order
+// (offsets[e] + rank), which indexes the compact expert-output buffer.
 __global__ void __launch_bounds__(kGroupTokens *kMaxK)
     group_kernel(int T, int E, int K, int nb_route, unsigned flags, const int32_t *__restrict__ idx,
                  const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
@@ -323,7 +325,7 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
     const int rp = s_poff[e] + r;
     perm_tok[rp] = (flat0 + tid) / K;
     perm_gate[rp] = gate[flat0 + tid];
-    pos[flat0 + tid] = rp;
+    pos[flat0 + tid] = s_off[e] + r;  // unpadded grouped row
   }
   const int nb = gridDim.x;
   for (int ee = b; ee < E; ee += nb) {
@@ -385,8 +387,10 @@ __device__ __forceinline__ float4 load4(const __nv_bfloat16 *p) {
   return make_float4(a.x, a.y, b.x, b.y);
 }
 
-// y[t] = sum_k (sum_s O[s][pos[t,k]]): slot 0 then slot 1, splits in order.
-// The gate was applied by the down projection's epilogue.  No atomics.
+// y[t] = sum_k (sum_s O[s][pos[t,k]]): slot 0 then slot 1, splits in order,
+// with O the compact [splits, T*K, d] output of the down projection (pos is an
+// unpadded grouped row).  The gate was applied by the down projection's
+// epilogue.  No atomics.
 template <typename Tout>
 __global__ void __launch_bounds__(256) combine_kernel(Tout *__restrict__ y, int T, int d, int K, int S,
                                                       long long split_stride, const float *__restrict__ obuf,
@@ -438,7 +442,7 @@ __global__ void route_export_kernel(int T, int E, int K, const int32_t *__restri
   const int n = T * K;
   for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < n; i += gridDim.x * blockDim.x) {
     const int e = idx_ws[i];
-    const int ru = offsets_ws[e] + (pos_ws[i] - poffsets_ws[e]);
+    const int ru = pos_ws[i];
     idx[i] = e;
     gate[i] = gate_ws[i];
     perm_tok[ru] = i / K;
@@ -516,21 +520,21 @@ cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, 
                        E, static_cast<uint4 *>(P.xperm), P.status);
 }
 
-cudaError_t launch_combine(void *y, int T, int d, int K, int S, int R, int dtype, unsigned flags, const Ptrs &P,
+cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsigned flags, const Ptrs &P,
                            int num_sms, cudaStream_t s) {
   const long long total = static_cast<long long>(T) * (d / 4);
   long long blocks = (total + 255) / 256;
   if (blocks > num_sms * 16LL) blocks = num_sms * 16LL;
   if (blocks < 1) blocks = 1;
-  const long long split_stride = static_cast<long long>(R) * d;
+  const long long split_stride = static_cast<long long>(T) * K * d;  // compact [S, T*K, d]
   const dim3 grid(static_cast<unsigned>(blocks)), block(256);
   if (dtype == MOE_BF16)
     return launch_kernel(combine_kernel<__nv_bfloat16>, grid, block, 0, s, true, static_cast<__nv_bfloat16 *>(y), T,
                          d, K, S, split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos),
-                         R, flags, P.status);
+                         T * K, flags, P.status);
   return launch_kernel(combine_kernel<float>, grid, block, 0, s, true, static_cast<float *>(y), T, d, K, S,
-                       split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos), R, flags,
-                       P.status);
+                       split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos), T * K,
+                       flags, P.status);
 }
 
 cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate, int32_t *perm_tok,

@@ -76,3 +76,23 @@ def gate_invariants(idx_gpu, gate_gpu, E: int, K: int) -> None:
     assert np.abs(gate_gpu.sum(axis=1) - 1.0).max() <= 2e-7
     if K == 2:
         assert (gate_gpu[:, 0] >= gate_gpu[:, 1]).all()
+
+
+def half_ulp(v, dtype: str) -> np.ndarray:
+    """Half a unit in the last place of each value as stored in ``dtype``
+    (bf16: 8 significant bits, fp32: 24), i.e. the largest error of one
+    round-to-nearest into that type."""
+    bits = {"bf16": 8, "f32": 24}[dtype]
+    a = np.abs(np.asarray(v, dtype=np.float64))
+    e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
+    return np.where(a > 0, np.exp2(e - bits), 0.0)
+
+
+def residual_rel_err(h_new, h_prev, y_ref, dtype: str) -> float:
+    """Error of a residual update h_new = round(h_prev + y) against the oracle's
+    y, relative to max|y_ref| like rel_linf, after removing the one rounding
+    of the sum into the storage type (which the MoE output is not charged for)."""
+    h_new = np.asarray(h_new, dtype=np.float64)
+    dev = np.abs(h_new - np.asarray(h_prev, dtype=np.float64) - np.asarray(y_ref, dtype=np.float64))
+    excess = np.maximum(dev - half_ulp(h_new, dtype), 0.0)
+    return float(excess.max() / (np.abs(y_ref).max() + 1e-6)) if dev.size else 0.0

@@ -28,7 +28,7 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _header_functions()
-    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_route",
+    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_block_forward", "moe_route",
                             "moe_route_noalloc", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
@@ -48,9 +48,10 @@ def test_status_strings_and_version(lib):
 
 def test_workspace_bytes(lib):
     mix = lib.moe_workspace_bytes(4096, 4096, 14336, 8, 2, _lib.MOE_BF16)
-    # grouped rows: 8192 tokens*slots + 8 * 127 pad rows, rounded to 128 -> 9216
-    R = 9216
-    lower = R * 4096 * 2 + R * 14336 * 2 + R * 4096 * 4
+    # grouped rows: 8192 tokens*slots + 8 * 127 pad rows, rounded to 128 -> 9216;
+    # padded X_perm and H, compact fp32 expert outputs, the block's normalised input
+    R, TK = 9216, 8192
+    lower = R * 4096 * 2 + R * 14336 * 2 + TK * 4096 * 4 + 4096 * 4096 * 2
     assert lower <= mix <= lower + 2 * 1024 * 1024
     assert lib.moe_workspace_bytes(0, 64, 128, 8, 2, _lib.MOE_F32) > 0
     # invalid shapes -> 0
@@ -119,3 +120,22 @@ def test_binding_has_no_fallback(monkeypatch, tmp_path):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="missing"):
         _lib.load()
+
+
+def test_block_forward_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    f32 = ctypes.c_float
+
+    def blk(h=0x1000, T=16, K=2, eps=1e-5, ws=0x200000, ws_bytes=1 << 40, flags=0):
+        return lib.moe_block_forward(vp(h), vp(0x2000), vp(0x3000), vp(0x4000), vp(0x5000), T, 64, 128, 8, K,
+                                     _lib.MOE_BF16, f32(eps), vp(ws), ws_bytes, flags, vp(0))
+
+    assert blk(K=3) == _lib.MOE_ERR_UNSUPPORTED
+    assert blk(eps=0.0) == _lib.MOE_ERR_INVALID_ARG
+    assert blk(flags=_lib.MOE_ACCUMULATE) == _lib.MOE_ERR_INVALID_ARG   # accumulation is implied
+    assert blk(h=0) == _lib.MOE_ERR_INVALID_ARG
+    assert blk(h=0x1008) == _lib.MOE_ERR_INVALID_ARG
+    assert blk(ws=0) == _lib.MOE_ERR_WORKSPACE
+    assert blk(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
+    assert blk(h=0x200000 + 256) == _lib.MOE_ERR_INVALID_ARG            # h inside the workspace
+    assert blk(h=0, T=0) == _lib.MOE_OK                                  # empty input: no-op

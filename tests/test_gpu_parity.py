@@ -94,6 +94,13 @@ def _bf16_inputs(T, d, f, E, K, seed):
     (8, 512, 1024, 8, 2),
     (128, 512, 1024, 8, 2),
     (3000, 256, 256, 8, 2),     # 6 m-tiles per expert, many tiles per CTA
+    # decode-like shapes whose gate/up contraction is split (fp32 partials,
+    # completed by the last split's CTA): odd n-tile count with a ragged
+    # tail, ragged K, top-1 with 3 experts
+    (16, 1024, 1032, 8, 2),
+    (5, 2056, 1160, 8, 2),
+    (3, 1544, 904, 6, 2),
+    (24, 1048, 1096, 3, 1),
 ])
 def test_bf16_shapes(moe, T, d, f, E, K):
     inp = _bf16_inputs(T, d, f, E, K, seed=100 + T)
@@ -172,3 +179,19 @@ def test_debug_checks_report_nonfinite_router_input(moe):
     assert moe.moe_read_status(ws) == 6  # MOE_ERR_NONFINITE
     moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, 2, workspace=ws, flags=moe.MOE_DEBUG_CHECKS)
     assert moe.moe_read_status(ws) == 0
+
+
+@pytest.mark.parametrize("dt,tol_key", [(torch.bfloat16, "bf16"), (torch.float32, "f32")])
+def test_block_stack_small(moe, dt, tol_key):
+    """Four pre-norm MoE blocks h <- h + MoE_l(RMSNorm(h)), each layer with its
+    own seeded weights, checked layer by layer against the oracle."""
+    from tests.stack_check import check_stack_layer
+    dev = torch.device("cuda:0")
+    T, d, f, E, K, L = 300, 256, 512, 8, 2, 4
+    h = W.stack_h0(T, d, device=dev, dtype=dt)
+    ws = moe.Workspace(T, d, f, E, K, dt, dev)
+    toks = np.arange(T)
+    for l in range(L):
+        wts = W.stack_layer_weights(l, d, f, E, device=dev, dtype=dt)
+        err_y, err_h, rep = check_stack_layer(moe, h, wts, K, toks, ws, tol_key)
+        print(f"layer {l}: rel err y {err_y:.2e}, residual {err_h:.2e}, {rep}")
