@@ -9,9 +9,22 @@
 //             pages).
 //
 // One persistent kernel per GEMM, launched as clusters of two CTAs (one CTA
-// of 192 threads per SM).  Each CTA computes 128x256 output tiles; the two
-// CTAs of a cluster work on a pair of tiles that share an operand, and each
-// loads half of the shared operand and multicasts it to both:
+// of 192 threads per SM), in one of two forms chosen per call:
+//
+// Pair MMA (PAIR = true; batches with at least two 128-row tiles per expert):
+//   the two CTAs run one 256x256 tile together with tcgen05.mma.cta_group::2:
+//   rows 128r..128r+127 come from CTA r's A tile and CTA r holds half of the
+//   256 B columns, so each CTA stages 16 KiB of A and 16 KiB of B per
+//   64-deep k-block (6-stage ring) and its TMEM receives its own 128 rows x
+//   256 columns.  Copies of both CTAs complete on the first CTA's stage
+//   barrier; that CTA's single MMA thread issues M256 N256 K16 MMAs and its
+//   commits release the stage (and hand the accumulator to the epilogue) in
+//   both CTAs.  An expert with an odd tile count pairs its last tile with a
+//   phantom tile whose rows are computed but never stored.
+// Multicast pairs (PAIR = false; decode-sized batches): each CTA computes
+//   its own 128x256 tile with cta_group::1 MMAs; the two CTAs work on a pair
+//   of tiles that share an operand, and each loads half of the shared
+//   operand and multicasts it to both:
 //   M-pair  tiles (m, n) and (m+1, n) of one expert share the 64x256 weight
 //           tile: each CTA loads its own 128x64 A tile and two of the four
 //           64-column B boxes, multicast (32 KiB per CTA per k-block
@@ -19,14 +32,13 @@
 //   N-pair  for the last m-tile of an expert with an odd count, tiles
 //           (m, n) and (m, n+1) share the A tile: each CTA loads 64 of its
 //           128 rows multicast and its own B tile.
+//   A stage is refilled only after both CTAs' MMAs have read it (4 stages).
 // Roles per CTA:
-//   warp 0      TMA producer (one elected thread), 4-stage shared-memory ring
-//               (A 128x64 K-major, B 4 x (64x64) N-major since the weights
-//               are stored [E, K, N]; 128-byte swizzle);
-//   warp 1      TMEM allocator + MMA issuer (one thread): 4 x (M128 N256 K16)
-//               per 64-deep k-block into one of two 256-column accumulators;
-//               its commit frees the stage in both CTAs (a stage is refilled
-//               only after both CTAs' MMAs have read it);
+//   warp 0      TMA producer (one elected thread), shared-memory ring
+//               (A 128x64 K-major, B in 64x64 N-major boxes since the
+//               weights are stored [E, K, N]; 128-byte swizzle);
+//   warp 1      TMEM allocator + MMA issuer (one thread) into one of two
+//               256-column accumulators;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, SwiGLU or gate
 //               scale, global stores; the second accumulator lets the next
 //               tile's MMAs run under this tile's epilogue.
@@ -52,12 +64,22 @@ namespace {
 constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
-constexpr int STAGES = 4;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KiB
 constexpr int A_HALF = A_BYTES / 2;     // 64 rows
 constexpr int B_CHUNK = 64 * BK * 2;    // 8 KiB: 64 N-columns x 64 K-rows
-constexpr int B_BYTES = 4 * B_CHUNK;    // 32 KiB
-constexpr int STAGE_TX = A_BYTES + B_BYTES;
+constexpr int MAX_STAGES = 6;
+// Ring geometry of the two forms (stages, B bytes per CTA and stage).
+template <bool PAIR>
+struct Ring {
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int B_BYTES = (PAIR ? 2 : 4) * B_CHUNK;  // half or all of the 256 B columns
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // bytes that complete one stage: both CTAs' copies (pair MMA: on the first
+  // CTA's barrier) or this CTA's A plus all four B boxes (multicast pairs)
+  static constexpr int STAGE_TX = PAIR ? 2 * STAGE_BYTES : A_BYTES + 4 * B_CHUNK;
+  static constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 1024 /*Ctrl*/;
+};
+static_assert(Ring<true>::SMEM <= 232448 && Ring<false>::SMEM <= 232448, "shared memory budget");
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: the whole TMEM of the SM
 constexpr int NUM_THREADS = 192;
@@ -88,8 +110,8 @@ struct GemmArgs {
 };
 
 struct Ctrl {
-  uint64_t full[STAGES];
-  uint64_t empty[STAGES];
+  uint64_t full[MAX_STAGES];
+  uint64_t empty[MAX_STAGES];
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
@@ -103,9 +125,7 @@ struct Ctrl {
   int uoff[kMaxE + 1];
 };
 
-constexpr int SMEM_BYTES = 1024 /*alignment slack*/ + STAGES * (A_BYTES + B_BYTES) + 1024 /*Ctrl*/;
 static_assert(sizeof(Ctrl) <= 1024, "control block too large");
-static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 struct Tile {
   int e, mt, nt, s;
@@ -114,18 +134,22 @@ struct Tile {
 
 // Units of expert e: its M-pairs ordered (pair group, split, n-tile, pair in
 // group) with the pair fastest, so clusters running together share weight
-// panels; then, for an odd m-tile count, the N-pairs of its last m-tile.
+// panels; then, for an odd m-tile count, the N-pairs of its last m-tile
+// (multicast pairs) or one more M-pair with a phantom second tile (pair MMA).
+template <bool PAIR>
 __device__ __forceinline__ int units_of(int mt_e, int NT, int S) {
+  if (PAIR) return ((mt_e + 1) >> 1) * NT * S;
   return (mt_e >> 1) * NT * S + (mt_e & 1) * ((NT + 1) >> 1) * S;
 }
 
+template <bool PAIR>
 __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S, int rank) {
   Tile t;
   int e = 0;
   while (u >= c.ustart[e + 1]) ++e;
   int r = u - c.ustart[e];
   const int mt_e = c.mtiles[e];
-  const int mp = mt_e >> 1;
+  const int mp = PAIR ? (mt_e + 1) >> 1 : mt_e >> 1;
   const int per = NT * S;
   t.e = e;
   if (r < mp * per) {
@@ -179,30 +203,36 @@ __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Ctrl &
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_half,
                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                        const GemmArgs args) {
+  using RG = Ring<PAIR>;
+  constexpr int STAGES = RG::STAGES;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;
   uint8_t *sB = base + STAGES * A_BYTES;
-  Ctrl &c = *reinterpret_cast<Ctrl *>(sB + STAGES * B_BYTES);
+  Ctrl &c = *reinterpret_cast<Ctrl *>(sB + STAGES * RG::B_BYTES);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int NT = args.num_n_tiles, S = args.splits;
   const int rank = static_cast<int>(ptx::cluster_ctarank());
   const int cluster = static_cast<int>(ptx::cluster_id_x());
   const int nclusters = static_cast<int>(ptx::num_clusters_x());
+  // Pair MMA: CTA 0 of the pair issues every MMA and owns the stage-full and
+  // accumulator-empty barriers that both CTAs signal.
+  const bool leader = !PAIR || rank == 0;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&c.full[s], 1);
-      ptx::mbar_init(&c.empty[s], CLUSTER);  // both CTAs' MMAs release a stage
+      // multicast pairs: both CTAs' MMAs release a stage; pair MMA: one commit
+      ptx::mbar_init(&c.empty[s], PAIR ? 1 : CLUSTER);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&c.tfull[a], 1);
-      ptx::mbar_init(&c.tempty[a], 4);  // one arrive per epilogue warp
+      ptx::mbar_init(&c.tempty[a], PAIR ? 8 : 4);  // one arrive per epilogue warp (of both CTAs for PAIR)
     }
     ptx::mbar_init(&c.drain, 1);
     ptx::mbar_init(&c.exit_bar, 1);
@@ -226,7 +256,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       c.uoff[e] = args.offsets[e];
       c.mtiles[e] = mt;
       c.ustart[e] = acc;
-      acc += units_of(mt, NT, S);
+      acc += units_of<PAIR>(mt, NT, S);
     }
     if (bad) {
       atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
@@ -245,12 +275,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (cluster >= total) return;
 
   if (warp == 1) {
-    ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
-    ptx::tmem_relinquish();
+    if (PAIR) {
+      ptx::tmem_alloc_pair(&c.tmem_base, TMEM_COLS);  // with the peer CTA's warp 1
+      ptx::tmem_relinquish_pair();
+    } else {
+      ptx::tmem_alloc(&c.tmem_base, TMEM_COLS);
+      ptx::tmem_relinquish();
+    }
   }
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
-    ptx::prefetch_tmap(&tmA_half);
+    if (!PAIR) ptx::prefetch_tmap(&tmA_half);
     ptx::prefetch_tmap(&tmB0);
     if (MODE == MODE_GATE_UP) ptx::prefetch_tmap(&tmB1);
   }
@@ -271,45 +306,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t pol_b = ptx::policy_evict_normal();
       bool ok = true;
       for (int u = cluster; ok && u < total; u += nclusters) {
-        const Tile t = decode_unit(u, c, NT, S, rank);
+        const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
         const int row0 = c.poff[t.e] + t.mt * BM;
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
         for (int kb = kb0; kb < kb1; ++kb) {
           if (!wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, true)) { ok = false; break; }
-          uint64_t *bar = &c.full[p_stage];
-          ptx::mbar_arrive_expect_tx(bar, STAGE_TX);  // own and peer copies together fill the stage
           uint8_t *a_dst = sA + p_stage * A_BYTES;
-          uint8_t *b_dst = sB + p_stage * B_BYTES;
+          uint8_t *b_dst = sB + p_stage * RG::B_BYTES;
           const int k0 = kb * BK;
-          if (!t.npair) {
-            ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);
-            // this CTA's two of the four B boxes, delivered to both CTAs
+          if (PAIR) {
+            // both CTAs' copies complete on the first CTA's barrier, which
+            // expects the bytes of both
+            if (leader) ptx::mbar_arrive_expect_tx(&c.full[p_stage], RG::STAGE_TX);
+            const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[p_stage]), 0);
+            ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, row0, pol_a);
             if (MODE == MODE_GATE_UP) {
+              // CTA 0 holds the W1 half of the 256 columns, CTA 1 the W3 half
               const int n0 = t.nt * (BN / 2);
-              const CUtensorMap *mb = rank == 0 ? &tmB0 : &tmB1;  // W1 boxes from rank 0, W3 boxes from rank 1
-              ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, mb, bar, n0, k0, t.e, kBothCtas, pol_b);
-              ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, mb, bar, n0 + 64, k0, t.e, kBothCtas, pol_b);
+              const CUtensorMap *mb = rank == 0 ? &tmB0 : &tmB1;
+              ptx::tma_load_3d_pair(b_dst, mb, bar, n0, k0, t.e, pol_b);
+              ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, n0 + 64, k0, t.e, pol_b);
             } else {
-              const int n0 = t.nt * BN;
-              ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank), k0, t.e, kBothCtas,
-                                  pol_b);
-              ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank + 1), k0, t.e,
-                                  kBothCtas, pol_b);
+              const int n0 = t.nt * BN + rank * (BN / 2);
+              ptx::tma_load_3d_pair(b_dst, &tmB0, bar, n0, k0, t.e, pol_b);
+              ptx::tma_load_3d_pair(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, k0, t.e, pol_b);
             }
           } else {
-            // this CTA's 64 of the shared 128 A rows, delivered to both CTAs
-            ptx::tma_load_2d_mc(a_dst + rank * A_HALF, &tmA_half, bar, k0, row0 + 64 * rank, kBothCtas, pol_a);
-            if (MODE == MODE_GATE_UP) {
-              const int n0 = t.nt * (BN / 2);
-              ptx::tma_load_3d(b_dst, &tmB0, bar, n0, k0, t.e, pol_b);
-              ptx::tma_load_3d(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, k0, t.e, pol_b);
-              ptx::tma_load_3d(b_dst + 2 * B_CHUNK, &tmB1, bar, n0, k0, t.e, pol_b);
-              ptx::tma_load_3d(b_dst + 3 * B_CHUNK, &tmB1, bar, n0 + 64, k0, t.e, pol_b);
+            uint64_t *bar = &c.full[p_stage];
+            ptx::mbar_arrive_expect_tx(bar, RG::STAGE_TX);  // own and peer copies together fill the stage
+            if (!t.npair) {
+              ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);
+              // this CTA's two of the four B boxes, delivered to both CTAs
+              if (MODE == MODE_GATE_UP) {
+                const int n0 = t.nt * (BN / 2);
+                const CUtensorMap *mb = rank == 0 ? &tmB0 : &tmB1;  // W1 boxes from rank 0, W3 boxes from rank 1
+                ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, mb, bar, n0, k0, t.e, kBothCtas, pol_b);
+                ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, mb, bar, n0 + 64, k0, t.e, kBothCtas, pol_b);
+              } else {
+                const int n0 = t.nt * BN;
+                ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank), k0, t.e,
+                                    kBothCtas, pol_b);
+                ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank + 1), k0, t.e,
+                                    kBothCtas, pol_b);
+              }
             } else {
-              const int n0 = t.nt * BN;
+              // this CTA's 64 of the shared 128 A rows, delivered to both CTAs
+              ptx::tma_load_2d_mc(a_dst + rank * A_HALF, &tmA_half, bar, k0, row0 + 64 * rank, kBothCtas, pol_a);
+              if (MODE == MODE_GATE_UP) {
+                const int n0 = t.nt * (BN / 2);
+                ptx::tma_load_3d(b_dst, &tmB0, bar, n0, k0, t.e, pol_b);
+                ptx::tma_load_3d(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, k0, t.e, pol_b);
+                ptx::tma_load_3d(b_dst + 2 * B_CHUNK, &tmB1, bar, n0, k0, t.e, pol_b);
+                ptx::tma_load_3d(b_dst + 3 * B_CHUNK, &tmB1, bar, n0 + 64, k0, t.e, pol_b);
+              } else {
+                const int n0 = t.nt * BN;
 #pragma unroll
-              for (int j = 0; j < 4; ++j) ptx::tma_load_3d(b_dst + j * B_CHUNK, &tmB0, bar, n0 + 64 * j, k0, t.e, pol_b);
+                for (int j = 0; j < 4; ++j)
+                  ptx::tma_load_3d(b_dst + j * B_CHUNK, &tmB0, bar, n0 + 64 * j, k0, t.e, pol_b);
+              }
             }
           }
           issued |= 1u << p_stage;
@@ -320,14 +375,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else if (warp == 1) {
     // ------------------------------------------------------------ MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(BM, BN, /*A MN-major*/ false, /*B MN-major*/ true);
+    if (lane == 0 && leader) {
+      // pair MMA: M = 256 over both CTAs' rows
+      constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false,
+                                                     /*B MN-major*/ true);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
       for (int u = cluster; ok && u < total; u += nclusters) {
-        const Tile t = decode_unit(u, c, NT, S, rank);
+        const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
         const int acc = local & 1;
@@ -339,30 +396,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!wait_bounded(&c.full[stage], phase, c, args.status, true)) { ok = false; break; }
           ptx::tc_fence_after();
           const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
-          const uint32_t b_addr = ptx::smem_u32(sB + stage * B_BYTES);
+          const uint32_t b_addr = ptx::smem_u32(sB + stage * RG::B_BYTES);
 #pragma unroll
           for (int ks = 0; ks < BK / 16; ++ks) {
             // A: K-major, 128 B rows, 8-row groups 1024 B apart; K step = 32 B.
             const uint64_t ad = ptx::smem_desc_sw128(a_addr + ks * 32, 16, 1024);
             // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO); K step = 16 rows.
             const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 2048, B_CHUNK, 1024);
-            ptx::mma_bf16(d_tmem, ad, bd, idesc, (kb > kb0 || ks > 0) ? 1u : 0u);
+            const uint32_t accum = (kb > kb0 || ks > 0) ? 1u : 0u;
+            if (PAIR) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+            else ptx::mma_bf16(d_tmem, ad, bd, idesc, accum);
           }
           // frees the stage in both CTAs once these MMAs have read it
-          ptx::mma_commit_mc(&c.empty[stage], kBothCtas);
+          if (PAIR) ptx::mma_commit_pair_mc(&c.empty[stage], kBothCtas);
+          else ptx::mma_commit_mc(&c.empty[stage], kBothCtas);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
-        ptx::mma_commit(&c.tfull[acc]);      // accumulator ready for the epilogue
+        // accumulator ready for the epilogue (of both CTAs for pair MMA)
+        if (PAIR) ptx::mma_commit_pair_mc(&c.tfull[acc], kBothCtas);
+        else ptx::mma_commit(&c.tfull[acc]);
         ++local;
       }
     }
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    // where this warp reports a drained accumulator: the MMA-issuing CTA
+    const uint32_t tempty_at0 = ptx::mapa_shared(ptx::smem_u32(&c.tempty[0]), PAIR ? 0 : rank);
+    const uint32_t tempty_at1 = ptx::mapa_shared(ptx::smem_u32(&c.tempty[1]), PAIR ? 0 : rank);
     int local = 0;
     for (int u = cluster; u < total; u += nclusters) {
-      const Tile t = decode_unit(u, c, NT, S, rank);
+      const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
       const int acc = local & 1;
       const uint32_t apar = (local >> 1) & 1;
       int ok = 1;
@@ -371,9 +436,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (!ok) break;
       ptx::tc_fence_after();
       // This thread's accumulator row: padded grouped row `row`; the first
-      // count_e rows of an expert's segment are real, the rest padding.
+      // count_e rows of an expert's segment are real, the rest padding, and
+      // rows past the segment (the phantom tile of pair MMA) are not stored.
       const int seg_row = t.mt * BM + q * 32 + lane;
       const int row = c.poff[t.e] + seg_row;
+      const bool in_seg = seg_row < c.mtiles[t.e] * BM;
       const bool real = seg_row < c.uoff[t.e + 1] - c.uoff[t.e];
       const int ru = c.uoff[t.e] + seg_row;  // unpadded grouped row (valid if real)
       const uint32_t tbase = tmem + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
@@ -398,16 +465,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
               const int col = n0 + cc * 32;
               __nv_bfloat16 *dst = H + static_cast<size_t>(row) * args.n_out + col;
+              if (in_seg) {
 #pragma unroll
-              for (int vv = 0; vv < 4; ++vv)
-                if (col + vv * 8 < args.n_out)
-                  *reinterpret_cast<uint4 *>(dst + vv * 8) =
-                      make_uint4(packed[4 * vv], packed[4 * vv + 1], packed[4 * vv + 2], packed[4 * vv + 3]);
+                for (int vv = 0; vv < 4; ++vv)
+                  if (col + vv * 8 < args.n_out)
+                    *reinterpret_cast<uint4 *>(dst + vv * 8) =
+                        make_uint4(packed[4 * vv], packed[4 * vv + 1], packed[4 * vv + 2], packed[4 * vv + 3]);
+              }
             }
           }
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
+          if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
         } else {
           // Split contraction: store this split's fp32 sums of the real rows,
           // release the accumulator, and let the CTA that completes the tile
@@ -441,7 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
           ptx::tc_fence_before();
           __syncwarp();
-          if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
+          if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
           if (n0 < args.n_out) {
             // One arrival counter per (m-tile, n-tile, lane quarter): each
             // epilogue warp completes its own 32 rows, with no cross-warp wait.
@@ -531,14 +600,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(&c.tempty[acc]);
+        if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
       }
       ++local;
     }
   }
 
-  // Producer tail: every stage's last release (by both CTAs' MMAs) has
-  // arrived, so no remote arrive can still land in this CTA's barriers.
+  // Producer tail: every stage's last release has arrived, so no commit can
+  // still land in this CTA's barriers.
   if (warp == 0 && lane == 0) {
     for (int i = 0; i < STAGES; ++i) {
       wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, false);
@@ -549,14 +618,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   if (*reinterpret_cast<volatile int *>(&c.abort)) {
     // Some role gave up: before TMEM and shared memory are released, wait
-    // (bounded) for this CTA's MMAs and for every copy it expects.
-    if (warp == 1 && lane == 0) {
-      ptx::mma_commit(&c.drain);
+    // (bounded) for the MMAs this CTA issued and for every copy completing on
+    // its barriers.
+    if (warp == 1 && lane == 0 && leader) {
+      if (PAIR) ptx::mma_commit_pair(&c.drain);
+      else ptx::mma_commit(&c.drain);
       wait_bounded(&c.drain, 0, c, args.status, false);
     }
-    if (warp == 0 && lane == 0) {
+    if (warp == 0 && lane == 0 && leader) {
       for (int s = 0; s < STAGES; ++s)
         if (issued & (1u << s)) wait_bounded(&c.full[s], (last_par >> s) & 1u, c, args.status, false);
+    }
+    if (PAIR && warp == 0 && lane == 0) {
+      // Pair MMA: a CTA's copies complete on its partner's barriers, which
+      // cannot tell this CTA when they have landed; copies take microseconds,
+      // so give any still in flight 50 us before shared memory is released.
+      const uint64_t t0 = ptx::globaltimer_ns();
+      while (ptx::globaltimer_ns() - t0 < 50000ull) {
+      }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -569,7 +648,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __syncthreads();
   if (warp == 1) {
     ptx::tc_fence_after();
-    ptx::tmem_dealloc(tmem, TMEM_COLS);
+    if (PAIR) ptx::tmem_dealloc_pair(tmem, TMEM_COLS);  // with the peer CTA's warp 1
+    else ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
 }
 
@@ -621,6 +701,28 @@ struct DevState {
   int clusters = 0;
 };
 
+template <int MODE, bool PAIR>
+cudaError_t set_smem_attr() {
+  return cudaFuncSetAttribute(expert_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Ring<PAIR>::SMEM);
+}
+
+template <bool PAIR>
+cudaError_t max_clusters(int num_sms, int *n) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((num_sms / CLUSTER) * CLUSTER);
+  cfg.blockDim = dim3(NUM_THREADS);
+  cfg.dynamicSmemBytes = Ring<PAIR>::SMEM;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaOccupancyMaxActiveClusters(n, expert_gemm_kernel<MODE_GATE_UP, PAIR>, &cfg);
+}
+
 cudaError_t device_state(int num_sms, int *clusters) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
@@ -630,26 +732,16 @@ cudaError_t device_state(int num_sms, int *clusters) {
   static DevState st[64];
   std::lock_guard<std::mutex> lock(mu);
   if (!st[dev].ready) {
-    err = cudaFuncSetAttribute(expert_gemm_kernel<MODE_GATE_UP>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               SMEM_BYTES);
-    if (err == cudaSuccess)
-      err = cudaFuncSetAttribute(expert_gemm_kernel<MODE_DOWN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 SMEM_BYTES);
+    err = set_smem_attr<MODE_GATE_UP, false>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, false>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, true>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, true>();
     if (err != cudaSuccess) return err;
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((num_sms / CLUSTER) * CLUSTER);
-    cfg.blockDim = dim3(NUM_THREADS);
-    cfg.dynamicSmemBytes = SMEM_BYTES;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = CLUSTER;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    int n = 0;
-    err = cudaOccupancyMaxActiveClusters(&n, expert_gemm_kernel<MODE_GATE_UP>, &cfg);
+    int n0 = 0, n1 = 0;
+    err = max_clusters<false>(num_sms, &n0);
+    if (err == cudaSuccess) err = max_clusters<true>(num_sms, &n1);
     if (err != cudaSuccess) return err;
+    const int n = n0 < n1 ? n0 : n1;  // one persistent grid size for both forms
     if (n < 1) return cudaErrorInvalidConfiguration;
     st[dev].clusters = n;
     st[dev].ready = true;
@@ -658,13 +750,13 @@ cudaError_t device_state(int num_sms, int *clusters) {
   return cudaSuccess;
 }
 
-template <int MODE>
+template <int MODE, bool PAIR>
 cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMap &a, const CUtensorMap &ah,
                         const CUtensorMap &b0, const CUtensorMap &b1, const GemmArgs &args) {
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(clusters * CLUSTER);
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = SMEM_BYTES;
+  cfg.dynamicSmemBytes = Ring<PAIR>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -675,7 +767,7 @@ cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMa
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE>, a, ah, b0, b1, args);
+  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE, PAIR>, a, ah, b0, b1, args);
 }
 
 }  // namespace
@@ -710,7 +802,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.splits = L.S_gu;
   g1.kb_per_split = L.kb_per_split_gu;
   g1.status = P.status;
-  err = launch_gemm<MODE_GATE_UP>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
+  err = L.pair ? launch_gemm<MODE_GATE_UP, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
+               : launch_gemm<MODE_GATE_UP, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
@@ -724,7 +817,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
-  return launch_gemm<MODE_DOWN>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2);
+  return L.pair ? launch_gemm<MODE_DOWN, true>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2)
+                : launch_gemm<MODE_DOWN, false>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2);
 }
 
 }  // namespace moe

@@ -55,6 +55,7 @@ struct WsLayout {
   int kb_per_split;
   int S_gu;           // split count over the contraction of the gate/up projection
   int kb_per_split_gu;
+  bool pair;          // run the expert GEMMs as CTA-pair (cta_group::2) 256-row tiles
   int n_route_blocks;
 };
 

@@ -138,6 +138,10 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   L.kb_per_split = down.kb_per_split;
   L.S_gu = gu.S;
   L.kb_per_split_gu = gu.kb_per_split;
+  // CTA-pair MMAs once experts average two or more 128-row tiles: the pair
+  // halves each CTA's weight-tile traffic and shared-memory footprint; with
+  // fewer rows the phantom half-tile of an odd tile count would dominate.
+  L.pair = dtype == MOE_BF16 && touched > 0 && TKl >= 2LL * kSegPad * touched && L.S_gu == 1;
   const size_t TK = static_cast<size_t>(T) * K;
   const size_t R = static_cast<size_t>(L.R);
   size_t o = 0;

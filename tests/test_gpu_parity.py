@@ -101,6 +101,11 @@ def _bf16_inputs(T, d, f, E, K, seed):
     (5, 2056, 1160, 8, 2),
     (3, 1544, 904, 6, 2),
     (24, 1048, 1096, 3, 1),
+    # CTA-pair (256-row) tiles: two or more 128-row tiles per expert; odd
+    # tile counts leave a phantom half tile; ragged N/K tails; top-1
+    (1100, 512, 1024, 4, 2),
+    (2500, 520, 1032, 8, 2),
+    (700, 256, 384, 2, 1),
 ])
 def test_bf16_shapes(moe, T, d, f, E, K):
     inp = _bf16_inputs(T, d, f, E, K, seed=100 + T)
@@ -115,8 +120,9 @@ def test_bf16_e1_k1_is_plain_swiglu(moe):
     assert parity.rel_linf(_np(out.float()), want) <= 2e-2
 
 
-def test_bf16_deterministic(moe):
-    inp = _bf16_inputs(700, 512, 1024, 8, 2, seed=5)
+@pytest.mark.parametrize("T", [700, 2100])   # 128-row tiles (multicast pairs) and CTA-pair tiles
+def test_bf16_deterministic(moe, T):
+    inp = _bf16_inputs(T, 512, 1024, 8, 2, seed=5)
     a, ia, ga, pa, oa, sa = _run(moe, inp)
     b, ib, gb, pb, ob, sb = _run(moe, inp)
     assert torch.equal(a, b) and torch.equal(ia, ib) and torch.equal(ga, gb) and torch.equal(pa, pb)
