@@ -78,6 +78,14 @@ enum { MOE_BF16 = 0, MOE_F32 = 1 };
 /* moe_forward flags. */
 #define MOE_ACCUMULATE   0x1u  /* y += MoE(x) instead of y = MoE(x) (residual stream) */
 #define MOE_DEBUG_CHECKS 0x2u  /* device-side range and finiteness checks */
+/* Failure-path test hook (bf16 only): the gate/up expert GEMM first waits on a
+ * barrier that nothing signals, so its bounded wait expires after about one
+ * second; the kernel then stops issuing, drains its own copies and MMAs, frees
+ * its tensor memory and returns, and the call's status word reads
+ * MOE_ERR_DEVICE_TIMEOUT.  The outputs of such a call are unspecified; the
+ * context stays usable.  With MOE_F32 the flag is rejected (that path has no
+ * waits). */
+#define MOE_DEBUG_FORCE_TIMEOUT 0x4u
 
 /*
  * Workspace size in bytes for moe_forward / moe_route with these sizes, or 0
@@ -108,7 +116,7 @@ MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype)
  *   workspace / ws_bytes: device buffer of at least moe_workspace_bytes().
  *     Calls sharing one workspace must be ordered on the GPU (same stream or
  *     synchronised); concurrent calls need separate workspaces.
- *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS.
+ *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT.
  * Returns MOE_OK once every kernel is enqueued.
  */
 MOE_API int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,

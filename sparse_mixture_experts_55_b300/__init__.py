@@ -18,8 +18,8 @@ import ctypes
 import torch
 
 from . import _lib
-from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_F32, MoEError,  # noqa: F401
-                   status_string)
+from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_TIMEOUT, MOE_F32,  # noqa: F401
+                   MoEError, status_string)
 
 __all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",

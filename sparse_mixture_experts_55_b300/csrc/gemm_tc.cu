@@ -85,7 +85,7 @@ constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: the whole TMEM of the SM
 constexpr int NUM_THREADS = 192;
 constexpr int CLUSTER = 2;
 constexpr uint16_t kBothCtas = 0x3;
-constexpr int GROUP_PAIRS = 4;           // M-pairs rastered together (weight reuse in L2)
+constexpr int GROUP_PAIRS = 16;          // M-pairs rastered together (weight reuse in L2)
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
@@ -106,6 +106,7 @@ struct GemmArgs {
   int num_kb;               // k-blocks of 64 over the contraction
   int splits;
   int kb_per_split;
+  int force_timeout;        // failure-path test: wait on a barrier nothing signals first
   int *status;
 };
 
@@ -115,6 +116,7 @@ struct Ctrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t stall;           // never signalled (failure-path test)
   uint64_t exit_bar;        // the peer CTA's "done issuing" arrival
   uint32_t tmem_base;
   int abort;
@@ -235,6 +237,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&c.tempty[a], PAIR ? 8 : 4);  // one arrive per epilogue warp (of both CTAs for PAIR)
     }
     ptx::mbar_init(&c.drain, 1);
+    ptx::mbar_init(&c.stall, 1);
     ptx::mbar_init(&c.exit_bar, 1);
     ptx::fence_barrier_init();
   }
@@ -383,6 +386,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
+      // failure-path test: this wait expires, raising the CTA's abort flag
+      if (args.force_timeout) ok = wait_bounded(&c.stall, 0, c, args.status, true);
       for (int u = cluster; ok && u < total; u += nclusters) {
         const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
         const int kb0 = t.s * args.kb_per_split;
@@ -607,8 +612,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
 
   // Producer tail: every stage's last release has arrived, so no commit can
-  // still land in this CTA's barriers.
-  if (warp == 0 && lane == 0) {
+  // still land in this CTA's barriers.  (After an abort some releases never
+  // come; the drain below covers that case.)
+  if (warp == 0 && lane == 0 && !*reinterpret_cast<volatile int *>(&c.abort)) {
     for (int i = 0; i < STAGES; ++i) {
       wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, false);
       if (++p_stage == STAGES) { p_stage = 0; p_phase ^= 1u; }
@@ -775,7 +781,6 @@ cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMa
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
                                      cudaStream_t s, void *const *mid_event) {
-  (void)flags;
   int clusters = 0;
   cudaError_t err = device_state(num_sms, &clusters);
   if (err != cudaSuccess) return err;
@@ -801,6 +806,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.num_kb = (d + BK - 1) / BK;
   g1.splits = L.S_gu;
   g1.kb_per_split = L.kb_per_split_gu;
+  g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
   g1.status = P.status;
   err = L.pair ? launch_gemm<MODE_GATE_UP, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
                : launch_gemm<MODE_GATE_UP, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
@@ -812,6 +818,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.out_split_stride = static_cast<long long>(g1.tk) * d;
   g2.part = nullptr;
   g2.tile_cnt = nullptr;
+  g2.force_timeout = 0;
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + BK - 1) / BK;

@@ -13,12 +13,13 @@ namespace moe {
 // Rows of every expert segment in the grouped buffers are padded to a
 // multiple of this, so a 128-row MMA tile never straddles two experts.
 constexpr int kSegPad = 128;
-// Tokens per router block (each block writes one expert histogram).
-constexpr int kRouteTokens = 16;
+// Router blocks: kRouteThreads threads, each owning one 16-byte slice of d;
+// a block routes route_tpb consecutive tokens (a multiple of kRouteGroup,
+// sized so that the grid is about one wave) and writes one expert histogram.
 constexpr int kRouteThreads = 512;
-// Tokens whose (token, slot) entries one grouping block ranks; a multiple of kRouteTokens.
+constexpr int kRouteGroup = 4;
+// Tokens whose (token, slot) entries one grouping block ranks.
 constexpr int kGroupTokens = 256;
-static_assert(kGroupTokens % kRouteTokens == 0, "grouping chunk must cover whole router blocks");
 constexpr int kMaxE = 32;
 constexpr int kMaxK = 2;
 // Status-word slots at the start of the workspace.
@@ -56,6 +57,7 @@ struct WsLayout {
   int S_gu;           // split count over the contraction of the gate/up projection
   int kb_per_split_gu;
   bool pair;          // run the expert GEMMs as CTA-pair (cta_group::2) 256-row tiles
+  int route_tpb;      // tokens per router block
   int n_route_blocks;
 };
 
@@ -89,9 +91,8 @@ Ptrs carve(void *ws, const WsLayout &L);
 
 // -------- routing.cu
 cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
-                         const Ptrs &P, cudaStream_t s);
-cudaError_t launch_group(int T, int E, int K, int n_route_blocks, unsigned flags, const Ptrs &P,
-                         cudaStream_t s);
+                         const WsLayout &L, const Ptrs &P, cudaStream_t s);
+cudaError_t launch_group(int T, int E, int K, const WsLayout &L, unsigned flags, const Ptrs &P, cudaStream_t s);
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
                           cudaStream_t s);
 cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsigned flags, const Ptrs &P,

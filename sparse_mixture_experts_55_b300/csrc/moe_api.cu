@@ -115,7 +115,12 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   WsLayout L{};
   const size_t eb = elem_bytes(dtype);
   L.R = static_cast<int>(align_up(static_cast<size_t>(T) * K + static_cast<size_t>(E) * (kSegPad - 1), kSegPad));
-  L.n_route_blocks = (T + kRouteTokens - 1) / kRouteTokens;
+  {
+    // about one wave of router blocks: ceil(T / SMs) tokens each, in groups of kRouteGroup
+    const int per = (T + num_sms - 1) / (num_sms > 0 ? num_sms : 1);
+    L.route_tpb = ((per > 0 ? per : 1) + kRouteGroup - 1) / kRouteGroup * kRouteGroup;
+    L.n_route_blocks = (T + L.route_tpb - 1) / L.route_tpb;
+  }
   const long long TKl = static_cast<long long>(T) * K;
   L.TK = static_cast<int>(TKl);
   const long long touched = TKl < E ? TKl : E;
@@ -209,7 +214,8 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
                         unsigned flags, moe_stream_t stream, void *const *events) {
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
-  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if ((flags & MOE_DEBUG_FORCE_TIMEOUT) && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;  // empty input: nothing to compute, x and y may be NULL
   if (!x || !Wg || !W1 || !W3 || !W2 || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(y))
@@ -232,9 +238,9 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
   };
   cudaError_t err = mark(0);
-  if (err == cudaSuccess) err = launch_route(x, Wg, T, d, E, K, dtype, flags, P, s);
+  if (err == cudaSuccess) err = launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s);
   if (err == cudaSuccess) err = mark(1);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L.n_route_blocks, flags, P, s);
+  if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
   if (err == cudaSuccess) err = mark(2);
   if (err == cudaSuccess) err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
   if (err == cudaSuccess) err = mark(3);
@@ -261,7 +267,7 @@ int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, c
                       moe_stream_t stream) {
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
-  if (flags & ~MOE_DEBUG_CHECKS) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
   if (!(eps > 0.f)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!h || !aligned16(h)) return MOE_ERR_INVALID_ARG;
@@ -313,8 +319,8 @@ int moe_route(const void *x, const void *Wg, int T, int d, int E, int K, int dty
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Ptrs P = carve(workspace, L);
   if (cudaMemsetAsync(P.status, 0, kStatusInts * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, 0, P, s);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L.n_route_blocks, 0, P, s);
+  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, 0, L, P, s);
+  if (err == cudaSuccess) err = launch_group(T, E, K, L, 0, P, s);
   if (err == cudaSuccess) err = launch_route_export(T, E, K, P, idx, gate, perm_tok, offsets, pos, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -28,7 +28,7 @@ namespace {
 
 // Routing scratch for T <= MOE_ROUTE_NOALLOC_MAX_T tokens, K <= 2, E <= 32:
 // status word, idx, gate, block histograms, offsets, pos and the padded
-// grouped token/gate arrays (about 801 KiB at the limit).
+// grouped token/gate arrays (under 0.7 MiB at the limit).
 constexpr size_t kNoAllocBytes = 1024 * 1024;
 static __device__ __align__(256) unsigned char g_route_scratch[kNoAllocBytes];
 
@@ -91,8 +91,8 @@ extern "C" int moe_route_noalloc(const void *x, const void *Wg, int T, int d, in
   // The status word must start at zero; every other scratch word the kernels
   // read is written earlier in the same call.
   if (cudaMemsetAsync(P.status, 0, kStatusInts * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, 0, P, s);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L.n_route_blocks, 0, P, s);
+  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, 0, L, P, s);
+  if (err == cudaSuccess) err = launch_group(T, E, K, L, 0, P, s);
   if (err == cudaSuccess) err = launch_route_export(T, E, K, P, idx, gate, perm_tok, offsets, pos, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

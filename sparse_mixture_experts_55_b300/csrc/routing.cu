@@ -191,7 +191,7 @@ __device__ __forceinline__ void select_and_store(const float (&l)[EP], int t, in
   atomicAdd(&s_cnt[i2], 1);
 }
 
-// One block routes kRouteTokens tokens.  Thread i owns the i-th 16-byte slice
+// One block routes tpb consecutive tokens.  Thread i owns the i-th 16-byte slice
 // of d (8 bf16 or 4 fp32 columns).  With up to 8 experts it keeps its rows of
 // W_g in registers for all the block's tokens; the x slices of the next group
 // of tokens are loaded while the current group is reduced.  Per token, each
@@ -199,19 +199,19 @@ __device__ __forceinline__ void select_and_store(const float (&l)[EP], int t, in
 // fixed order, so the logits are deterministic.
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, unsigned flags,
-                 int32_t *__restrict__ idx, float *__restrict__ gate, int32_t *__restrict__ blockcounts,
-                 int *status) {
+    route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
+                 unsigned flags, int32_t *__restrict__ idx, float *__restrict__ gate,
+                 int32_t *__restrict__ blockcounts, int *status) {
   constexpr int NV = Vec<Tin>::N;
   constexpr int NW = kRouteThreads / 32;
-  constexpr int G = 4;  // tokens per reduction group
+  constexpr int G = kRouteGroup;  // tokens per reduction group
   constexpr bool kCached = EP == 8;
   __shared__ float s_red[G][NW][EP];
   __shared__ float s_log[G][EP];
   __shared__ int s_cnt[kMaxE];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int t0 = blockIdx.x * kRouteTokens;
-  const int nt = min(kRouteTokens, T - t0);
+  const int t0 = blockIdx.x * tpb;
+  const int nt = min(tpb, T - t0);
   const int nchunks = d / NV;
   if (tid < kMaxE) s_cnt[tid] = 0;
   pdl_wait();
@@ -270,7 +270,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // and gate 0.  pos[t, k] is the entry's row in the unpadded grouped order
 // (offsets[e] + rank), which indexes the compact expert-output buffer.
 __global__ void __launch_bounds__(kGroupTokens *kMaxK)
-    group_kernel(int T, int E, int K, int nb_route, unsigned flags, const int32_t *__restrict__ idx,
+    group_kernel(int T, int E, int K, int nb_route, int tpb, unsigned flags, const int32_t *__restrict__ idx,
                  const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
                  int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status) {
   constexpr int NT = kGroupTokens * kMaxK;
@@ -284,12 +284,19 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
-  const int rb_before = b * (kGroupTokens / kRouteTokens);  // router blocks ahead of this chunk
+  // entries ahead of this chunk: whole router blocks from their histograms,
+  // plus the part of the router block it starts in, counted from idx
+  const int tok0 = b * kGroupTokens;
+  const int rb_full = tok0 / tpb;
   for (int i = tid; i < nb_route * E; i += NT) {
     const int rb = i / E, e = i - rb * E;
     const int c = blockcounts[i];
     atomicAdd(&s_tot[e], c);
-    if (rb < rb_before) atomicAdd(&s_base[e], c);
+    if (rb < rb_full) atomicAdd(&s_base[e], c);
+  }
+  for (int i = rb_full * tpb * K + tid; i < tok0 * K; i += NT) {
+    const int e = idx[i];
+    if (e >= 0 && e < E) atomicAdd(&s_base[e], 1);
   }
   __syncthreads();
   if (tid == 0) {
@@ -480,32 +487,33 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T
 }  // namespace
 
 cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
-                         const Ptrs &P, cudaStream_t s) {
+                         const WsLayout &L, const Ptrs &P, cudaStream_t s) {
   // First kernel of a forward pass: an ordinary launch, ordered after all
   // earlier work in the stream.
-  const dim3 grid((T + kRouteTokens - 1) / kRouteTokens), block(kRouteThreads);
+  const dim3 grid(L.n_route_blocks), block(kRouteThreads);
+  const int tpb = L.route_tpb;
   if (dtype == MOE_BF16) {
     auto *xx = static_cast<const __nv_bfloat16 *>(x);
     auto *ww = static_cast<const __nv_bfloat16 *>(Wg);
     if (E <= 8)
-      return launch_kernel(route_kernel<__nv_bfloat16, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags,
+      return launch_kernel(route_kernel<__nv_bfloat16, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags,
                            P.idx, P.gate, P.blockcounts, P.status);
-    return launch_kernel(route_kernel<__nv_bfloat16, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags,
+    return launch_kernel(route_kernel<__nv_bfloat16, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags,
                          P.idx, P.gate, P.blockcounts, P.status);
   }
   auto *xx = static_cast<const float *>(x);
   auto *ww = static_cast<const float *>(Wg);
   if (E <= 8)
-    return launch_kernel(route_kernel<float, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags, P.idx,
+    return launch_kernel(route_kernel<float, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags, P.idx,
                          P.gate, P.blockcounts, P.status);
-  return launch_kernel(route_kernel<float, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, flags, P.idx,
+  return launch_kernel(route_kernel<float, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags, P.idx,
                        P.gate, P.blockcounts, P.status);
 }
 
-cudaError_t launch_group(int T, int E, int K, int nb_route, unsigned flags, const Ptrs &P, cudaStream_t s) {
+cudaError_t launch_group(int T, int E, int K, const WsLayout &L, unsigned flags, const Ptrs &P, cudaStream_t s) {
   const dim3 grid((T + kGroupTokens - 1) / kGroupTokens), block(kGroupTokens * kMaxK);
-  return launch_kernel(group_kernel, grid, block, 0, s, true, T, E, K, nb_route, flags, P.idx, P.gate,
-                       P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status);
+  return launch_kernel(group_kernel, grid, block, 0, s, true, T, E, K, L.n_route_blocks, L.route_tpb, flags, P.idx,
+                       P.gate, P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status);
 }
 
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,

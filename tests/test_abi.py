@@ -96,6 +96,12 @@ def test_forward_rejects_bad_arguments_on_host(lib, kw, code):
     assert _fwd(lib, **kw) == code
 
 
+def test_forced_timeout_flag_is_bf16_only(lib):
+    assert _fwd(lib, flags=_lib.MOE_DEBUG_FORCE_TIMEOUT, dtype=_lib.MOE_F32) == _lib.MOE_ERR_UNSUPPORTED
+    # accepted for bf16: the call goes on to the workspace check
+    assert _fwd(lib, flags=_lib.MOE_DEBUG_FORCE_TIMEOUT, ws_bytes=1) == _lib.MOE_ERR_WORKSPACE
+
+
 def test_fp32_multiple_of_4_is_accepted_by_shape_check(lib):
     # d = 60 is fine for fp32 (16-byte rows); with a 1-byte workspace the call
     # stops at the workspace check, after the shape checks passed.

@@ -201,3 +201,24 @@ def test_block_stack_small(moe, dt, tol_key):
         wts = W.stack_layer_weights(l, d, f, E, device=dev, dtype=dt)
         err_y, err_h, rep = check_stack_layer(moe, h, wts, K, toks, ws, tol_key)
         print(f"layer {l}: rel err y {err_y:.2e}, residual {err_h:.2e}, {rep}")
+
+
+@pytest.mark.parametrize("T", [300, 2100])   # multicast-pair and CTA-pair GEMM forms
+def test_forced_timeout_is_reported_and_context_survives(moe, T):
+    """The failure path of the bounded waits: with MOE_DEBUG_FORCE_TIMEOUT the
+    gate/up GEMM waits on a barrier nothing signals; the wait expires, the
+    call's status reads MOE_ERR_DEVICE_TIMEOUT, and the next call on the same
+    workspace runs normally and matches the oracle."""
+    import time
+    dev = torch.device("cuda:0")
+    inp = _bf16_inputs(T, 512, 1024, 8, 2, seed=17)
+    g = inp.to(dev)
+    ws = moe.Workspace(T, 512, 1024, 8, 2, torch.bfloat16, dev)
+    t0 = time.time()
+    moe.moe_forward(g.x, g.Wg, g.W1, g.W3, g.W2, 2, workspace=ws, flags=moe.MOE_DEBUG_FORCE_TIMEOUT)
+    assert moe.moe_read_status(ws) == 5          # MOE_ERR_DEVICE_TIMEOUT
+    assert time.time() - t0 < 30.0
+    y = moe.moe_forward(g.x, g.Wg, g.W1, g.W3, g.W2, 2, workspace=ws)
+    assert moe.moe_read_status(ws) == 0
+    ref = oracle.moe_layer(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, 2)
+    assert parity.rel_linf(_np(y.float()), ref.y) <= parity.TOL["bf16"]
