@@ -21,7 +21,7 @@ from . import _lib
 from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_TIMEOUT, MOE_F32,  # noqa: F401
                    MoEError, status_string)
 
-__all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+__all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
 
@@ -165,6 +165,53 @@ def moe_forward_host(x_host, y_host, Wg, W1, W3, W2, K: int = 2, x_dev=None, y_d
         moe_forward(x_dev, Wg, W1, W3, W2, K, y=y_dev, workspace=workspace, stream=s)
         y_host.copy_(y_dev, non_blocking=True)
     return y_host
+
+
+class HostPipeline:
+    """moe_forward on batches held in pinned host memory, with the copy of the
+    next batch in and of the previous result out overlapping the current
+    batch's layer: two device (x, y) buffer pairs, a copy-in stream, a compute
+    stream and a copy-out stream ordered by events.  ``submit`` only enqueues;
+    ``synchronize`` waits for every submitted batch (read ``y_host`` after it).
+    All batches have the shape and dtype given here."""
+
+    def __init__(self, Wg, W1, W3, W2, K: int, T: int, device=None, workspace: Workspace | None = None):
+        self.dev = W1.device if device is None else device
+        E, d, f = W1.shape
+        self.w = (Wg, W1, W3, W2)
+        self.K = K
+        self.ws = workspace or Workspace(T, d, f, E, K, W1.dtype, self.dev)
+        self.x = [torch.empty((T, d), dtype=W1.dtype, device=self.dev) for _ in range(2)]
+        self.y = [torch.empty((T, d), dtype=W1.dtype, device=self.dev) for _ in range(2)]
+        self.s_in = torch.cuda.Stream(self.dev)
+        self.s_run = torch.cuda.Stream(self.dev)
+        self.s_out = torch.cuda.Stream(self.dev)
+        self.in_done = [torch.cuda.Event() for _ in range(2)]
+        self.run_done = [torch.cuda.Event() for _ in range(2)]
+        self.out_done = [torch.cuda.Event() for _ in range(2)]
+        self.n = 0
+
+    def submit(self, x_host, y_host):
+        b = self.n & 1
+        if self.n >= 2:
+            self.s_in.wait_event(self.run_done[b])    # x[b] was read by the layer two batches ago
+        with torch.cuda.stream(self.s_in):
+            self.x[b].copy_(x_host, non_blocking=True)
+            self.in_done[b].record(self.s_in)
+        self.s_run.wait_event(self.in_done[b])
+        if self.n >= 2:
+            self.s_run.wait_event(self.out_done[b])   # y[b] was copied out two batches ago
+        moe_forward(self.x[b], *self.w, self.K, y=self.y[b], workspace=self.ws, stream=self.s_run)
+        self.run_done[b].record(self.s_run)
+        self.s_out.wait_event(self.run_done[b])
+        with torch.cuda.stream(self.s_out):
+            y_host.copy_(self.y[b], non_blocking=True)
+            self.out_done[b].record(self.s_out)
+        self.n += 1
+
+    def synchronize(self):
+        for s in (self.s_in, self.s_run, self.s_out):
+            s.synchronize()
 
 
 def moe_route(x, Wg, K: int = 2, workspace: Workspace | None = None, stream=None):

@@ -222,3 +222,19 @@ def test_forced_timeout_is_reported_and_context_survives(moe, T):
     assert moe.moe_read_status(ws) == 0
     ref = oracle.moe_layer(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, 2)
     assert parity.rel_linf(_np(y.float()), ref.y) <= parity.TOL["bf16"]
+
+
+def test_host_pipeline_matches_device_calls(moe):
+    """Batches in pinned host memory through HostPipeline (copies overlapping
+    the layer) give the same bits as moe_forward on device tensors."""
+    dev = torch.device("cuda:0")
+    inp = _bf16_inputs(200, 256, 512, 8, 2, seed=21).to(dev)
+    xs = [W.rms_rows(200, 256, 900 + i, "cpu", torch.bfloat16).pin_memory() for i in range(5)]
+    ys = [torch.empty_like(xs[0]).pin_memory() for _ in range(5)]
+    pipe = moe.HostPipeline(inp.Wg, inp.W1, inp.W3, inp.W2, 2, 200, dev)
+    for x, y in zip(xs, ys):
+        pipe.submit(x, y)
+    pipe.synchronize()
+    for x, y in zip(xs, ys):
+        want = moe.moe_forward(x.to(dev), inp.Wg, inp.W1, inp.W3, inp.W2, 2)
+        assert torch.equal(y, want.cpu())
