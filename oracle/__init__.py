@@ -8,3 +8,6 @@ from .moe_oracle import (f64, router_logits, topk_indices, topk_mask, softmax, g
                          expert, moe_layer, moe_layer_dense, moe_layer_tokens, permutation,
                          rmsnorm, moe_block, logit_gaps, Gating, LayerResult, Permutation,
                          RMS_EPS)
+from . import fp8_oracle  # noqa: F401
+from .fp8_oracle import (e4m3_decode, e4m3_encode, quantize_weight_columns, dequantize_weight_columns,  # noqa: F401
+                         quantize_rows, dequantize_rows, moe_layer_fp8, E4M3_MAX)
