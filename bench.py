@@ -54,6 +54,9 @@ CONFIGS = {
     # per-expert GEMM shape of the prefill layer at a quarter of its memory
     "prefill_e2": dict(T=1024, d=4096, f=14336, E=2, K=2),
 }
+# the same workloads with e4m3 expert weights (quantised once, untimed)
+for _n in ("prefill", "decode1", "decode8", "decode32", "decode128", "skew"):
+    CONFIGS[_n + "_fp8"] = dict(CONFIGS[_n], fp8=True)
 WORKLOAD_TEXT = {
     "prefill": "Mixtral-shaped MoE layer prefill: T=4096 tokens, d=4096, f=14336, E=8 experts, top-2, bf16, "
                "fp32 accumulate",
@@ -65,6 +68,9 @@ WORKLOAD_TEXT["prefill_e2"] = "profiling stand-in: T=1024 tokens, d=4096, f=1433
 for _t in (1, 8, 32, 128):
     WORKLOAD_TEXT[f"decode{_t}"] = f"Mixtral-shaped MoE layer decode batch: T={_t} tokens, d=4096, f=14336, " \
                                    f"E=8, top-2, bf16 (weight-streaming)"
+for _n in ("prefill", "decode1", "decode8", "decode32", "decode128", "skew"):
+    WORKLOAD_TEXT[_n + "_fp8"] = WORKLOAD_TEXT[_n].replace("bf16", "e4m3 expert weights (per-column scales), " \
+                                                           "bf16 tokens")
 
 
 # ---------------------------------------------------------------------------
@@ -309,6 +315,7 @@ def max_over_ranks(v: float, world: int, dev) -> float:
 
 def make_inputs(cfg_name: str, rank: int, dev, weights=None):
     c = CONFIGS[cfg_name]
+    cfg_name = cfg_name.replace("_fp8", "")
     seed = W.BASE_SEED + 1009 * rank     # replicas: own tokens per rank (same model weights)
     if weights is None:
         weights = W.mixtral_weights(c["d"], c["f"], c["E"], seed=W.BASE_SEED, device=dev)
@@ -323,12 +330,15 @@ def make_inputs(cfg_name: str, rank: int, dev, weights=None):
 
 def algorithmic(c, n_touched):
     """Per layer: FLOPs of the whole layer and of the gate/up GEMM; bytes of the
-    whole layer and of the gate/up GEMM (touched experts' weights once)."""
+    whole layer and of the gate/up GEMM (touched experts' weights once, one
+    byte per weight with e4m3 weights, plus their scales)."""
     T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
+    wb = 1 if c.get("fp8") else 2
+    scales = (3 * f * 4 + d * 4) if c.get("fp8") else 0            # fp32 column scales per expert
     flops = T * K * 6 * d * f + 2 * T * d * E
     gate_up_flops = T * K * 4 * d * f
-    bytes_step = n_touched * 3 * d * f * 2 + 2 * d * E + 2 * T * d * 2
-    gate_up_bytes = n_touched * 2 * d * f * 2
+    bytes_step = n_touched * (3 * d * f * wb + scales) + 2 * d * E + 2 * T * d * 2
+    gate_up_bytes = n_touched * (2 * d * f * wb + 2 * f * 4)
     return flops, gate_up_flops, bytes_step, gate_up_bytes
 
 
@@ -603,10 +613,29 @@ def run_ours(args, world, rank, local):
     c = CONFIGS[args.config]
     T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
     inp, weights = make_inputs(args.config, rank, dev)
-    ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
+    fp8 = bool(c.get("fp8"))
     y = torch.empty_like(inp.x)
     stream = torch.cuda.current_stream(dev)
     steps, warmup = args.steps, max(args.warmup, 3)
+    if fp8:
+        # e4m3 expert weights: quantised once before timing (weight preparation)
+        q8 = [t for W_ in (inp.W1, inp.W3, inp.W2) for t in moe.quantize_weights_fp8(W_)]
+        ws = moe.Workspace(T, d, f, E, K, torch.float8_e4m3fn, dev)
+
+        def fwd(out):
+            moe.moe_forward_fp8(inp.x, inp.Wg, *q8, K, y=out, workspace=ws, stream=stream)
+
+        def fwd_timed(evs, out):
+            moe.moe_forward_fp8_timed(inp.x, inp.Wg, *q8, K, evs, y=out, workspace=ws, stream=stream)
+    else:
+        q8 = None
+        ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
+
+        def fwd(out):
+            moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, y=out, workspace=ws, stream=stream)
+
+        def fwd_timed(evs, out):
+            moe.moe_forward_timed(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, evs, y=out, workspace=ws, stream=stream)
 
     # touched experts of this routing (algorithmic bytes at decode sizes)
     _, _, _, offs, _ = moe.moe_route(inp.x, inp.Wg, K)
@@ -617,7 +646,7 @@ def run_ours(args, world, rank, local):
         return [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
 
     for _ in range(warmup):
-        moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, y=y, workspace=ws, stream=stream)
+        fwd(y)
     torch.cuda.synchronize(dev)
     if moe.moe_read_status(ws) != 0:
         raise RuntimeError(f"device status {moe.moe_read_status(ws)}")
@@ -630,7 +659,7 @@ def run_ours(args, world, rank, local):
     with ClockSampler(local) as clk:
         start.record(stream)
         for i in range(steps):
-            moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, y=y, workspace=ws, stream=stream)
+            fwd(y)
         end.record(stream)
         torch.cuda.synchronize(dev)
     barrier(world)
@@ -645,7 +674,7 @@ def run_ours(args, world, rank, local):
     evs = new_events(steps)
     torch.cuda.synchronize(dev)
     for i in range(steps):
-        moe.moe_forward_timed(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, evs[i], y=y, workspace=ws, stream=stream)
+        fwd_timed(evs[i], y)
     torch.cuda.synchronize(dev)
     stage_ms = {}
     for j, name in enumerate(("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")):
@@ -657,7 +686,7 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(3, min(steps, 50))
     x_hosts = [inp.x.cpu().pin_memory() for _ in range(2)]
     y_hosts = [torch.empty_like(x_hosts[0]).pin_memory() for _ in range(2)]
-    pipe = moe.HostPipeline(inp.Wg, inp.W1, inp.W3, inp.W2, K, T, dev, workspace=ws)
+    pipe = moe.HostPipeline(inp.Wg, inp.W1, inp.W3, inp.W2, K, T, dev, workspace=ws, fp8_weights=q8)
     for i in range(3):
         pipe.submit(x_hosts[i & 1], y_hosts[i & 1])
     pipe.synchronize()
@@ -674,6 +703,11 @@ def run_ours(args, world, rank, local):
     tokens_per_s = world * T / (ms / 1e3)
     gu_ms = stage_ms["gate_up_gemm"]
     hbm_bound = args.config.startswith("decode")
+    # e4m3 contractions take the bf16 measured peaks times the nominal fp8/bf16 ratio (4.5 / 2.25)
+    tensor_ratio = 2.0 if fp8 else 1.0
+    tensor_peak = peaks["bf16_tflops_sustained"] * tensor_ratio
+    tensor_peak_burst = peaks["bf16_tflops"] * tensor_ratio
+    peak_note = " x 2 (nominal e4m3/bf16 dense ratio)" if fp8 else ""
     kernel_file = ROOT / "sparse_mixture_experts_55_b300" / "csrc" / "gemm_tc.cu"
     if hbm_bound:
         achieved = gu_bytes / (gu_ms / 1e3) / 1e9
@@ -684,33 +718,34 @@ def run_ours(args, world, rank, local):
     else:
         achieved = gu_flops / (gu_ms / 1e3) / 1e12
         roof = {"kernel": "gate_up_gemm", "bound": "tensor", "achieved": achieved,
-                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": achieved / peaks["bf16_tflops_sustained"],
-                "frac_of_burst": achieved / peaks["bf16_tflops"],
+                "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved / tensor_peak,
+                "frac_of_burst": achieved / tensor_peak_burst,
                 "traffic": traffic_from_profiles(kernel_file, f"{args.config}_traffic_bytes_per_launch"),
                 "algorithmic_flops_per_launch": gu_flops,
-                "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peak_src}; kernel timed inside a "
-                               f"long run of steps)"}
+                "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained{peak_note} ({peak_src}; kernel timed "
+                               f"inside a long run of steps)"}
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
         "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
-        "dtype": "bf16", "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens",
+        "dtype": "e4m3 experts, bf16 tokens" if fp8 else "bf16",
+        "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens",
         "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step" % (
-                       n_touched * 3 * d * f * 2 / 1e9), "touched_experts": n_touched},
+                       n_touched * 3 * d * f * (1 if fp8 else 2) / 1e9), "touched_experts": n_touched},
         "tflops": flops / (ms / 1e3) / 1e12 * world,
-        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
         "hbm_gbs_algorithmic": bytes_step / (ms / 1e3) / 1e9,
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
         "roofline": roof,
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
-        "gpu_launches": 6 * steps,
+        "gpu_launches": (7 if fp8 else 6) * steps,
         "stage_timing": "separate pass of the same K forwards with library-recorded stage events",
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         n_tok = min(T, args.cpu_tokens)
         rate, dt, threads = cpu_oracle_rate(inp, n_tok)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",

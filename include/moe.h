@@ -72,8 +72,10 @@ enum {
   MOE_ERR_DEVICE_BOUNDS = 7    /* device-side index check failed (MOE_DEBUG_CHECKS only) */
 };
 
-/* Element types. */
-enum { MOE_BF16 = 0, MOE_F32 = 1 };
+/* Element types.  MOE_FP8_E4M3 names the e4m3-weight variant (bf16 tokens,
+ * router and output; e4m3 expert weights and expert-GEMM activations): it is
+ * the dtype of moe_workspace_bytes for moe_forward_fp8. */
+enum { MOE_BF16 = 0, MOE_F32 = 1, MOE_FP8_E4M3 = 2 };
 
 /* moe_forward flags. */
 #define MOE_ACCUMULATE   0x1u  /* y += MoE(x) instead of y = MoE(x) (residual stream) */
@@ -161,6 +163,52 @@ MOE_API int moe_forward_timed(const void *x, const void *Wg, const void *W1, con
 MOE_API int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2,
                       int T, int d, int f, int E, int K, int dtype, float eps,
                       void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * e4m3 expert weights.  The pages name FP8 only as deployment work
+ * (paper-graph-ui summary, "Inference and Deployment Infrastructure"), so the
+ * scheme is this library's:
+ *   e4m3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
+ *         largest finite magnitude 448; values round to nearest, ties to the
+ *         even code, and saturate at +-448.
+ *   weights: one fp32 scale per output column n of each expert bank,
+ *         s[e, n] = max_k |W[e, k, n]| / 448 (1 for an all-zero column);
+ *         codes q[e, n, k] = e4m3(W[e, k, n] / s[e, n]) (fp32 division),
+ *         stored K-contiguous, i.e. transposed from the bf16 bank.
+ *   activations: the same with one scale per row, for each grouped token row
+ *         (gate/up input) and for each row of the SwiGLU output H after it is
+ *         rounded to bf16 (down input).
+ * The expert GEMMs multiply e4m3 codes on the tensor cores (fp32
+ * accumulation) and apply the row and column scales in their epilogues.
+ *
+ * moe_quantize_weights_fp8: W [E, K, N] bf16 -> Wq [E, N, K] e4m3 codes (one
+ * byte each) and scales [E, N] fp32, all device memory owned by the caller;
+ * K, N >= 1.  For the layer: W1 and W3 ([E, d, f]) give [E, f, d] codes and
+ * [E, f] scales, W2 ([E, f, d]) gives [E, d, f] codes and [E, d] scales.
+ */
+MOE_API int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales,
+                             moe_stream_t stream);
+
+/*
+ * The layer with e4m3 expert weights: y = sum over the K selected experts of
+ * gate * SwiGLU_expert(x), as moe_forward, with the expert projections on
+ * e4m3 operands (scheme above).  x [T, d], Wg [d, E] and y [T, d] are bf16;
+ * W1q, W3q [E, f, d] and W2q [E, d, f] are e4m3 codes with scales s1, s3
+ * [E, f] and s2 [E, d] from moe_quantize_weights_fp8.  d and f are multiples
+ * of 16.  workspace: at least moe_workspace_bytes(T, d, f, E, K,
+ * MOE_FP8_E4M3).  flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS |
+ * MOE_DEBUG_FORCE_TIMEOUT.  Other rules as moe_forward.
+ */
+MOE_API int moe_forward_fp8(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
+                    const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
+                    int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+
+/* moe_forward_fp8 with the stage events of moe_forward_timed (stage 4, the
+ * gate/up GEMM, includes the quantisation of H). */
+MOE_API int moe_forward_fp8_timed(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
+                          const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f,
+                          int E, int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                          void *const *events);
 
 /*
  * Routing only, for inspection: the router and grouping kernels that

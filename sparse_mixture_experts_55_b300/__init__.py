@@ -19,13 +19,16 @@ import torch
 
 from . import _lib
 from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_TIMEOUT, MOE_F32,  # noqa: F401
-                   MoEError, status_string)
+                   MOE_FP8_E4M3, MoEError, status_string)
 
-__all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+__all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "quantize_weights_fp8",
+           "moe_forward_fp8", "moe_forward_fp8_timed", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
 
 _DTYPES = {torch.bfloat16: MOE_BF16, torch.float32: MOE_F32}
+# workspace sizing of the e4m3-weight variant (tokens stay bf16)
+_WS_DTYPES = {**_DTYPES, torch.float8_e4m3fn: MOE_FP8_E4M3}
 
 
 def library_path() -> str:
@@ -59,7 +62,7 @@ def _need(t: torch.Tensor, name: str, dtype=None, device=None):
 
 
 def moe_workspace_bytes(T: int, d: int, f: int, E: int, K: int, dtype=torch.bfloat16) -> int:
-    code = _DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
+    code = _WS_DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype)
     n = _lib.load().moe_workspace_bytes(T, d, f, E, K, code)
     if n == 0:
         raise ValueError(f"unsupported sizes T={T} d={d} f={f} E={E} K={K} dtype={dtype}")
@@ -167,6 +170,73 @@ def moe_forward_host(x_host, y_host, Wg, W1, W3, W2, K: int = 2, x_dev=None, y_d
     return y_host
 
 
+def quantize_weights_fp8(W, stream=None):
+    """e4m3 codes of an expert bank: W [E, K, N] bf16 -> (Wq [E, N, K]
+    float8_e4m3fn, K contiguous; scales [E, N] fp32), one scale per output
+    column (scale = max |column| / 448)."""
+    _need(W, "W", torch.bfloat16)
+    E, Kd, N = W.shape
+    Wq = torch.empty((E, N, Kd), dtype=torch.float8_e4m3fn, device=W.device)
+    scales = torch.empty((E, N), dtype=torch.float32, device=W.device)
+    rc = _lib.load().moe_quantize_weights_fp8(_ptr(W), E, Kd, N, _ptr(Wq), _ptr(scales), _stream_ptr(stream, W.device))
+    _lib.check("moe_quantize_weights_fp8", rc)
+    return Wq, scales
+
+
+def _fp8_args(x, Wg, W1q, s1, W3q, s3, W2q, s2, y):
+    dev = x.device
+    _need(x, "x", torch.bfloat16, dev)
+    _need(Wg, "Wg", torch.bfloat16, dev)
+    for t, n in ((W1q, "W1q"), (W3q, "W3q"), (W2q, "W2q")):
+        _need(t, n, torch.float8_e4m3fn, dev)
+    for t, n in ((s1, "s1"), (s3, "s3"), (s2, "s2")):
+        _need(t, n, torch.float32, dev)
+    T, d = x.shape
+    E, f, d1 = W1q.shape
+    if (Wg.shape != (d, E) or d1 != d or W3q.shape != (E, f, d) or W2q.shape != (E, d, f) or s1.shape != (E, f)
+            or s3.shape != (E, f) or s2.shape != (E, d)):
+        raise ValueError("shape mismatch: x [T,d], Wg [d,E], W1q/W3q [E,f,d], W2q [E,d,f], s1/s3 [E,f], s2 [E,d]")
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", torch.bfloat16, dev)
+    return T, d, f, E, y
+
+
+def moe_forward_fp8(x, Wg, W1q, s1, W3q, s3, W2q, s2, K: int = 2, y=None, workspace: Workspace | None = None,
+                    flags: int = 0, stream=None):
+    """The layer with e4m3 expert weights (codes and scales from
+    quantize_weights_fp8); x, Wg, y bf16.  Returns y [T, d]."""
+    T, d, f, E, y = _fp8_args(x, Wg, W1q, s1, W3q, s3, W2q, s2, y)
+    if workspace is None:
+        workspace = Workspace(T, d, f, E, K, torch.float8_e4m3fn, x.device)
+    rc = _lib.load().moe_forward_fp8(_ptr(x), _ptr(Wg), _ptr(W1q), _ptr(s1), _ptr(W3q), _ptr(s3), _ptr(W2q), _ptr(s2),
+                                     _ptr(y), T, d, f, E, K, workspace.ptr(), workspace.nbytes, flags,
+                                     _stream_ptr(stream, x.device))
+    _lib.check("moe_forward_fp8", rc)
+    return y
+
+
+def moe_forward_fp8_timed(x, Wg, W1q, s1, W3q, s3, W2q, s2, K: int, events, y=None,
+                          workspace: Workspace | None = None, flags: int = 0, stream=None):
+    """moe_forward_fp8 recording the seven stage events (see moe_forward_timed)."""
+    T, d, f, E, y = _fp8_args(x, Wg, W1q, s1, W3q, s3, W2q, s2, y)
+    s = stream if stream is not None else torch.cuda.current_stream(x.device)
+    handles = []
+    for ev in events:
+        if ev.cuda_event == 0:
+            ev.record(s)
+        handles.append(ev.cuda_event)
+    arr = (ctypes.c_void_p * len(handles))(*handles)
+    if workspace is None:
+        workspace = Workspace(T, d, f, E, K, torch.float8_e4m3fn, x.device)
+    rc = _lib.load().moe_forward_fp8_timed(_ptr(x), _ptr(Wg), _ptr(W1q), _ptr(s1), _ptr(W3q), _ptr(s3), _ptr(W2q),
+                                           _ptr(s2), _ptr(y), T, d, f, E, K, workspace.ptr(), workspace.nbytes,
+                                           flags, ctypes.c_void_p(s.cuda_stream), arr)
+    _lib.check("moe_forward_fp8_timed", rc)
+    return y
+
+
 class HostPipeline:
     """moe_forward on batches held in pinned host memory, with the copy of the
     next batch in and of the previous result out overlapping the current
@@ -175,12 +245,14 @@ class HostPipeline:
     ``synchronize`` waits for every submitted batch (read ``y_host`` after it).
     All batches have the shape and dtype given here."""
 
-    def __init__(self, Wg, W1, W3, W2, K: int, T: int, device=None, workspace: Workspace | None = None):
+    def __init__(self, Wg, W1, W3, W2, K: int, T: int, device=None, workspace: Workspace | None = None,
+                 fp8_weights=None):
         self.dev = W1.device if device is None else device
         E, d, f = W1.shape
         self.w = (Wg, W1, W3, W2)
+        self.q8 = fp8_weights        # (W1q, s1, W3q, s3, W2q, s2): run moe_forward_fp8 instead
         self.K = K
-        self.ws = workspace or Workspace(T, d, f, E, K, W1.dtype, self.dev)
+        self.ws = workspace or Workspace(T, d, f, E, K, torch.float8_e4m3fn if fp8_weights else W1.dtype, self.dev)
         self.x = [torch.empty((T, d), dtype=W1.dtype, device=self.dev) for _ in range(2)]
         self.y = [torch.empty((T, d), dtype=W1.dtype, device=self.dev) for _ in range(2)]
         self.s_in = torch.cuda.Stream(self.dev)
@@ -201,7 +273,10 @@ class HostPipeline:
         self.s_run.wait_event(self.in_done[b])
         if self.n >= 2:
             self.s_run.wait_event(self.out_done[b])   # y[b] was copied out two batches ago
-        moe_forward(self.x[b], *self.w, self.K, y=self.y[b], workspace=self.ws, stream=self.s_run)
+        if self.q8 is not None:
+            moe_forward_fp8(self.x[b], self.w[0], *self.q8, self.K, y=self.y[b], workspace=self.ws, stream=self.s_run)
+        else:
+            moe_forward(self.x[b], *self.w, self.K, y=self.y[b], workspace=self.ws, stream=self.s_run)
         self.run_done[b].record(self.s_run)
         self.s_out.wait_event(self.run_done[b])
         with torch.cuda.stream(self.s_out):

@@ -23,6 +23,7 @@ MOE_ERR_DEVICE_BOUNDS = 7
 
 MOE_BF16 = 0
 MOE_F32 = 1
+MOE_FP8_E4M3 = 2
 
 MOE_ACCUMULATE = 0x1
 MOE_NUM_STAGE_EVENTS = 7
@@ -38,6 +39,10 @@ SIGNATURES = {
     "moe_forward_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp, _vp]),
     "moe_block_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _sz, _u,
                                 _vp]),
+    "moe_quantize_weights_fp8": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
+    "moe_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
+    "moe_forward_fp8_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp,
+                                   _vp]),
     "moe_route": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_rmsnorm": (_i, [_vp, _vp, _i, _i, ctypes.c_float, _i, _vp]),

@@ -1,0 +1,214 @@
+// fp8.cu -- the e4m3 pieces of the FP8-weight variant of the layer: weight
+// quantisation (one fp32 scale per output column, codes stored K-contiguous),
+// the row gather that quantises each grouped activation row with its own
+// scale, and the per-row quantisation of the SwiGLU output H.
+//
+// Scheme (the pages name FP8 only as deployment work -- paper-graph-ui
+// summary, "Inference and Deployment Infrastructure" -- so it is this
+// library's): scale = max |v| / 448 over the column (weights) or row
+// (activations), 1 where that maximum is 0; code = e4m3(v / scale) rounded to
+// nearest, ties to even, saturating at 448; the division is an fp32 IEEE
+// division.
+#include <cuda_bf16.h>
+#include <cuda_fp8.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+constexpr float kE4M3Max = 448.0f;
+
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+__device__ __forceinline__ float scale_of(float absmax) { return absmax > 0.f ? absmax / kE4M3Max : 1.0f; }
+
+__device__ __forceinline__ uint8_t to_e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// scales[e, n] = max_k |W[e, k, n]| / 448 (1 for an all-zero column).
+// Block: 64 columns x 4 row phases.
+__global__ void __launch_bounds__(256) weight_absmax_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N,
+                                                            float *__restrict__ scales) {
+  __shared__ float red[4][64];
+  const int e = blockIdx.y;
+  const int j = threadIdx.x & 63, ph = threadIdx.x >> 6;
+  const int n = blockIdx.x * 64 + j;
+  float m = 0.f;
+  if (n < N) {
+    const __nv_bfloat16 *col = W + static_cast<size_t>(e) * K * N + n;
+    for (int k = ph; k < K; k += 4) m = fmaxf(m, fabsf(__bfloat162float(col[static_cast<size_t>(k) * N])));
+  }
+  red[ph][j] = m;
+  __syncthreads();
+  if (ph == 0 && n < N) {
+    const float a = fmaxf(fmaxf(red[0][j], red[1][j]), fmaxf(red[2][j], red[3][j]));
+    scales[static_cast<size_t>(e) * N + n] = scale_of(a);
+  }
+}
+
+// Wq[e, n, k] = e4m3(W[e, k, n] / scales[e, n]); 64x64 tiles through shared
+// memory so that both the reads (along n) and the writes (along k) coalesce.
+__global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N,
+                                                           const float *__restrict__ scales, uint8_t *__restrict__ Wq) {
+  __shared__ uint8_t tile[64][65];
+  const int e = blockIdx.z;
+  const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
+  const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  const __nv_bfloat16 *Wb = W + static_cast<size_t>(e) * K * N;
+  const int n = n0 + tx;
+  const float s = n < N ? scales[static_cast<size_t>(e) * N + n] : 1.0f;
+  for (int i = ty; i < 64; i += 4) {
+    const int k = k0 + i;
+    uint8_t q = 0;
+    if (k < K && n < N) q = to_e4m3(__bfloat162float(Wb[static_cast<size_t>(k) * N + n]) / s);
+    tile[tx][i] = q;  // [n][k]
+  }
+  __syncthreads();
+  uint8_t *Wqb = Wq + static_cast<size_t>(e) * N * K;
+  for (int i = ty; i < 64; i += 4) {
+    const int nn = n0 + i, k = k0 + tx;
+    if (nn < N && k < K) Wqb[static_cast<size_t>(nn) * K + k] = tile[i][tx];
+  }
+}
+
+// X_perm8[r, :] = e4m3(x[perm_tok[r], :] / xs[r]) with xs[r] the row's scale;
+// pad rows are zero with scale 0.  One warp per grouped row.
+__global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *__restrict__ x, int T, int d,
+                                                           const int32_t *__restrict__ perm_tok,
+                                                           const int32_t *__restrict__ poffsets, int E,
+                                                           uint8_t *__restrict__ xq, float *__restrict__ xs,
+                                                           int *status) {
+  pdl_wait();
+  pdl_trigger();
+  const int rows = poffsets[E];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int nchunk = d / 8;  // 8 bf16 in, 8 codes out
+  for (int r = gw; r < rows; r += nw) {
+    int tok = perm_tok[r];
+    if (tok >= T) {
+      atomicCAS(status, 0, MOE_ERR_DEVICE_BOUNDS);
+      tok = -1;
+    }
+    uint8_t *dst = xq + static_cast<size_t>(r) * d;
+    if (tok < 0) {
+      for (int c = lane; c < nchunk; c += 32) *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(0, 0);
+      if (lane == 0) xs[r] = 0.f;
+      continue;
+    }
+    const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * d);
+    float m = 0.f;
+    for (int c = lane; c < nchunk; c += 32) {
+      const uint4 u = __ldg(src + c);
+      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float s = scale_of(m);
+    for (int c = lane; c < nchunk; c += 32) {
+      const uint4 u = __ldg(src + c);
+      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+      uint32_t w[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = __bfloat1622float2(h[i]);
+        const uint32_t q = static_cast<uint32_t>(to_e4m3(f.x / s)) | (static_cast<uint32_t>(to_e4m3(f.y / s)) << 8);
+        w[i >> 1] |= q << (16 * (i & 1));
+      }
+      *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(w[0], w[1]);
+    }
+    if (lane == 0) xs[r] = s;
+  }
+}
+
+// Hq[r, :] = e4m3(H[r, :] / hs[r]) for every real grouped row, with hs[r] =
+// max over the row's n-tiles of the tile maxima habs[r, :] written by the
+// gate/up epilogue (the maxima of the bf16 H values), / 448.  One warp per
+// row; padding rows are left alone (the down projection drops their output).
+__global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__restrict__ H, int f,
+                                                      const float *__restrict__ habs, int n_tiles,
+                                                      const int32_t *__restrict__ offsets,
+                                                      const int32_t *__restrict__ poffsets, int E,
+                                                      uint8_t *__restrict__ hq, float *__restrict__ hs) {
+  pdl_wait();
+  pdl_trigger();
+  const int rows = poffsets[E];
+  const int lane = threadIdx.x & 31;
+  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+  const int nw = (gridDim.x * blockDim.x) >> 5;
+  const int nchunk = f / 8;
+  for (int r = gw; r < rows; r += nw) {
+    int e = 0;
+    while (e < E - 1 && r >= poffsets[e + 1]) ++e;
+    if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row
+    float m = 0.f;
+    for (int t = lane; t < n_tiles; t += 32) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float s = scale_of(m);
+    const uint4 *src = reinterpret_cast<const uint4 *>(H + static_cast<size_t>(r) * f);
+    uint8_t *dst = hq + static_cast<size_t>(r) * f;
+    for (int c = lane; c < nchunk; c += 32) {
+      const uint4 u = src[c];
+      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+      uint32_t w[2] = {0, 0};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 v = __bfloat1622float2(h[i]);
+        const uint32_t q = static_cast<uint32_t>(to_e4m3(v.x / s)) | (static_cast<uint32_t>(to_e4m3(v.y / s)) << 8);
+        w[i >> 1] |= q << (16 * (i & 1));
+      }
+      *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(w[0], w[1]);
+    }
+    if (lane == 0) hs[r] = s;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales,
+                                        cudaStream_t s) {
+  const dim3 g1((N + 63) / 64, E);
+  weight_absmax_kernel<<<g1, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(W), K, N, scales);
+  cudaError_t err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const dim3 g2((N + 63) / 64, (K + 63) / 64, E);
+  weight_quant_kernel<<<g2, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(W), K, N, scales,
+                                         static_cast<uint8_t *>(Wq));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const Ptrs &P, int num_sms,
+                                cudaStream_t s) {
+  int blocks = (R + 7) / 8;
+  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(gather_quant_kernel, dim3(blocks), dim3(256), 0, s, true,
+                       static_cast<const __nv_bfloat16 *>(x), T, d, static_cast<const int32_t *>(P.perm_tok),
+                       static_cast<const int32_t *>(P.poffsets), E, static_cast<uint8_t *>(P.xperm), P.xscale,
+                       P.status);
+}
+
+cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
+  int blocks = (R + 7) / 8;
+  if (blocks > num_sms * 8) blocks = num_sms * 8;
+  if (blocks < 1) blocks = 1;
+  return launch_kernel(quant_h_kernel, dim3(blocks), dim3(256), 0, s, true,
+                       static_cast<const __nv_bfloat16 *>(P.hbuf), f, static_cast<const float *>(P.habs), n_tiles,
+                       static_cast<const int32_t *>(P.offsets), static_cast<const int32_t *>(P.poffsets), E,
+                       static_cast<uint8_t *>(P.hq), P.hscale);
+}
+
+}  // namespace moe

@@ -107,6 +107,13 @@ struct GemmArgs {
   int splits;
   int kb_per_split;
   int force_timeout;        // failure-path test: wait on a barrier nothing signals first
+  // e4m3 operands only: per-row scale of A (indexed by padded row), per-column
+  // scales of B ([E, n_out]; col_scale1 is the W3 bank's for gate/up), and
+  // the per-(row, n-tile) maxima of the bf16 H values the gate/up writes
+  const float *row_scale;
+  const float *col_scale0;
+  const float *col_scale1;
+  float *habs;
   int *status;
 };
 
@@ -205,13 +212,16 @@ __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Ctrl &
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_half,
                        const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
                        const GemmArgs args) {
   using RG = Ring<PAIR>;
   constexpr int STAGES = RG::STAGES;
+  // a k-block is one 128-byte row of A and of B in shared memory: 64 bf16 or
+  // 128 e4m3 elements of the contraction
+  constexpr int KB_ELEMS = FP8 ? 128 : BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;
@@ -317,8 +327,42 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (!wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, true)) { ok = false; break; }
           uint8_t *a_dst = sA + p_stage * A_BYTES;
           uint8_t *b_dst = sB + p_stage * RG::B_BYTES;
-          const int k0 = kb * BK;
-          if (PAIR) {
+          const int k0 = kb * KB_ELEMS;
+          if (FP8) {
+            // e4m3 weights are stored K-contiguous ([E, N, K]): a B box is 128
+            // columns (rows of the bank) x 128 k, 16 KiB, one 128-byte row per column
+            if (PAIR) {
+              if (leader) ptx::mbar_arrive_expect_tx(&c.full[p_stage], RG::STAGE_TX);
+              const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[p_stage]), 0);
+              ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, row0, pol_a);
+              if (MODE == MODE_GATE_UP)
+                ptx::tma_load_3d_pair(b_dst, rank == 0 ? &tmB0 : &tmB1, bar, k0, t.nt * (BN / 2), t.e, pol_b);
+              else
+                ptx::tma_load_3d_pair(b_dst, &tmB0, bar, k0, t.nt * BN + rank * (BN / 2), t.e, pol_b);
+            } else {
+              uint64_t *bar = &c.full[p_stage];
+              ptx::mbar_arrive_expect_tx(bar, RG::STAGE_TX);
+              constexpr int HALF_B = 2 * B_CHUNK;  // 128 columns
+              if (!t.npair) {
+                ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);
+                if (MODE == MODE_GATE_UP)
+                  ptx::tma_load_3d_mc(b_dst + rank * HALF_B, rank == 0 ? &tmB0 : &tmB1, bar, k0, t.nt * (BN / 2), t.e,
+                                      kBothCtas, pol_b);
+                else
+                  ptx::tma_load_3d_mc(b_dst + rank * HALF_B, &tmB0, bar, k0, t.nt * BN + rank * (BN / 2), t.e,
+                                      kBothCtas, pol_b);
+              } else {
+                ptx::tma_load_2d_mc(a_dst + rank * A_HALF, &tmA_half, bar, k0, row0 + 64 * rank, kBothCtas, pol_a);
+                if (MODE == MODE_GATE_UP) {
+                  ptx::tma_load_3d(b_dst, &tmB0, bar, k0, t.nt * (BN / 2), t.e, pol_b);
+                  ptx::tma_load_3d(b_dst + HALF_B, &tmB1, bar, k0, t.nt * (BN / 2), t.e, pol_b);
+                } else {
+                  ptx::tma_load_3d(b_dst, &tmB0, bar, k0, t.nt * BN, t.e, pol_b);
+                  ptx::tma_load_3d(b_dst + HALF_B, &tmB0, bar, k0, t.nt * BN + BN / 2, t.e, pol_b);
+                }
+              }
+            }
+          } else if (PAIR) {
             // both CTAs' copies complete on the first CTA's barrier, which
             // expects the bytes of both
             if (leader) ptx::mbar_arrive_expect_tx(&c.full[p_stage], RG::STAGE_TX);
@@ -380,8 +424,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0 && leader) {
       // pair MMA: M = 256 over both CTAs' rows
-      constexpr uint32_t idesc = ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false,
-                                                     /*B MN-major*/ true);
+      constexpr uint32_t idesc = FP8 ? ptx::idesc_e4m3_f32(PAIR ? 2 * BM : BM, BN)
+                                     : ptx::idesc_bf16_f32(PAIR ? 2 * BM : BM, BN, /*A MN-major*/ false,
+                                                           /*B MN-major*/ true);
       int stage = 0;
       uint32_t phase = 0;
       int local = 0;
@@ -403,14 +448,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           const uint32_t a_addr = ptx::smem_u32(sA + stage * A_BYTES);
           const uint32_t b_addr = ptx::smem_u32(sB + stage * RG::B_BYTES);
 #pragma unroll
-          for (int ks = 0; ks < BK / 16; ++ks) {
-            // A: K-major, 128 B rows, 8-row groups 1024 B apart; K step = 32 B.
+          for (int ks = 0; ks < 4; ++ks) {
+            // A: K-major, 128 B rows, 8-row groups 1024 B apart; K step = 32 B
+            // (16 bf16 or 32 e4m3 elements per MMA).
             const uint64_t ad = ptx::smem_desc_sw128(a_addr + ks * 32, 16, 1024);
-            // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups 1024 B apart (SBO); K step = 16 rows.
-            const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 2048, B_CHUNK, 1024);
             const uint32_t accum = (kb > kb0 || ks > 0) ? 1u : 0u;
-            if (PAIR) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
-            else ptx::mma_bf16(d_tmem, ad, bd, idesc, accum);
+            if (FP8) {
+              // B: K-major like A (one 128-byte row per column).
+              const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 32, 16, 1024);
+              if (PAIR) ptx::mma_f8_pair(d_tmem, ad, bd, idesc, accum);
+              else ptx::mma_f8(d_tmem, ad, bd, idesc, accum);
+            } else {
+              // B: N-major, 64-column chunks 8 KiB apart (LBO), 8-row K groups
+              // 1024 B apart (SBO); K step = 16 rows.
+              const uint64_t bd = ptx::smem_desc_sw128(b_addr + ks * 2048, B_CHUNK, 1024);
+              if (PAIR) ptx::mma_bf16_pair(d_tmem, ad, bd, idesc, accum);
+              else ptx::mma_bf16(d_tmem, ad, bd, idesc, accum);
+            }
           }
           // frees the stage in both CTAs once these MMAs have read it
           if (PAIR) ptx::mma_commit_pair_mc(&c.empty[stage], kBothCtas);
@@ -454,18 +508,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (S == 1) {
           __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out);
           if (n0 < args.n_out) {
+            // e4m3 operands: accumulators carry codes; scale by the A row's and
+            // the B column's scales, and keep the row's max |bf16 H| over the tile
+            const float rs = FP8 && in_seg ? args.row_scale[row] : 0.f;  // phantom rows lie past the buffers
+            const float *cs1 = FP8 ? args.col_scale0 + static_cast<size_t>(t.e) * args.n_out : nullptr;
+            const float *cs3 = FP8 ? args.col_scale1 + static_cast<size_t>(t.e) * args.n_out : nullptr;
+            float hmax = 0.f;
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
               uint32_t g[32], v[32];
               ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
               ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, v);
               ptx::tmem_wait_ld();
+              if (FP8) {
+                const int cb = n0 + cc * 32;
+#pragma unroll
+                for (int j = 0; j < 32; ++j) {
+                  const bool in = cb + j < args.n_out;
+                  g[j] = __float_as_uint(__uint_as_float(g[j]) * rs * (in ? __ldg(cs1 + cb + j) : 0.f));
+                  v[j] = __float_as_uint(__uint_as_float(v[j]) * rs * (in ? __ldg(cs3 + cb + j) : 0.f));
+                }
+              }
               uint32_t packed[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
                 const float h0 = silu_f(__uint_as_float(g[2 * j])) * __uint_as_float(v[2 * j]);
                 const float h1 = silu_f(__uint_as_float(g[2 * j + 1])) * __uint_as_float(v[2 * j + 1]);
                 __nv_bfloat162 hb = __floats2bfloat162_rn(h0, h1);
+                if (FP8) {
+                  const float2 hr = __bfloat1622float2(hb);
+                  hmax = fmaxf(hmax, fmaxf(fabsf(hr.x), fabsf(hr.y)));
+                }
                 packed[j] = *reinterpret_cast<uint32_t *>(&hb);
               }
               const int col = n0 + cc * 32;
@@ -478,6 +551,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         make_uint4(packed[4 * vv], packed[4 * vv + 1], packed[4 * vv + 2], packed[4 * vv + 3]);
               }
             }
+            if (FP8 && in_seg) args.habs[static_cast<size_t>(row) * NT + t.nt] = hmax;
           }
           ptx::tc_fence_before();
           __syncwarp();
@@ -583,7 +657,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       } else {
         // gate-scaled rows into the compact output; padding rows are dropped
         float *O = static_cast<float *>(args.out) + static_cast<size_t>(t.s) * args.out_split_stride;
-        const float gsc = real ? args.perm_gate[row] : 0.f;
+        // e4m3 operands: the gate times the H row's scale; the W2 column scale below
+        const float gsc = real ? args.perm_gate[row] * (FP8 ? args.row_scale[row] : 1.f) : 0.f;
         const int n0 = t.nt * BN;
         if (n0 < args.n_out) {
 #pragma unroll 1
@@ -592,6 +667,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
             ptx::tmem_wait_ld();
             const int col = n0 + cc * 32;
+            if (FP8) {
+              const float *cs2 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
+#pragma unroll
+              for (int j = 0; j < 32; ++j)
+                v[j] = __float_as_uint(__uint_as_float(v[j]) * (col + j < args.n_out ? __ldg(cs2 + col + j) : 0.f));
+            }
             if (real) {
               float *dst = O + static_cast<size_t>(ru) * args.n_out + col;
 #pragma unroll
@@ -700,6 +781,34 @@ bool tmap_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 2-D e4m3 matrix [rows, cols] (cols contiguous), box = 128 columns (128
+// bytes) x box_rows rows, 128-byte swizzle.
+bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D e4m3 bank [E, rows, cols] (cols = the contraction, contiguous), box =
+// 128 x 128 x 1, 128-byte swizzle.
+bool tmap_3d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, E};
+  cuuint64_t strides[2] = {cols, cols * rows};
+  cuuint32_t box[3] = {128, 128, 1};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // Per device: shared-memory attribute set, and how many 2-CTA clusters of
 // this kernel can be resident at once (the persistent grid size).
 struct DevState {
@@ -707,9 +816,9 @@ struct DevState {
   int clusters = 0;
 };
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool FP8>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(expert_gemm_kernel<MODE, PAIR>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(expert_gemm_kernel<MODE, PAIR, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               Ring<PAIR>::SMEM);
 }
 
@@ -726,7 +835,7 @@ cudaError_t max_clusters(int num_sms, int *n) {
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, expert_gemm_kernel<MODE_GATE_UP, PAIR>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, expert_gemm_kernel<MODE_GATE_UP, PAIR, false>, &cfg);
 }
 
 cudaError_t device_state(int num_sms, int *clusters) {
@@ -738,10 +847,14 @@ cudaError_t device_state(int num_sms, int *clusters) {
   static DevState st[64];
   std::lock_guard<std::mutex> lock(mu);
   if (!st[dev].ready) {
-    err = set_smem_attr<MODE_GATE_UP, false>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, false>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, true>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, true>();
+    err = set_smem_attr<MODE_GATE_UP, false, false>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, false, false>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, true, false>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, true, false>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, false, true>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, false, true>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, true, true>();
+    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, true, true>();
     if (err != cudaSuccess) return err;
     int n0 = 0, n1 = 0;
     err = max_clusters<false>(num_sms, &n0);
@@ -756,7 +869,7 @@ cudaError_t device_state(int num_sms, int *clusters) {
   return cudaSuccess;
 }
 
-template <int MODE, bool PAIR>
+template <int MODE, bool PAIR, bool FP8>
 cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMap &a, const CUtensorMap &ah,
                         const CUtensorMap &b0, const CUtensorMap &b1, const GemmArgs &args) {
   cudaLaunchConfig_t cfg = {};
@@ -773,7 +886,7 @@ cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMa
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE, PAIR>, a, ah, b0, b1, args);
+  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE, PAIR, FP8>, a, ah, b0, b1, args);
 }
 
 }  // namespace
@@ -808,8 +921,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.kb_per_split = L.kb_per_split_gu;
   g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
   g1.status = P.status;
-  err = L.pair ? launch_gemm<MODE_GATE_UP, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
-               : launch_gemm<MODE_GATE_UP, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
+  err = L.pair ? launch_gemm<MODE_GATE_UP, true, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
+               : launch_gemm<MODE_GATE_UP, false, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
@@ -824,8 +937,68 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
-  return L.pair ? launch_gemm<MODE_DOWN, true>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2)
-                : launch_gemm<MODE_DOWN, false>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2);
+  return L.pair ? launch_gemm<MODE_DOWN, true, false>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2)
+                : launch_gemm<MODE_DOWN, false, false>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2,
+                                                       g2);
+}
+
+cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
+                                    const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
+                                    const Ptrs &P, unsigned flags, int num_sms, cudaStream_t s,
+                                    void *const *mid_event) {
+  int clusters = 0;
+  cudaError_t err = device_state(num_sms, &clusters);
+  if (err != cudaSuccess) return err;
+  // e4m3 operands: X_perm [R, d], H [R, f] and the banks [E, N, K], all K-contiguous
+  CUtensorMap tm_x, tm_xh, tm_w1, tm_w3, tm_h, tm_hh, tm_w2;
+  if (!tmap_2d_u8(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d_u8(&tm_xh, P.xperm, d, L.R, BM / 2) ||
+      !tmap_3d_u8(&tm_w1, W1q, d, f, E) || !tmap_3d_u8(&tm_w3, W3q, d, f, E) ||
+      !tmap_2d_u8(&tm_h, P.hq, f, L.R, BM) || !tmap_2d_u8(&tm_hh, P.hq, f, L.R, BM / 2) ||
+      !tmap_3d_u8(&tm_w2, W2q, f, d, E))
+    return cudaErrorInvalidValue;
+
+  GemmArgs g1{};
+  g1.poffsets = P.poffsets;
+  g1.offsets = P.offsets;
+  g1.perm_gate = P.perm_gate;
+  g1.out = P.hbuf;
+  g1.E = E;
+  g1.rows_bound = L.R;
+  g1.tk = L.TK;
+  g1.n_out = f;
+  g1.num_n_tiles = (f + BN / 2 - 1) / (BN / 2);
+  g1.num_kb = (d + 127) / 128;
+  g1.splits = 1;
+  g1.kb_per_split = g1.num_kb;
+  g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
+  g1.row_scale = P.xscale;
+  g1.col_scale0 = s1;
+  g1.col_scale1 = s3;
+  g1.habs = P.habs;
+  g1.status = P.status;
+  err = L.pair ? launch_gemm<MODE_GATE_UP, true, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
+               : launch_gemm<MODE_GATE_UP, false, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
+  // H rows to e4m3 with their own scales, inside the gate/up stage
+  if (err == cudaSuccess) err = launch_quant_h(f, E, L.R, g1.num_n_tiles, P, num_sms, s);
+  if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
+  if (err != cudaSuccess) return err;
+
+  GemmArgs g2 = g1;
+  g2.out = P.obuf;
+  g2.out_split_stride = static_cast<long long>(L.TK) * d;
+  g2.n_out = d;
+  g2.num_n_tiles = (d + BN - 1) / BN;
+  g2.num_kb = (f + 127) / 128;
+  g2.splits = L.S;
+  g2.kb_per_split = L.kb_per_split;
+  g2.force_timeout = 0;
+  g2.row_scale = P.hscale;
+  g2.col_scale0 = s2;
+  g2.col_scale1 = nullptr;
+  g2.habs = nullptr;
+  return L.pair ? launch_gemm<MODE_DOWN, true, true>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2)
+                : launch_gemm<MODE_DOWN, false, true>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2,
+                                                      g2);
 }
 
 }  // namespace moe

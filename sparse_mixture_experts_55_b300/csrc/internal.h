@@ -48,6 +48,7 @@ struct WsLayout {
   // byte offsets into the workspace
   size_t status, tile_cnt, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf, obuf,
       gu_part, xnorm;
+  size_t xscale, habs, hq, hscale;  // e4m3 variant only (0 bytes otherwise)
   size_t total;
   size_t zero_bytes;  // bytes from `status` that every call clears (status word + split counters)
   int TK;             // T*K: rows of the compact grouped buffers
@@ -86,6 +87,12 @@ struct Ptrs {
   float *obuf;    // [S, T*K, d] gate-scaled expert outputs, unpadded grouped rows
   float *gu_part; // [S_gu, T*K, 2f] fp32 partial sums of the split gate/up projection
   void *xnorm;  // [T, d] normalised block input (moe_block_forward)
+  // e4m3 variant: X_perm holds codes [R, d]; H stays bf16 [R, f] and is
+  // re-quantised into hq [R, f] with one scale per row
+  float *xscale;  // [R] scale of each grouped activation row
+  float *habs;    // [R, gate/up n-tiles] max |bf16 H| per row and tile
+  void *hq;       // [R, f] e4m3 codes of H
+  float *hscale;  // [R] scale of each H row
 };
 Ptrs carve(void *ws, const WsLayout &L);
 
@@ -106,6 +113,17 @@ cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, in
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
                                      cudaStream_t s, void *const *mid_event);
+
+// -------- fp8.cu (e4m3 expert weights)
+cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, cudaStream_t s);
+cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const Ptrs &P, int num_sms,
+                                cudaStream_t s);
+cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s);
+// gemm_tc.cu, e4m3 operands: gate/up GEMM, H quantisation, down GEMM
+cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
+                                    const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
+                                    const Ptrs &P, unsigned flags, int num_sms, cudaStream_t s,
+                                    void *const *mid_event);
 
 // -------- gemm_simt.cu (exact fp32 path)
 cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,

@@ -51,15 +51,17 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
-int elem_bytes(int dtype) { return dtype == MOE_BF16 ? 2 : 4; }
+// bytes per element of the tokens x, y (the e4m3 variant keeps them bf16)
+int elem_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 
 // Shape checks shared by every entry point.  Returns MOE_OK or an error code.
 int check_shape(int T, int d, int f, int E, int K, int dtype) {
-  if (dtype != MOE_BF16 && dtype != MOE_F32) return MOE_ERR_UNSUPPORTED;
+  if (dtype != MOE_BF16 && dtype != MOE_F32 && dtype != MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
   if (T < 0 || d < 1 || f < 1 || E < 1 || K < 1) return MOE_ERR_INVALID_ARG;
   if (K > E) return MOE_ERR_INVALID_ARG;
   if (K > kMaxK || E > kMaxE) return MOE_ERR_UNSUPPORTED;
-  const int mult = dtype == MOE_BF16 ? 8 : 4;  // 16-byte rows for vector loads and TMA strides
+  // 16-byte rows for vector loads and TMA strides (one-byte codes for e4m3)
+  const int mult = dtype == MOE_BF16 ? 8 : dtype == MOE_F32 ? 4 : 16;
   if (d % mult != 0 || f % mult != 0) return MOE_ERR_INVALID_ARG;
   // index arithmetic of the grouped buffers stays in 32-bit rows
   const long long rows = static_cast<long long>(T) * K + static_cast<long long>(E) * kSegPad;
@@ -124,18 +126,22 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   const long long TKl = static_cast<long long>(T) * K;
   L.TK = static_cast<int>(TKl);
   const long long touched = TKl < E ? TKl : E;
-  SplitPlan down{1, (f + 63) / 64}, gu{1, (d + 63) / 64};
-  if (dtype == MOE_BF16 && touched > 0) {
+  const bool fp8 = dtype == MOE_FP8_E4M3;
+  const int kbw = fp8 ? 128 : 64;  // contraction elements per 128-byte k-block
+  SplitPlan down{1, (f + kbw - 1) / kbw}, gu{1, (d + kbw - 1) / kbw};
+  if (dtype != MOE_F32 && touched > 0) {
     const int clusters = num_sms / 2;
+    const double wb = fp8 ? 1.0 : 2.0;  // weight bytes per element
     // partial-sum bytes (written once, read once, fp32) per split over the
     // weight bytes each projection streams
-    down = plan_splits(TKl, E, (d + 255) / 256, (f + 63) / 64, clusters,
-                       4.0 * static_cast<double>(TKl) / (static_cast<double>(touched) * f));
+    down = plan_splits(TKl, E, (d + 255) / 256, (f + kbw - 1) / kbw, clusters,
+                       8.0 / wb * static_cast<double>(TKl) / (static_cast<double>(touched) * f));
     // The split gate/up tile is completed inside the GEMM by the last split's
     // epilogue warp, whose latency grows with the real rows it owns; beyond
     // about four rows per expert it stalls the MMA pipeline more than the
     // balanced split saves, so larger batches keep one split.
-    if (TKl <= 4 * touched)
+    // (the e4m3 gate/up epilogue scales and re-quantises whole rows: one split)
+    if (TKl <= 4 * touched && !fp8)
       gu = plan_splits(TKl, E, (f + 127) / 128, (d + 63) / 64, clusters,
                        4.0 * static_cast<double>(TKl) / (static_cast<double>(touched) * d));
   }
@@ -146,7 +152,7 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   // CTA-pair MMAs once experts average two or more 128-row tiles: the pair
   // halves each CTA's weight-tile traffic and shared-memory footprint; with
   // fewer rows the phantom half-tile of an odd tile count would dominate.
-  L.pair = dtype == MOE_BF16 && touched > 0 && TKl >= 2LL * kSegPad * touched && L.S_gu == 1;
+  L.pair = dtype != MOE_F32 && touched > 0 && TKl >= 2LL * kSegPad * touched && L.S_gu == 1;
   const size_t TK = static_cast<size_t>(T) * K;
   const size_t R = static_cast<size_t>(L.R);
   size_t o = 0;
@@ -168,11 +174,16 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   L.pos = take(TK * 4);
   L.perm_tok = take(R * 4);
   L.perm_gate = take(R * 4);
-  L.xperm = take(R * d * eb);
+  L.xperm = take(R * d * (fp8 ? 1 : eb));
   L.hbuf = take(R * f * eb);
   L.obuf = take(static_cast<size_t>(L.S) * TK * d * 4);
   L.gu_part = take(L.S_gu > 1 ? static_cast<size_t>(L.S_gu) * TK * 2 * f * 4 : 0);
   L.xnorm = take(static_cast<size_t>(T) * d * eb);
+  const size_t nt_gu = (f + 127) / 128;
+  L.xscale = take(fp8 ? R * 4 : 0);
+  L.habs = take(fp8 ? R * nt_gu * 4 : 0);
+  L.hq = take(fp8 ? R * f : 0);
+  L.hscale = take(fp8 ? R * 4 : 0);
   L.total = o;
   return L;
 }
@@ -195,6 +206,10 @@ Ptrs carve(void *ws, const WsLayout &L) {
   P.obuf = reinterpret_cast<float *>(b + L.obuf);
   P.gu_part = reinterpret_cast<float *>(b + L.gu_part);
   P.xnorm = b + L.xnorm;
+  P.xscale = reinterpret_cast<float *>(b + L.xscale);
+  P.habs = reinterpret_cast<float *>(b + L.habs);
+  P.hq = b + L.hq;
+  P.hscale = reinterpret_cast<float *>(b + L.hscale);
   return P;
 }
 
@@ -212,6 +227,7 @@ size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
 static int forward_impl(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
                         int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
                         unsigned flags, moe_stream_t stream, void *const *events) {
+  if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;  // e4m3 weights go through moe_forward_fp8
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
   if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
@@ -265,6 +281,7 @@ int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, c
 int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d, int f,
                       int E, int K, int dtype, float eps, void *workspace, size_t ws_bytes, unsigned flags,
                       moe_stream_t stream) {
+  if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
   if (flags & ~(MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
@@ -292,6 +309,78 @@ int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void 
   for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, events);
+}
+
+int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, moe_stream_t stream) {
+  if (E < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
+  if (!W || !Wq || !scales) return MOE_ERR_INVALID_ARG;
+  if (overlaps(W, static_cast<size_t>(E) * K * N * 2, Wq, static_cast<size_t>(E) * K * N)) return MOE_ERR_INVALID_ARG;
+  const int st = check_device();
+  if (st != MOE_OK) return st;
+  return launch_quantize_weights_fp8(W, E, K, N, Wq, scales, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+             ? MOE_OK
+             : MOE_ERR_CUDA;
+}
+
+static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
+                            const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
+                            int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                            void *const *events) {
+  constexpr int dtype = MOE_FP8_E4M3;
+  int st = check_shape(T, d, f, E, K, dtype);
+  if (st != MOE_OK) return st;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  if (!x || !Wg || !W1q || !W3q || !W2q || !s1 || !s3 || !s2 || !y) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1q) || !aligned16(W3q) || !aligned16(W2q) || !aligned16(y) ||
+      !aligned16(s1) || !aligned16(s3) || !aligned16(s2))
+    return MOE_ERR_INVALID_ARG;
+  const size_t act_bytes = static_cast<size_t>(T) * d * 2;
+  if (overlaps(x, act_bytes, y, act_bytes)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  const int sms = sm_count_or_default();
+  const WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Ptrs P = carve(workspace, L);
+  if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+  auto mark = [&](int i) -> cudaError_t {
+    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
+  };
+  // routing on the bf16 tokens, as moe_forward; the gather quantises rows
+  cudaError_t err = mark(0);
+  if (err == cudaSuccess) err = launch_route(x, Wg, T, d, E, K, MOE_BF16, flags, L, P, s);
+  if (err == cudaSuccess) err = mark(1);
+  if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
+  if (err == cudaSuccess) err = mark(2);
+  if (err == cudaSuccess) err = launch_gather_quant(x, T, d, E, L.R, P, sms, s);
+  if (err == cudaSuccess) err = mark(3);
+  if (err == cudaSuccess)
+    err = launch_expert_gemms_fp8(W1q, s1, W3q, s3, W2q, s2, d, f, E, L, P, flags, sms, s, events ? events + 4 : nullptr);
+  if (err == cudaSuccess) err = mark(5);
+  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, MOE_BF16, flags, P, sms, s);
+  if (err == cudaSuccess) err = mark(6);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_forward_fp8(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q, const float *s3,
+                    const void *W2q, const float *s2, void *y, int T, int d, int f, int E, int K, void *workspace,
+                    size_t ws_bytes, unsigned flags, moe_stream_t stream) {
+  return forward_fp8_impl(x, Wg, W1q, s1, W3q, s3, W2q, s2, y, T, d, f, E, K, workspace, ws_bytes, flags, stream,
+                          nullptr);
+}
+
+int moe_forward_fp8_timed(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
+                          const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
+                          int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                          void *const *events) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return forward_fp8_impl(x, Wg, W1q, s1, W3q, s3, W2q, s2, y, T, d, f, E, K, workspace, ws_bytes, flags, stream,
+                          events);
 }
 
 int moe_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, int32_t *idx, float *gate,

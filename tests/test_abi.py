@@ -29,6 +29,7 @@ def lib():
 def test_header_declares_the_boundary():
     names = _header_functions()
     assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_block_forward", "moe_route",
+                            "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_timed",
                             "moe_route_noalloc", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
@@ -145,3 +146,31 @@ def test_block_forward_rejects_bad_arguments(lib):
     assert blk(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
     assert blk(h=0x200000 + 256) == _lib.MOE_ERR_INVALID_ARG            # h inside the workspace
     assert blk(h=0, T=0) == _lib.MOE_OK                                  # empty input: no-op
+
+
+def test_fp8_entry_points_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+
+    def fwd8(d=64, f=128, x=0x1000, w=0x3000, s=0x9000, ws=0x200000, ws_bytes=1 << 40, flags=0, K=2):
+        return lib.moe_forward_fp8(vp(x), vp(0x2000), vp(w), vp(s), vp(0x4000), vp(s), vp(0x5000), vp(s),
+                                   vp(0x100000), 16, d, f, 8, K, vp(ws), ws_bytes, flags, vp(0))
+
+    assert fwd8(d=72) == _lib.MOE_ERR_INVALID_ARG          # e4m3 rows need multiples of 16
+    assert fwd8(f=136) == _lib.MOE_ERR_INVALID_ARG
+    assert fwd8(K=3) == _lib.MOE_ERR_UNSUPPORTED
+    assert fwd8(w=0) == _lib.MOE_ERR_INVALID_ARG
+    assert fwd8(s=0) == _lib.MOE_ERR_INVALID_ARG
+    assert fwd8(w=0x3008) == _lib.MOE_ERR_INVALID_ARG      # misaligned
+    assert fwd8(flags=0x80) == _lib.MOE_ERR_INVALID_ARG
+    assert fwd8(ws=0) == _lib.MOE_ERR_WORKSPACE
+    assert fwd8(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
+    # the bf16 entry point does not take the e4m3 dtype
+    assert _fwd(lib, dtype=_lib.MOE_FP8_E4M3) == _lib.MOE_ERR_UNSUPPORTED
+    assert lib.moe_workspace_bytes(16, 64, 128, 8, 2, _lib.MOE_FP8_E4M3) > 0
+    assert lib.moe_workspace_bytes(16, 72, 128, 8, 2, _lib.MOE_FP8_E4M3) == 0
+    assert lib.moe_quantize_weights_fp8(vp(0), 8, 64, 64, vp(0x1000), vp(0x2000), vp(0)) == _lib.MOE_ERR_INVALID_ARG
+    assert lib.moe_quantize_weights_fp8(vp(0x1000), 0, 64, 64, vp(0x900000), vp(0x2000), vp(0)) == \
+        _lib.MOE_ERR_INVALID_ARG
+    # codes overlapping the bank
+    assert lib.moe_quantize_weights_fp8(vp(0x1000), 1, 64, 64, vp(0x1000 + 64), vp(0x90000), vp(0)) == \
+        _lib.MOE_ERR_INVALID_ARG

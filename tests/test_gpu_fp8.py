@@ -1,0 +1,112 @@
+"""GPU parity of the e4m3-weight variant against the float64 oracle
+(oracle/fp8_oracle.py): weight quantisation bit for bit; the layer within the
+bf16 bar on ragged shapes, both GEMM forms, decode sizes with split down
+projections, top-1, and at full Mixtral size for a one-token decode.  All
+calls go through the C ABI."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import oracle.fp8_oracle as F8
+import workloads as W
+from tests import parity
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_device):
+    from sparse_mixture_experts_55_b300 import build
+    build.build()
+    import sparse_mixture_experts_55_b300 as m
+    return m
+
+
+def _np(t):
+    return t.detach().cpu().numpy()
+
+
+@pytest.mark.parametrize("E,K,N", [(3, 64, 96), (2, 200, 72), (1, 4096, 128)])
+def test_weight_quantisation_bit_exact(moe, E, K, N):
+    Wb = W.randn((E, K, N), 0.02, 77 + K, "cpu", torch.bfloat16)
+    Wb[0, :, 5] = 0                                   # an all-zero column: scale 1
+    Wq, s = moe.quantize_weights_fp8(Wb.cuda())
+    q_ref, s_ref = F8.quantize_weight_columns(Wb)
+    assert np.array_equal(_np(s), s_ref)
+    assert np.array_equal(_np(Wq.view(torch.uint8)), q_ref)
+
+
+def _fp8_case(T, d, f, E, K, seed):
+    Wg, W1, W3, W2 = W.mixtral_weights(d, f, E, seed=seed, device="cpu")
+    x = W.rms_rows(T, d, seed * 7 + 1, "cpu", torch.bfloat16)
+    return x, Wg, W1, W3, W2
+
+
+def _check_fp8_layer(moe, T, d, f, E, K, seed, tol=2e-2):
+    x, Wg, W1, W3, W2 = _fp8_case(T, d, f, E, K, seed)
+    dev = torch.device("cuda:0")
+    q1, s1 = moe.quantize_weights_fp8(W1.to(dev))
+    q3, s3 = moe.quantize_weights_fp8(W3.to(dev))
+    q2, s2 = moe.quantize_weights_fp8(W2.to(dev))
+    ws = moe.Workspace(T, d, f, E, K, torch.float8_e4m3fn, dev)
+    y = moe.moe_forward_fp8(x.to(dev), Wg.to(dev), q1, s1, q3, s3, q2, s2, K, workspace=ws)
+    assert moe.moe_read_status(ws) == 0
+    # the oracle quantises the bf16 banks itself
+    r1, t1 = F8.quantize_weight_columns(W1)
+    r3, t3 = F8.quantize_weight_columns(W3)
+    r2, t2 = F8.quantize_weight_columns(W2)
+    ref = F8.moe_layer_fp8(x, Wg, r1, t1, r3, t3, r2, t2, K)
+    g = oracle.gating(x, Wg, K)
+    idx, gate, perm, offs, pos = moe.moe_route(x.to(dev), Wg.to(dev), K)
+    rep = parity.check_routing(_np(idx), _np(gate), g, K)
+    assert rep.n_mismatch == 0, rep
+    err = parity.rel_linf(_np(y.float()), ref.y)
+    bf = oracle.moe_layer(x, Wg, W1, W3, W2, K).y
+    qerr = parity.rel_linf(_np(y.float()), bf)
+    print(f"\nfp8 T={T} d={d} f={f} E={E} K={K}: rel err vs fp8 oracle {err:.2e}, vs bf16-weight oracle {qerr:.2e}")
+    assert err <= tol, err
+    # deterministic
+    y2 = moe.moe_forward_fp8(x.to(dev), Wg.to(dev), q1, s1, q3, s3, q2, s2, K, workspace=ws)
+    assert torch.equal(y, y2)
+    return err
+
+
+@pytest.mark.parametrize("T,d,f,E,K", [
+    (300, 512, 1024, 8, 2),     # multicast-pair tiles
+    (1100, 512, 1024, 4, 2),    # CTA-pair tiles, odd tile counts (phantom halves)
+    (257, 528, 1040, 8, 2),     # ragged K (k-block tails) and N (odd n-tile count)
+    (600, 256, 512, 4, 1),      # top-1
+    (1, 512, 1024, 8, 2),       # decode: split down projection
+    (8, 1024, 1536, 8, 2),
+    (129, 256, 384, 32, 2),     # many experts, empty segments
+])
+def test_fp8_layer_parity(moe, T, d, f, E, K):
+    _check_fp8_layer(moe, T, d, f, E, K, seed=300 + T)
+
+
+def test_fp8_full_size_decode_one_token(moe, cuda_device):
+    """Mixtral-sized weights, one token: the oracle quantises and evaluates
+    only the two experts the token selects."""
+    Wg, W1, W3, W2 = W.mixtral_weights(device=cuda_device)
+    inp = W.decode(1, device=cuda_device, weights=(Wg, W1, W3, W2))
+    q1, s1 = moe.quantize_weights_fp8(W1)
+    q3, s3 = moe.quantize_weights_fp8(W3)
+    q2, s2 = moe.quantize_weights_fp8(W2)
+    y = moe.moe_forward_fp8(inp.x, Wg, q1, s1, q3, s3, q2, s2, 2)
+    g = oracle.gating(inp.x.cpu(), Wg.cpu(), 2)
+    sel = sorted(set(g.idx[0].tolist()))
+    # sub-banks of the selected experts, router columns restricted to them
+    sub = lambda B: B[sel].cpu()
+    r1, t1 = F8.quantize_weight_columns(sub(W1))
+    r3, t3 = F8.quantize_weight_columns(sub(W3))
+    r2, t2 = F8.quantize_weight_columns(sub(W2))
+    # the codes the GPU made for those experts are the oracle's, bit for bit
+    assert np.array_equal(_np(q1[sel].view(torch.uint8)), r1)
+    Wg_sub = Wg.cpu()[:, sel]
+    ref = F8.moe_layer_fp8(inp.x.cpu(), Wg_sub, r1, t1, r3, t3, r2, t2, 2)
+    err = parity.rel_linf(_np(y.float()), ref.y)
+    print(f"\nfp8 full-size T=1: experts {sel}, rel err {err:.2e}")
+    assert err <= 2e-2
