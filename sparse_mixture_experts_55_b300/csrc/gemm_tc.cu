@@ -502,12 +502,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const bool in_seg = seg_row < c.mtiles[t.e] * BM;
       const bool real = seg_row < c.uoff[t.e + 1] - c.uoff[t.e];
       const int ru = c.uoff[t.e] + seg_row;  // unpadded grouped row (valid if real)
+      // A warp whose 32 rows are all padding has nothing anyone reads (the down
+      // projection drops padding rows), so it skips its quarter entirely.
+      const bool warp_real = __ballot_sync(0xffffffffu, real) != 0;
       const uint32_t tbase = tmem + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       if (MODE == MODE_GATE_UP) {
         const int n0 = t.nt * (BN / 2);
         if (S == 1) {
           __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out);
-          if (n0 < args.n_out) {
+          if (n0 < args.n_out && warp_real) {
             // e4m3 operands: accumulators carry codes; scale by the A row's and
             // the B column's scales, and keep the row's max |bf16 H| over the tile
             const float rs = FP8 && in_seg ? args.row_scale[row] : 0.f;  // phantom rows lie past the buffers
@@ -523,10 +526,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (FP8) {
                 const int cb = n0 + cc * 32;
 #pragma unroll
-                for (int j = 0; j < 32; ++j) {
-                  const bool in = cb + j < args.n_out;
-                  g[j] = __float_as_uint(__uint_as_float(g[j]) * rs * (in ? __ldg(cs1 + cb + j) : 0.f));
-                  v[j] = __float_as_uint(__uint_as_float(v[j]) * rs * (in ? __ldg(cs3 + cb + j) : 0.f));
+                for (int j4 = 0; j4 < 8; ++j4) {
+                  // n_out is a multiple of 16, so a group of four is all in or all out
+                  const int c0 = cb + 4 * j4;
+                  const bool in = c0 < args.n_out;
+                  const float4 a4 = in ? __ldg(reinterpret_cast<const float4 *>(cs1 + c0)) : make_float4(0, 0, 0, 0);
+                  const float4 b4 = in ? __ldg(reinterpret_cast<const float4 *>(cs3 + c0)) : make_float4(0, 0, 0, 0);
+                  const float sa[4] = {a4.x, a4.y, a4.z, a4.w}, sb[4] = {b4.x, b4.y, b4.z, b4.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    g[4 * j4 + i] = __float_as_uint(__uint_as_float(g[4 * j4 + i]) * rs * sa[i]);
+                    v[4 * j4 + i] = __float_as_uint(__uint_as_float(v[4 * j4 + i]) * rs * sb[i]);
+                  }
                 }
               }
               uint32_t packed[16];
@@ -563,7 +574,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           // order and apply SwiGLU -- deterministic whatever the arrival order.
           const size_t pstride = 2 * static_cast<size_t>(args.n_out);
           float *P = args.part + static_cast<size_t>(t.s) * args.tk * pstride;
-          if (n0 < args.n_out) {
+          if (n0 < args.n_out && warp_real) {
 #pragma unroll 1
             for (int cc = 0; cc < 4; ++cc) {
               uint32_t g[32], v[32];
@@ -590,7 +601,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ptx::tc_fence_before();
           __syncwarp();
           if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
-          if (n0 < args.n_out) {
+          if (n0 < args.n_out && warp_real) {
             // One arrival counter per (m-tile, n-tile, lane quarter): each
             // epilogue warp completes its own 32 rows, with no cross-warp wait.
             int *cnt = args.tile_cnt + (static_cast<size_t>(row / BM) * NT + t.nt) * 4 + q;
@@ -606,12 +617,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               // The warp completes its real rows four at a time, lane l taking
               // columns [4l, 4l + 4) of the tile's 128, so the partial loads
               // are coalesced and those of four rows are in flight together.
-              // Each sum runs over the splits in order.
+              // Each sum runs over the splits in order.  e4m3 operands: the
+              // sums are scaled by the A row's and the B columns' scales, and
+              // the row's max |bf16 H| over the tile goes to habs.
               const int col = n0 + 4 * lane;
               const size_t sstride = static_cast<size_t>(args.tk) * pstride;
+              float4 c1 = make_float4(1.f, 1.f, 1.f, 1.f), c3 = c1;
+              if (FP8) {
+                const float *b1 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
+                const float *b3 = args.col_scale1 + static_cast<size_t>(t.e) * args.n_out;
+                if (col < args.n_out) {
+                  c1 = make_float4(b1[col], b1[col + 1], b1[col + 2], b1[col + 3]);
+                  c3 = make_float4(b3[col], b3[col + 1], b3[col + 2], b3[col + 3]);
+                }
+              }
               unsigned m = __ballot_sync(0xffffffffu, real);
               while (m) {
                 int src[4];
+                float hm[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                   src[j] = m ? __ffs(m) - 1 : -1;
@@ -640,6 +663,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                   for (int j = 0; j < 4; ++j) {
                     if (src[j] < 0) continue;
+                    if (FP8) {
+                      const float rsj = args.row_scale[row - lane + src[j]];
+                      a[j].x *= rsj * c1.x; a[j].y *= rsj * c1.y; a[j].z *= rsj * c1.z; a[j].w *= rsj * c1.w;
+                      b[j].x *= rsj * c3.x; b[j].y *= rsj * c3.y; b[j].z *= rsj * c3.z; b[j].w *= rsj * c3.w;
+                    }
                     __nv_bfloat162 h01 = __floats2bfloat162_rn(silu_f(a[j].x) * b[j].x, silu_f(a[j].y) * b[j].y);
                     __nv_bfloat162 h23 = __floats2bfloat162_rn(silu_f(a[j].z) * b[j].z, silu_f(a[j].w) * b[j].w);
                     uint2 packed;
@@ -648,6 +676,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __nv_bfloat16 *H = static_cast<__nv_bfloat16 *>(args.out) +
                                        static_cast<size_t>(row - lane + src[j]) * args.n_out + col;
                     *reinterpret_cast<uint2 *>(H) = packed;
+                    if (FP8) {
+                      const float2 p = __bfloat1622float2(h01), q2 = __bfloat1622float2(h23);
+                      hm[j] = fmaxf(fmaxf(fabsf(p.x), fabsf(p.y)), fmaxf(fabsf(q2.x), fabsf(q2.y)));
+                    }
+                  }
+                }
+                if (FP8) {
+#pragma unroll
+                  for (int j = 0; j < 4; ++j) {
+                    float m = hm[j];
+#pragma unroll
+                    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+                    if (lane == 0 && src[j] >= 0)
+                      args.habs[static_cast<size_t>(row - lane + src[j]) * NT + t.nt] = m;
                   }
                 }
               }
@@ -660,7 +702,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // e4m3 operands: the gate times the H row's scale; the W2 column scale below
         const float gsc = real ? args.perm_gate[row] * (FP8 ? args.row_scale[row] : 1.f) : 0.f;
         const int n0 = t.nt * BN;
-        if (n0 < args.n_out) {
+        if (n0 < args.n_out && warp_real) {
 #pragma unroll 1
           for (int cc = 0; cc < BN / 32; ++cc) {
             uint32_t v[32];
@@ -670,8 +712,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (FP8) {
               const float *cs2 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
 #pragma unroll
-              for (int j = 0; j < 32; ++j)
-                v[j] = __float_as_uint(__uint_as_float(v[j]) * (col + j < args.n_out ? __ldg(cs2 + col + j) : 0.f));
+              for (int j4 = 0; j4 < 8; ++j4) {
+                const int c0 = col + 4 * j4;
+                const float4 s4 =
+                    c0 < args.n_out ? __ldg(reinterpret_cast<const float4 *>(cs2 + c0)) : make_float4(0, 0, 0, 0);
+                v[4 * j4] = __float_as_uint(__uint_as_float(v[4 * j4]) * s4.x);
+                v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) * s4.y);
+                v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) * s4.z);
+                v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) * s4.w);
+              }
             }
             if (real) {
               float *dst = O + static_cast<size_t>(ru) * args.n_out + col;
@@ -968,8 +1017,10 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g1.n_out = f;
   g1.num_n_tiles = (f + BN / 2 - 1) / (BN / 2);
   g1.num_kb = (d + 127) / 128;
-  g1.splits = 1;
-  g1.kb_per_split = g1.num_kb;
+  g1.splits = L.S_gu;
+  g1.kb_per_split = L.kb_per_split_gu;
+  g1.part = P.gu_part;
+  g1.tile_cnt = P.tile_cnt;
   g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
   g1.row_scale = P.xscale;
   g1.col_scale0 = s1;
@@ -986,6 +1037,8 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   GemmArgs g2 = g1;
   g2.out = P.obuf;
   g2.out_split_stride = static_cast<long long>(L.TK) * d;
+  g2.part = nullptr;
+  g2.tile_cnt = nullptr;
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + 127) / 128;

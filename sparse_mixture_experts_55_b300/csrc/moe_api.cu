@@ -140,10 +140,9 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
     // epilogue warp, whose latency grows with the real rows it owns; beyond
     // about four rows per expert it stalls the MMA pipeline more than the
     // balanced split saves, so larger batches keep one split.
-    // (the e4m3 gate/up epilogue scales and re-quantises whole rows: one split)
-    if (TKl <= 4 * touched && !fp8)
-      gu = plan_splits(TKl, E, (f + 127) / 128, (d + 63) / 64, clusters,
-                       4.0 * static_cast<double>(TKl) / (static_cast<double>(touched) * d));
+    if (TKl <= 4 * touched)
+      gu = plan_splits(TKl, E, (f + 127) / 128, (d + kbw - 1) / kbw, clusters,
+                       8.0 / wb * static_cast<double>(TKl) / (static_cast<double>(touched) * d));
   }
   L.S = down.S;
   L.kb_per_split = down.kb_per_split;
