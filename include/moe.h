@@ -88,6 +88,15 @@ enum { MOE_BF16 = 0, MOE_F32 = 1, MOE_FP8_E4M3 = 2 };
  * context stays usable.  With MOE_F32 the flag is rejected (that path has no
  * waits). */
 #define MOE_DEBUG_FORCE_TIMEOUT 0x4u
+/* Expert-GEMM form overrides, for measurements (the results are bitwise the
+ * same in every form; ignored when the gate/up contraction is split, i.e. for
+ * decode-sized batches).  By default batches whose experts average 16 or
+ * more 128-row tiles use CTA-pair MMAs (tcgen05 cta_group::2, 256x256 tiles)
+ * and all others use pairs of 128x256 tiles sharing one operand by TMA
+ * multicast. */
+#define MOE_GEMM_PAIR_MMA 0x8u   /* CTA-pair MMAs (256x256 tiles) */
+#define MOE_GEMM_QUAD     0x10u  /* 2x2 tiles per 4-CTA cluster, both operands multicast */
+#define MOE_GEMM_MULTICAST_PAIRS 0x20u  /* pairs of 128x256 tiles, one operand multicast */
 
 /*
  * Workspace size in bytes for moe_forward / moe_route with these sizes, or 0
@@ -118,7 +127,7 @@ MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype)
  *   workspace / ws_bytes: device buffer of at least moe_workspace_bytes().
  *     Calls sharing one workspace must be ordered on the GPU (same stream or
  *     synchronised); concurrent calls need separate workspaces.
- *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT.
+ *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT | one MOE_GEMM_* form.
  * Returns MOE_OK once every kernel is enqueued.
  */
 MOE_API int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
@@ -196,8 +205,7 @@ MOE_API int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *W
  * W1q, W3q [E, f, d] and W2q [E, d, f] are e4m3 codes with scales s1, s3
  * [E, f] and s2 [E, d] from moe_quantize_weights_fp8.  d and f are multiples
  * of 16.  workspace: at least moe_workspace_bytes(T, d, f, E, K,
- * MOE_FP8_E4M3).  flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS |
- * MOE_DEBUG_FORCE_TIMEOUT.  Other rules as moe_forward.
+ * MOE_FP8_E4M3).  flags: as moe_forward.  Other rules as moe_forward.
  */
 MOE_API int moe_forward_fp8(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
                     const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,

@@ -225,6 +225,75 @@ def moe_block(h, Wg, W1, W3, W2, K: int, eps: float = RMS_EPS) -> np.ndarray:
 
 
 # ---------------------------------------------------------------------------
+# Backward pass  [GU section 3 information flow and "Top-K Gating Mechanism
+# and Routing": gradients flow only through the selected experts and their
+# logits; the choice of experts itself is piecewise constant]
+# ---------------------------------------------------------------------------
+@dataclass
+class LayerGrads:
+    dx: np.ndarray       # [T, d]
+    dWg: np.ndarray      # [d, n]
+    dW1: np.ndarray      # [n, d, f]
+    dW3: np.ndarray      # [n, d, f]
+    dW2: np.ndarray      # [n, f, d]
+    dlogits: np.ndarray  # [T, n]
+
+
+def dsilu(z: np.ndarray) -> np.ndarray:
+    """d/dz SiLU(z) = sigma(z) (1 + z (1 - sigma(z)))."""
+    sg = 1.0 / (1.0 + np.exp(-z))
+    return sg * (1.0 + z * (1.0 - sg))
+
+
+def softmax_backward(G: np.ndarray, dG: np.ndarray) -> np.ndarray:
+    """Gradient of the logits for G = softmax over the kept logits (zero
+    elsewhere): dl_i = G_i (dG_i - sum_j G_j dG_j), zero off the kept set."""
+    return G * (dG - np.sum(G * dG, axis=1, keepdims=True))
+
+
+def moe_layer_backward(x, Wg, W1, W3, W2, K: int, dy) -> LayerGrads:
+    """Gradients of L = <dy, y> for y = moe_layer(x, ...), by the chain rule
+    through y = sum_i G_i E_i(x): each selected expert's SwiGLU, the gates
+    G = softmax over the kept logits (zero elsewhere), and the router
+    l = x W_g.  The selected set is held fixed (it has no gradient)."""
+    x64 = f64(x)
+    dy64 = f64(dy)
+    Wg64 = f64(Wg)
+    g = gating(x64, Wg64, K)
+    T, d = x64.shape
+    E = g.G.shape[1]
+    f = W1.shape[2]
+    dx = np.zeros((T, d))
+    dW1 = np.zeros((E, d, f))
+    dW3 = np.zeros((E, d, f))
+    dW2 = np.zeros((E, f, d))
+    dG = np.zeros((T, E))
+    for e in range(E):
+        rows = np.nonzero((g.idx == e).any(axis=1))[0]
+        if rows.size == 0:
+            continue
+        W1e, W3e, W2e = f64(W1[e]), f64(W3[e]), f64(W2[e])
+        xe = x64[rows]
+        a = xe @ W1e
+        b = xe @ W3e
+        s = silu(a)
+        H = s * b
+        ye = H @ W2e                                   # E_e(x) on its tokens
+        dG[rows, e] = np.sum(dy64[rows] * ye, axis=1)  # dL/dG_e
+        dye = g.G[rows, e][:, None] * dy64[rows]       # dL/dE_e(x)
+        dW2[e] = H.T @ dye
+        dH = dye @ W2e.T
+        da = dH * b * dsilu(a)
+        db = dH * s
+        dW1[e] = xe.T @ da
+        dW3[e] = xe.T @ db
+        dx[rows] += da @ W1e.T + db @ W3e.T
+    dl = softmax_backward(g.G, dG)
+    dx += dl @ Wg64.T
+    return LayerGrads(dx, x64.T @ dl, dW1, dW3, dW2, dl)
+
+
+# ---------------------------------------------------------------------------
 # Near-tie bookkeeping for parity checks (float64 logits)
 # ---------------------------------------------------------------------------
 def logit_gaps(logits: np.ndarray, K: int):

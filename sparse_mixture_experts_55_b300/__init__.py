@@ -19,7 +19,8 @@ import torch
 
 from . import _lib
 from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_TIMEOUT, MOE_F32,  # noqa: F401
-                   MOE_FP8_E4M3, MoEError, status_string)
+                   MOE_FP8_E4M3, MOE_GEMM_MULTICAST_PAIRS, MOE_GEMM_PAIR_MMA, MOE_GEMM_QUAD, MoEError,
+                   status_string)
 
 __all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "quantize_weights_fp8",
            "moe_forward_fp8", "moe_forward_fp8_timed", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",

@@ -30,6 +30,9 @@ MOE_NUM_STAGE_EVENTS = 7
 STAGES = ("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")
 MOE_DEBUG_CHECKS = 0x2
 MOE_DEBUG_FORCE_TIMEOUT = 0x4
+MOE_GEMM_PAIR_MMA = 0x8
+MOE_GEMM_QUAD = 0x10
+MOE_GEMM_MULTICAST_PAIRS = 0x20
 
 # name -> (restype, argtypes), one entry per function declared in include/moe.h
 _vp, _i, _sz, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint

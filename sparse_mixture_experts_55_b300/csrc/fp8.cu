@@ -77,102 +77,105 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *
   }
 }
 
+// Maximum of v over the block (blockDim.x a multiple of 32, at most 1024).
+__device__ __forceinline__ float block_max(float v, float *red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  __syncthreads();  // red is free (an earlier row's readers are done)
+  if ((threadIdx.x & 31) == 0) red[w] = v;
+  __syncthreads();
+  float m = 0.f;
+  for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
+  return m;
+}
+
+// 8 values (16 bytes of bf16) to 8 e4m3 codes.
+__device__ __forceinline__ uint2 quant8(uint4 u, float s) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+  uint32_t w[2] = {0, 0};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    const uint32_t q = static_cast<uint32_t>(to_e4m3(f.x / s)) | (static_cast<uint32_t>(to_e4m3(f.y / s)) << 8);
+    w[i >> 1] |= q << (16 * (i & 1));
+  }
+  return make_uint2(w[0], w[1]);
+}
+
+__device__ __forceinline__ float absmax8(uint4 u) {
+  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+  float m = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = __bfloat1622float2(h[i]);
+    m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
+  }
+  return m;
+}
+
 // X_perm8[r, :] = e4m3(x[perm_tok[r], :] / xs[r]) with xs[r] the row's scale;
-// pad rows are zero with scale 0.  One warp per grouped row.
+// pad rows are zero with scale 0.  One block per grouped row (grid-stride),
+// so that a handful of rows (decode) still spreads over many threads.
 __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *__restrict__ x, int T, int d,
                                                            const int32_t *__restrict__ perm_tok,
                                                            const int32_t *__restrict__ poffsets, int E,
                                                            uint8_t *__restrict__ xq, float *__restrict__ xs,
                                                            int *status) {
+  __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
   const int rows = poffsets[E];
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nchunk = d / 8;  // 8 bf16 in, 8 codes out
-  for (int r = gw; r < rows; r += nw) {
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     int tok = perm_tok[r];
     if (tok >= T) {
-      atomicCAS(status, 0, MOE_ERR_DEVICE_BOUNDS);
+      if (threadIdx.x == 0) atomicCAS(status, 0, MOE_ERR_DEVICE_BOUNDS);
       tok = -1;
     }
     uint8_t *dst = xq + static_cast<size_t>(r) * d;
     if (tok < 0) {
-      for (int c = lane; c < nchunk; c += 32) *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(0, 0);
-      if (lane == 0) xs[r] = 0.f;
+      for (int c = threadIdx.x; c < nchunk; c += blockDim.x) *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(0, 0);
+      if (threadIdx.x == 0) xs[r] = 0.f;
       continue;
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * d);
     float m = 0.f;
-    for (int c = lane; c < nchunk; c += 32) {
-      const uint4 u = __ldg(src + c);
-      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        m = fmaxf(m, fmaxf(fabsf(f.x), fabsf(f.y)));
-      }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float s = scale_of(m);
-    for (int c = lane; c < nchunk; c += 32) {
-      const uint4 u = __ldg(src + c);
-      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-      uint32_t w[2] = {0, 0};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = __bfloat1622float2(h[i]);
-        const uint32_t q = static_cast<uint32_t>(to_e4m3(f.x / s)) | (static_cast<uint32_t>(to_e4m3(f.y / s)) << 8);
-        w[i >> 1] |= q << (16 * (i & 1));
-      }
-      *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(w[0], w[1]);
-    }
-    if (lane == 0) xs[r] = s;
+    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) m = fmaxf(m, absmax8(__ldg(src + c)));
+    const float s = scale_of(block_max(m, red));
+    for (int c = threadIdx.x; c < nchunk; c += blockDim.x)
+      *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(__ldg(src + c), s);
+    if (threadIdx.x == 0) xs[r] = s;
   }
 }
 
 // Hq[r, :] = e4m3(H[r, :] / hs[r]) for every real grouped row, with hs[r] =
 // max over the row's n-tiles of the tile maxima habs[r, :] written by the
-// gate/up epilogue (the maxima of the bf16 H values), / 448.  One warp per
-// row; padding rows are left alone (the down projection drops their output).
+// gate/up epilogue (the maxima of the bf16 H values), / 448.  One block per
+// row (grid-stride); padding rows are left alone (the down projection drops
+// their output).
 __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__restrict__ H, int f,
                                                       const float *__restrict__ habs, int n_tiles,
                                                       const int32_t *__restrict__ offsets,
                                                       const int32_t *__restrict__ poffsets, int E,
                                                       uint8_t *__restrict__ hq, float *__restrict__ hs) {
+  __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
   const int rows = poffsets[E];
-  const int lane = threadIdx.x & 31;
-  const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-  const int nw = (gridDim.x * blockDim.x) >> 5;
   const int nchunk = f / 8;
-  for (int r = gw; r < rows; r += nw) {
+  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
     int e = 0;
     while (e < E - 1 && r >= poffsets[e + 1]) ++e;
-    if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row
+    if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row (uniform over the block)
     float m = 0.f;
-    for (int t = lane; t < n_tiles; t += 32) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-    const float s = scale_of(m);
+    for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
+    const float s = scale_of(block_max(m, red));
     const uint4 *src = reinterpret_cast<const uint4 *>(H + static_cast<size_t>(r) * f);
     uint8_t *dst = hq + static_cast<size_t>(r) * f;
-    for (int c = lane; c < nchunk; c += 32) {
-      const uint4 u = src[c];
-      const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-      uint32_t w[2] = {0, 0};
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 v = __bfloat1622float2(h[i]);
-        const uint32_t q = static_cast<uint32_t>(to_e4m3(v.x / s)) | (static_cast<uint32_t>(to_e4m3(v.y / s)) << 8);
-        w[i >> 1] |= q << (16 * (i & 1));
-      }
-      *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(w[0], w[1]);
-    }
-    if (lane == 0) hs[r] = s;
+#pragma unroll 4
+    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], s);
+    if (threadIdx.x == 0) hs[r] = s;
   }
 }
 
@@ -192,7 +195,7 @@ cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void
 
 cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const Ptrs &P, int num_sms,
                                 cudaStream_t s) {
-  int blocks = (R + 7) / 8;
+  int blocks = R;  // one block per grouped row
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
   return launch_kernel(gather_quant_kernel, dim3(blocks), dim3(256), 0, s, true,
@@ -202,7 +205,7 @@ cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const
 }
 
 cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
-  int blocks = (R + 7) / 8;
+  int blocks = R;  // one block per grouped row
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
   return launch_kernel(quant_h_kernel, dim3(blocks), dim3(256), 0, s, true,

@@ -65,7 +65,6 @@ constexpr int BM = 128;
 constexpr int BN = 256;
 constexpr int BK = 64;
 constexpr int A_BYTES = BM * BK * 2;    // 16 KiB
-constexpr int A_HALF = A_BYTES / 2;     // 64 rows
 constexpr int B_CHUNK = 64 * BK * 2;    // 8 KiB: 64 N-columns x 64 K-rows
 constexpr int MAX_STAGES = 6;
 // Ring geometry of the two forms (stages, B bytes per CTA and stage).
@@ -83,9 +82,18 @@ static_assert(Ring<true>::SMEM <= 232448 && Ring<false>::SMEM <= 232448, "shared
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;  // 512: the whole TMEM of the SM
 constexpr int NUM_THREADS = 192;
-constexpr int CLUSTER = 2;
 constexpr uint16_t kBothCtas = 0x3;
 constexpr int GROUP_PAIRS = 16;          // M-pairs rastered together (weight reuse in L2)
+
+// The three forms of the kernel (see the file comment).
+enum { FORM_MC2 = 0, FORM_PAIR = 1, FORM_MC4 = 2 };
+template <int FORM>
+struct FormInfo {
+  static constexpr bool PAIR = FORM == FORM_PAIR;  // cta_group::2 MMAs
+  static constexpr bool QUAD = FORM == FORM_MC4;   // 2x2 tiles per cluster
+  static constexpr int CL = QUAD ? 4 : 2;           // CTAs per cluster
+  static constexpr uint16_t ALL = QUAD ? 0xF : 0x3;
+};
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
@@ -145,21 +153,24 @@ struct Tile {
 // group) with the pair fastest, so clusters running together share weight
 // panels; then, for an odd m-tile count, the N-pairs of its last m-tile
 // (multicast pairs) or one more M-pair with a phantom second tile (pair MMA).
-template <bool PAIR>
+template <int FORM>
 __device__ __forceinline__ int units_of(int mt_e, int NT, int S) {
-  if (PAIR) return ((mt_e + 1) >> 1) * NT * S;
+  if (FORM == FORM_PAIR) return ((mt_e + 1) >> 1) * NT * S;
+  if (FORM == FORM_MC4) return (mt_e >> 1) * ((NT + 1) >> 1) * S + (mt_e & 1) * ((NT + 3) >> 2) * S;
   return (mt_e >> 1) * NT * S + (mt_e & 1) * ((NT + 1) >> 1) * S;
 }
 
-template <bool PAIR>
+template <int FORM>
 __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S, int rank) {
   Tile t;
   int e = 0;
   while (u >= c.ustart[e + 1]) ++e;
   int r = u - c.ustart[e];
   const int mt_e = c.mtiles[e];
-  const int mp = PAIR ? (mt_e + 1) >> 1 : mt_e >> 1;
-  const int per = NT * S;
+  const int mp = FORM == FORM_PAIR ? (mt_e + 1) >> 1 : mt_e >> 1;
+  // n positions per M-pair unit: every n-tile, or n-tile pairs for 2x2 tiles
+  const int nu = FORM == FORM_MC4 ? (NT + 1) >> 1 : NT;
+  const int per = nu * S;
   t.e = e;
   if (r < mp * per) {
     const int full_groups = mp / GROUP_PAIRS;
@@ -176,15 +187,25 @@ __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S,
     }
     const int pi = r % gs;
     r /= gs;
-    t.nt = r % NT;
-    t.s = r / NT;
-    t.mt = 2 * (g * GROUP_PAIRS + pi) + rank;
+    if (FORM == FORM_MC4) {
+      // CTA (i, j) = (rank >> 1, rank & 1) takes m-tile 2p + i, n-tile 2q + j
+      t.nt = 2 * (r % nu) + (rank & 1);  // may equal NT for odd NT: all its loads and stores fall outside
+      t.s = r / nu;
+      t.mt = 2 * (g * GROUP_PAIRS + pi) + (rank >> 1);
+    } else {
+      t.nt = r % NT;
+      t.s = r / NT;
+      t.mt = 2 * (g * GROUP_PAIRS + pi) + rank;
+    }
     t.npair = false;
   } else {
+    // the last m-tile of an odd count: the cluster's CTAs take consecutive
+    // n-tiles of it and share its A tile
     r -= mp * per;
-    const int ntp = (NT + 1) >> 1;
-    t.nt = 2 * (r % ntp) + rank;  // may equal NT for odd NT: all its loads and stores fall outside
-    t.s = r / ntp;
+    const int nc = FORM == FORM_MC4 ? 4 : 2;
+    const int ntg = (NT + nc - 1) / nc;
+    t.nt = nc * (r % ntg) + rank;  // may reach NT: all its loads and stores fall outside
+    t.s = r / ntg;
     t.mt = mt_e - 1;
     t.npair = true;
   }
@@ -212,11 +233,15 @@ __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Ctrl &
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
 
-template <int MODE, bool PAIR, bool FP8>
+template <int MODE, int FORM, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     expert_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmA_half,
-                       const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
-                       const GemmArgs args) {
+                       const __grid_constant__ CUtensorMap tmA_quarter, const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1, const GemmArgs args) {
+  constexpr bool PAIR = FormInfo<FORM>::PAIR;
+  constexpr bool QUAD = FormInfo<FORM>::QUAD;
+  constexpr int CL = FormInfo<FORM>::CL;
+  constexpr uint16_t kAll = FormInfo<FORM>::ALL;  // every CTA of the cluster
   using RG = Ring<PAIR>;
   constexpr int STAGES = RG::STAGES;
   // a k-block is one 128-byte row of A and of B in shared memory: 64 bf16 or
@@ -239,8 +264,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < STAGES; ++s) {
       ptx::mbar_init(&c.full[s], 1);
-      // multicast pairs: both CTAs' MMAs release a stage; pair MMA: one commit
-      ptx::mbar_init(&c.empty[s], PAIR ? 1 : CLUSTER);
+      // multicast forms: every CTA's MMAs release a stage; pair MMA: one commit
+      ptx::mbar_init(&c.empty[s], PAIR ? 1 : CL);
     }
     for (int a = 0; a < 2; ++a) {
       ptx::mbar_init(&c.tfull[a], 1);
@@ -248,7 +273,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     ptx::mbar_init(&c.drain, 1);
     ptx::mbar_init(&c.stall, 1);
-    ptx::mbar_init(&c.exit_bar, 1);
+    ptx::mbar_init(&c.exit_bar, CL - 1);  // the other CTAs' "done" arrivals
     ptx::fence_barrier_init();
   }
   // Barriers must be initialised in both CTAs before either signals the other.
@@ -269,7 +294,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       c.uoff[e] = args.offsets[e];
       c.mtiles[e] = mt;
       c.ustart[e] = acc;
-      acc += units_of<PAIR>(mt, NT, S);
+      acc += units_of<FORM>(mt, NT, S);
     }
     if (bad) {
       atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
@@ -299,6 +324,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   if (warp == 0 && lane == 0) {
     ptx::prefetch_tmap(&tmA);
     if (!PAIR) ptx::prefetch_tmap(&tmA_half);
+    if (QUAD) ptx::prefetch_tmap(&tmA_quarter);
     ptx::prefetch_tmap(&tmB0);
     if (MODE == MODE_GATE_UP) ptx::prefetch_tmap(&tmB1);
   }
@@ -319,7 +345,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint64_t pol_b = ptx::policy_evict_normal();
       bool ok = true;
       for (int u = cluster; ok && u < total; u += nclusters) {
-        const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
+        const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
         const int row0 = c.poff[t.e] + t.mt * BM;
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
@@ -328,90 +354,66 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint8_t *a_dst = sA + p_stage * A_BYTES;
           uint8_t *b_dst = sB + p_stage * RG::B_BYTES;
           const int k0 = kb * KB_ELEMS;
-          if (FP8) {
-            // e4m3 weights are stored K-contiguous ([E, N, K]): a B box is 128
-            // columns (rows of the bank) x 128 k, 16 KiB, one 128-byte row per column
-            if (PAIR) {
-              if (leader) ptx::mbar_arrive_expect_tx(&c.full[p_stage], RG::STAGE_TX);
-              const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[p_stage]), 0);
-              ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, row0, pol_a);
-              if (MODE == MODE_GATE_UP)
-                ptx::tma_load_3d_pair(b_dst, rank == 0 ? &tmB0 : &tmB1, bar, k0, t.nt * (BN / 2), t.e, pol_b);
-              else
-                ptx::tma_load_3d_pair(b_dst, &tmB0, bar, k0, t.nt * BN + rank * (BN / 2), t.e, pol_b);
-            } else {
-              uint64_t *bar = &c.full[p_stage];
-              ptx::mbar_arrive_expect_tx(bar, RG::STAGE_TX);
-              constexpr int HALF_B = 2 * B_CHUNK;  // 128 columns
-              if (!t.npair) {
-                ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);
-                if (MODE == MODE_GATE_UP)
-                  ptx::tma_load_3d_mc(b_dst + rank * HALF_B, rank == 0 ? &tmB0 : &tmB1, bar, k0, t.nt * (BN / 2), t.e,
-                                      kBothCtas, pol_b);
-                else
-                  ptx::tma_load_3d_mc(b_dst + rank * HALF_B, &tmB0, bar, k0, t.nt * BN + rank * (BN / 2), t.e,
-                                      kBothCtas, pol_b);
-              } else {
-                ptx::tma_load_2d_mc(a_dst + rank * A_HALF, &tmA_half, bar, k0, row0 + 64 * rank, kBothCtas, pol_a);
-                if (MODE == MODE_GATE_UP) {
-                  ptx::tma_load_3d(b_dst, &tmB0, bar, k0, t.nt * (BN / 2), t.e, pol_b);
-                  ptx::tma_load_3d(b_dst + HALF_B, &tmB1, bar, k0, t.nt * (BN / 2), t.e, pol_b);
-                } else {
-                  ptx::tma_load_3d(b_dst, &tmB0, bar, k0, t.nt * BN, t.e, pol_b);
-                  ptx::tma_load_3d(b_dst + HALF_B, &tmB0, bar, k0, t.nt * BN + BN / 2, t.e, pol_b);
-                }
-              }
-            }
-          } else if (PAIR) {
+          if (PAIR) {
             // both CTAs' copies complete on the first CTA's barrier, which
-            // expects the bytes of both
+            // expects the bytes of both; CTA r holds half r of the 256 B
+            // columns (gate/up: W1 for CTA 0, W3 for CTA 1)
             if (leader) ptx::mbar_arrive_expect_tx(&c.full[p_stage], RG::STAGE_TX);
             const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[p_stage]), 0);
             ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, row0, pol_a);
-            if (MODE == MODE_GATE_UP) {
-              // CTA 0 holds the W1 half of the 256 columns, CTA 1 the W3 half
-              const int n0 = t.nt * (BN / 2);
-              const CUtensorMap *mb = rank == 0 ? &tmB0 : &tmB1;
-              ptx::tma_load_3d_pair(b_dst, mb, bar, n0, k0, t.e, pol_b);
-              ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, n0 + 64, k0, t.e, pol_b);
+            const CUtensorMap *mb = (MODE == MODE_GATE_UP && rank == 1) ? &tmB1 : &tmB0;
+            const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + rank * (BN / 2);
+            if (FP8) {
+              // e4m3 banks are K-contiguous ([E, N, K]): one 128 x 128 box, 16 KiB
+              ptx::tma_load_3d_pair(b_dst, mb, bar, k0, nb, t.e, pol_b);
             } else {
-              const int n0 = t.nt * BN + rank * (BN / 2);
-              ptx::tma_load_3d_pair(b_dst, &tmB0, bar, n0, k0, t.e, pol_b);
-              ptx::tma_load_3d_pair(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, k0, t.e, pol_b);
+              ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, t.e, pol_b);
+              ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, t.e, pol_b);
             }
           } else {
+            // multicast forms: this CTA's share of the A and B tiles, each
+            // delivered to the CTAs of the cluster that compute with it
             uint64_t *bar = &c.full[p_stage];
-            ptx::mbar_arrive_expect_tx(bar, RG::STAGE_TX);  // own and peer copies together fill the stage
-            if (!t.npair) {
-              ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);
-              // this CTA's two of the four B boxes, delivered to both CTAs
-              if (MODE == MODE_GATE_UP) {
-                const int n0 = t.nt * (BN / 2);
-                const CUtensorMap *mb = rank == 0 ? &tmB0 : &tmB1;  // W1 boxes from rank 0, W3 boxes from rank 1
-                ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, mb, bar, n0, k0, t.e, kBothCtas, pol_b);
-                ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, mb, bar, n0 + 64, k0, t.e, kBothCtas, pol_b);
-              } else {
-                const int n0 = t.nt * BN;
-                ptx::tma_load_3d_mc(b_dst + (2 * rank) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank), k0, t.e,
-                                    kBothCtas, pol_b);
-                ptx::tma_load_3d_mc(b_dst + (2 * rank + 1) * B_CHUNK, &tmB0, bar, n0 + 64 * (2 * rank + 1), k0, t.e,
-                                    kBothCtas, pol_b);
-              }
+            ptx::mbar_arrive_expect_tx(bar, RG::STAGE_TX);  // own and multicast-in copies fill the stage
+            if (!t.npair && !QUAD) {
+              ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);  // M-pair: own A tile
             } else {
-              // this CTA's 64 of the shared 128 A rows, delivered to both CTAs
-              ptx::tma_load_2d_mc(a_dst + rank * A_HALF, &tmA_half, bar, k0, row0 + 64 * rank, kBothCtas, pol_a);
-              if (MODE == MODE_GATE_UP) {
-                const int n0 = t.nt * (BN / 2);
-                ptx::tma_load_3d(b_dst, &tmB0, bar, n0, k0, t.e, pol_b);
-                ptx::tma_load_3d(b_dst + B_CHUNK, &tmB0, bar, n0 + 64, k0, t.e, pol_b);
-                ptx::tma_load_3d(b_dst + 2 * B_CHUNK, &tmB1, bar, n0, k0, t.e, pol_b);
-                ptx::tma_load_3d(b_dst + 3 * B_CHUNK, &tmB1, bar, n0 + 64, k0, t.e, pol_b);
+              // shared A tile: halves (N-pair; 2x2 tiles: the two CTAs of a row)
+              // or quarters (the odd m-tile of the 2x2 form: all four CTAs)
+              const bool quarter = QUAD && t.npair;
+              const int part = quarter ? rank : (QUAD ? (rank & 1) : rank);
+              const int prow = quarter ? 32 : 64;
+              const uint16_t amask = quarter ? uint16_t(0xF) : (QUAD ? uint16_t(0x3 << (rank & 2)) : kBothCtas);
+              ptx::tma_load_2d_mc(a_dst + part * prow * 128, quarter ? &tmA_quarter : &tmA_half, bar, k0,
+                                  row0 + part * prow, amask, pol_a);
+            }
+            // B: half h (128 of the 256 columns) of the tile; gate/up half 0 is
+            // W1, half 1 is W3
+            auto load_b_half = [&](int h, uint16_t mask) {
+              const CUtensorMap *mb = (MODE == MODE_GATE_UP && h == 1) ? &tmB1 : &tmB0;
+              const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + h * (BN / 2);
+              uint8_t *dst = b_dst + h * (2 * B_CHUNK);
+              if (FP8) {
+                if (mask) ptx::tma_load_3d_mc(dst, mb, bar, k0, nb, t.e, mask, pol_b);
+                else ptx::tma_load_3d(dst, mb, bar, k0, nb, t.e, pol_b);
               } else {
-                const int n0 = t.nt * BN;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                  ptx::tma_load_3d(b_dst + j * B_CHUNK, &tmB0, bar, n0 + 64 * j, k0, t.e, pol_b);
+                if (mask) {
+                  ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, t.e, mask, pol_b);
+                  ptx::tma_load_3d_mc(dst + B_CHUNK, mb, bar, nb + 64, k0, t.e, mask, pol_b);
+                } else {
+                  ptx::tma_load_3d(dst, mb, bar, nb, k0, t.e, pol_b);
+                  ptx::tma_load_3d(dst + B_CHUNK, mb, bar, nb + 64, k0, t.e, pol_b);
+                }
               }
+            };
+            if (t.npair) {
+              load_b_half(0, 0);  // own n-tile, whole
+              load_b_half(1, 0);
+            } else if (QUAD) {
+              // row i of the 2x2 tiles loads half i of its column's B tile, for both CTAs of that column
+              load_b_half(rank >> 1, uint16_t((1u << (rank & 1)) | (1u << (2 + (rank & 1)))));
+            } else {
+              load_b_half(rank, kBothCtas);  // M-pair: half r, for both CTAs
             }
           }
           issued |= 1u << p_stage;
@@ -434,7 +436,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // failure-path test: this wait expires, raising the CTA's abort flag
       if (args.force_timeout) ok = wait_bounded(&c.stall, 0, c, args.status, true);
       for (int u = cluster; ok && u < total; u += nclusters) {
-        const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
+        const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
         const int acc = local & 1;
@@ -467,8 +469,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
           // frees the stage in both CTAs once these MMAs have read it
-          if (PAIR) ptx::mma_commit_pair_mc(&c.empty[stage], kBothCtas);
-          else ptx::mma_commit_mc(&c.empty[stage], kBothCtas);
+          if (PAIR) ptx::mma_commit_pair_mc(&c.empty[stage], kAll);
+          else ptx::mma_commit_mc(&c.empty[stage], kAll);
           if (++stage == STAGES) { stage = 0; phase ^= 1u; }
         }
         if (!ok) break;
@@ -486,7 +488,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tempty_at1 = ptx::mapa_shared(ptx::smem_u32(&c.tempty[1]), PAIR ? 0 : rank);
     int local = 0;
     for (int u = cluster; u < total; u += nclusters) {
-      const Tile t = decode_unit<PAIR>(u, c, NT, S, rank);
+      const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
       const int acc = local & 1;
       const uint32_t apar = (local >> 1) & 1;
       int ok = 1;
@@ -776,9 +778,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
   }
-  // Neither CTA leaves while its peer may still send it copies or arrivals.
+  // No CTA leaves while another CTA of the cluster may still send it copies
+  // or arrivals.
   if (threadIdx.x == 0) {
-    ptx::mbar_arrive_remote(&c.exit_bar, static_cast<uint32_t>(rank ^ 1));
+    for (int r2 = 0; r2 < CL; ++r2)
+      if (r2 != rank) ptx::mbar_arrive_remote(&c.exit_bar, static_cast<uint32_t>(r2));
     wait_bounded(&c.exit_bar, 0, c, args.status, false);
   }
   __syncthreads();
@@ -865,77 +869,110 @@ struct DevState {
   int clusters = 0;
 };
 
-template <int MODE, bool PAIR, bool FP8>
+template <int MODE, int FORM, bool FP8>
 cudaError_t set_smem_attr() {
-  return cudaFuncSetAttribute(expert_gemm_kernel<MODE, PAIR, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Ring<PAIR>::SMEM);
+  return cudaFuncSetAttribute(expert_gemm_kernel<MODE, FORM, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Ring<FormInfo<FORM>::PAIR>::SMEM);
 }
 
-template <bool PAIR>
+template <int FORM>
 cudaError_t max_clusters(int num_sms, int *n) {
+  constexpr int CL = FormInfo<FORM>::CL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((num_sms / CLUSTER) * CLUSTER);
+  cfg.gridDim = dim3((num_sms / CL) * CL);
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = Ring<PAIR>::SMEM;
+  cfg.dynamicSmemBytes = Ring<FormInfo<FORM>::PAIR>::SMEM;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaOccupancyMaxActiveClusters(n, expert_gemm_kernel<MODE_GATE_UP, PAIR, false>, &cfg);
+  return cudaOccupancyMaxActiveClusters(n, expert_gemm_kernel<MODE_GATE_UP, FORM, false>, &cfg);
 }
 
-cudaError_t device_state(int num_sms, int *clusters) {
+template <int MODE>
+cudaError_t set_attrs_mode() {
+  cudaError_t err = set_smem_attr<MODE, FORM_MC2, false>();
+  if (err == cudaSuccess) err = set_smem_attr<MODE, FORM_PAIR, false>();
+  if (err == cudaSuccess) err = set_smem_attr<MODE, FORM_MC4, false>();
+  if (err == cudaSuccess) err = set_smem_attr<MODE, FORM_MC2, true>();
+  if (err == cudaSuccess) err = set_smem_attr<MODE, FORM_PAIR, true>();
+  if (err == cudaSuccess) err = set_smem_attr<MODE, FORM_MC4, true>();
+  return err;
+}
+
+// Persistent grid sizes: co-resident 2-CTA clusters (pair forms) and 4-CTA
+// clusters (2x2 form).
+struct Grids {
+  int clusters2 = 0, clusters4 = 0;
+};
+
+cudaError_t device_state(int num_sms, Grids *g) {
   int dev = 0;
   cudaError_t err = cudaGetDevice(&dev);
   if (err != cudaSuccess) return err;
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
   static std::mutex mu;
   static DevState st[64];
+  static Grids grids[64];
   std::lock_guard<std::mutex> lock(mu);
   if (!st[dev].ready) {
-    err = set_smem_attr<MODE_GATE_UP, false, false>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, false, false>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, true, false>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, true, false>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, false, true>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, false, true>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_GATE_UP, true, true>();
-    if (err == cudaSuccess) err = set_smem_attr<MODE_DOWN, true, true>();
+    err = set_attrs_mode<MODE_GATE_UP>();
+    if (err == cudaSuccess) err = set_attrs_mode<MODE_DOWN>();
     if (err != cudaSuccess) return err;
-    int n0 = 0, n1 = 0;
-    err = max_clusters<false>(num_sms, &n0);
-    if (err == cudaSuccess) err = max_clusters<true>(num_sms, &n1);
+    int n0 = 0, n1 = 0, n4 = 0;
+    err = max_clusters<FORM_MC2>(num_sms, &n0);
+    if (err == cudaSuccess) err = max_clusters<FORM_PAIR>(num_sms, &n1);
+    if (err == cudaSuccess) err = max_clusters<FORM_MC4>(num_sms, &n4);
     if (err != cudaSuccess) return err;
-    const int n = n0 < n1 ? n0 : n1;  // one persistent grid size for both forms
+    const int n = n0 < n1 ? n0 : n1;  // one persistent grid size for both 2-CTA forms
     if (n < 1) return cudaErrorInvalidConfiguration;
+    grids[dev].clusters2 = n;
+    grids[dev].clusters4 = n4;  // 0 if 4-CTA clusters cannot be resident: that form is not used
     st[dev].clusters = n;
     st[dev].ready = true;
   }
-  *clusters = st[dev].clusters;
+  *g = grids[dev];
   return cudaSuccess;
 }
 
-template <int MODE, bool PAIR, bool FP8>
-cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMap &a, const CUtensorMap &ah,
-                        const CUtensorMap &b0, const CUtensorMap &b1, const GemmArgs &args) {
+template <int MODE, int FORM, bool FP8>
+cudaError_t launch_gemm(const Grids &g, cudaStream_t s, bool pdl, const CUtensorMap &a, const CUtensorMap &ah,
+                        const CUtensorMap &aq, const CUtensorMap &b0, const CUtensorMap &b1, const GemmArgs &args) {
+  constexpr int CL = FormInfo<FORM>::CL;
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(clusters * CLUSTER);
+  cfg.gridDim = dim3((FORM == FORM_MC4 ? g.clusters4 : g.clusters2) * CL);
   cfg.blockDim = dim3(NUM_THREADS);
-  cfg.dynamicSmemBytes = Ring<PAIR>::SMEM;
+  cfg.dynamicSmemBytes = Ring<FormInfo<FORM>::PAIR>::SMEM;
   cfg.stream = s;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = CLUSTER;
+  attr[0].val.clusterDim.x = CL;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
   attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = pdl ? 2 : 1;
-  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE, PAIR, FP8>, a, ah, b0, b1, args);
+  return cudaLaunchKernelEx(&cfg, expert_gemm_kernel<MODE, FORM, FP8>, a, ah, aq, b0, b1, args);
+}
+
+// The form a call's grouping calls for (see ws_layout), and whether the 2x2
+// form can run on this device.
+int pick_form(const WsLayout &L, const Grids &g) {
+  if (L.form == FORM_MC4 && g.clusters4 < 1) return FORM_MC2;
+  return L.form;
+}
+
+template <int MODE, bool FP8>
+cudaError_t launch_form(int form, const Grids &g, cudaStream_t s, bool pdl, const CUtensorMap &a,
+                        const CUtensorMap &ah, const CUtensorMap &aq, const CUtensorMap &b0, const CUtensorMap &b1,
+                        const GemmArgs &args) {
+  if (form == FORM_PAIR) return launch_gemm<MODE, FORM_PAIR, FP8>(g, s, pdl, a, ah, aq, b0, b1, args);
+  if (form == FORM_MC4) return launch_gemm<MODE, FORM_MC4, FP8>(g, s, pdl, a, ah, aq, b0, b1, args);
+  return launch_gemm<MODE, FORM_MC2, FP8>(g, s, pdl, a, ah, aq, b0, b1, args);
 }
 
 }  // namespace
@@ -943,13 +980,15 @@ cudaError_t launch_gemm(int clusters, cudaStream_t s, bool pdl, const CUtensorMa
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
                                      cudaStream_t s, void *const *mid_event) {
-  int clusters = 0;
-  cudaError_t err = device_state(num_sms, &clusters);
+  Grids grids;
+  cudaError_t err = device_state(num_sms, &grids);
   if (err != cudaSuccess) return err;
-  CUtensorMap tm_x, tm_xh, tm_w1, tm_w3, tm_h, tm_hh, tm_w2;
+  const int form = pick_form(L, grids);
+  CUtensorMap tm_x, tm_xh, tm_xq, tm_w1, tm_w3, tm_h, tm_hh, tm_hq, tm_w2;
   if (!tmap_2d(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d(&tm_xh, P.xperm, d, L.R, BM / 2) ||
-      !tmap_3d(&tm_w1, W1, f, d, E) || !tmap_3d(&tm_w3, W3, f, d, E) || !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) ||
-      !tmap_2d(&tm_hh, P.hbuf, f, L.R, BM / 2) || !tmap_3d(&tm_w2, W2, d, f, E))
+      !tmap_2d(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_3d(&tm_w1, W1, f, d, E) || !tmap_3d(&tm_w3, W3, f, d, E) ||
+      !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) || !tmap_2d(&tm_hh, P.hbuf, f, L.R, BM / 2) ||
+      !tmap_2d(&tm_hq, P.hbuf, f, L.R, BM / 4) || !tmap_3d(&tm_w2, W2, d, f, E))
     return cudaErrorInvalidValue;
 
   GemmArgs g1{};
@@ -970,8 +1009,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.kb_per_split = L.kb_per_split_gu;
   g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
   g1.status = P.status;
-  err = L.pair ? launch_gemm<MODE_GATE_UP, true, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
-               : launch_gemm<MODE_GATE_UP, false, false>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
+  err = launch_form<MODE_GATE_UP, false>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
@@ -986,23 +1024,23 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
-  return L.pair ? launch_gemm<MODE_DOWN, true, false>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2)
-                : launch_gemm<MODE_DOWN, false, false>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2,
-                                                       g2);
+  return launch_form<MODE_DOWN, false>(form, grids, s, mid_event == nullptr, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 
 cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
                                     const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
                                     const Ptrs &P, unsigned flags, int num_sms, cudaStream_t s,
                                     void *const *mid_event) {
-  int clusters = 0;
-  cudaError_t err = device_state(num_sms, &clusters);
+  Grids grids;
+  cudaError_t err = device_state(num_sms, &grids);
   if (err != cudaSuccess) return err;
+  const int form = pick_form(L, grids);
   // e4m3 operands: X_perm [R, d], H [R, f] and the banks [E, N, K], all K-contiguous
-  CUtensorMap tm_x, tm_xh, tm_w1, tm_w3, tm_h, tm_hh, tm_w2;
+  CUtensorMap tm_x, tm_xh, tm_xq, tm_w1, tm_w3, tm_h, tm_hh, tm_hq, tm_w2;
   if (!tmap_2d_u8(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d_u8(&tm_xh, P.xperm, d, L.R, BM / 2) ||
-      !tmap_3d_u8(&tm_w1, W1q, d, f, E) || !tmap_3d_u8(&tm_w3, W3q, d, f, E) ||
-      !tmap_2d_u8(&tm_h, P.hq, f, L.R, BM) || !tmap_2d_u8(&tm_hh, P.hq, f, L.R, BM / 2) ||
+      !tmap_2d_u8(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_3d_u8(&tm_w1, W1q, d, f, E) ||
+      !tmap_3d_u8(&tm_w3, W3q, d, f, E) || !tmap_2d_u8(&tm_h, P.hq, f, L.R, BM) ||
+      !tmap_2d_u8(&tm_hh, P.hq, f, L.R, BM / 2) || !tmap_2d_u8(&tm_hq, P.hq, f, L.R, BM / 4) ||
       !tmap_3d_u8(&tm_w2, W2q, f, d, E))
     return cudaErrorInvalidValue;
 
@@ -1027,8 +1065,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g1.col_scale1 = s3;
   g1.habs = P.habs;
   g1.status = P.status;
-  err = L.pair ? launch_gemm<MODE_GATE_UP, true, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1)
-               : launch_gemm<MODE_GATE_UP, false, true>(clusters, s, true, tm_x, tm_xh, tm_w1, tm_w3, g1);
+  err = launch_form<MODE_GATE_UP, true>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   // H rows to e4m3 with their own scales, inside the gate/up stage
   if (err == cudaSuccess) err = launch_quant_h(f, E, L.R, g1.num_n_tiles, P, num_sms, s);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
@@ -1049,9 +1086,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g2.col_scale0 = s2;
   g2.col_scale1 = nullptr;
   g2.habs = nullptr;
-  return L.pair ? launch_gemm<MODE_DOWN, true, true>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2, g2)
-                : launch_gemm<MODE_DOWN, false, true>(clusters, s, mid_event == nullptr, tm_h, tm_hh, tm_w2, tm_w2,
-                                                      g2);
+  return launch_form<MODE_DOWN, true>(form, grids, s, mid_event == nullptr, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 
 }  // namespace moe

@@ -57,7 +57,7 @@ struct WsLayout {
   int kb_per_split;
   int S_gu;           // split count over the contraction of the gate/up projection
   int kb_per_split_gu;
-  bool pair;          // run the expert GEMMs as CTA-pair (cta_group::2) 256-row tiles
+  int form;           // expert GEMM form: 0 multicast pairs, 1 CTA-pair MMA, 2 2x2 multicast tiles
   int route_tpb;      // tokens per router block
   int n_route_blocks;
 };

@@ -51,6 +51,23 @@ bool overlaps(const void *a, size_t na, const void *b, size_t nb) {
   return x < y + nb && y < x + na;
 }
 
+constexpr unsigned kFormFlags = MOE_GEMM_PAIR_MMA | MOE_GEMM_QUAD | MOE_GEMM_MULTICAST_PAIRS;
+
+// At most one form flag; returns false for a combination.
+bool form_flags_ok(unsigned flags) {
+  const unsigned f = flags & kFormFlags;
+  return (f & (f - 1)) == 0;
+}
+
+// The layout's GEMM form, overridden by a form flag unless the gate/up
+// contraction is split.
+void apply_form_flags(WsLayout &L, unsigned flags) {
+  if (L.S_gu != 1) return;
+  if (flags & MOE_GEMM_PAIR_MMA) L.form = 1;
+  if (flags & MOE_GEMM_QUAD) L.form = 2;
+  if (flags & MOE_GEMM_MULTICAST_PAIRS) L.form = 0;
+}
+
 // bytes per element of the tokens x, y (the e4m3 variant keeps them bf16)
 int elem_bytes(int dtype) { return dtype == MOE_F32 ? 4 : 2; }
 
@@ -148,10 +165,12 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   L.kb_per_split = down.kb_per_split;
   L.S_gu = gu.S;
   L.kb_per_split_gu = gu.kb_per_split;
-  // CTA-pair MMAs once experts average two or more 128-row tiles: the pair
-  // halves each CTA's weight-tile traffic and shared-memory footprint; with
-  // fewer rows the phantom half-tile of an odd tile count would dominate.
-  L.pair = dtype != MOE_F32 && touched > 0 && TKl >= 2LL * kSegPad * touched && L.S_gu == 1;
+  // Expert GEMM form (gemm_tc.cu): CTA-pair MMAs once experts average 16 or
+  // more 128-row tiles (the phantom half-tile of an odd count then costs at
+  // most ~3%), multicast pairs otherwise.  Measured on B300 under the power
+  // cap: pairs are ~1% faster at 16+ tiles per expert and ~1% slower at 8;
+  // the 2x2 form is 3% slower at both.
+  L.form = (dtype != MOE_F32 && touched > 0 && TKl >= 16LL * kSegPad * touched && L.S_gu == 1) ? 1 : 0;
   const size_t TK = static_cast<size_t>(T) * K;
   const size_t R = static_cast<size_t>(L.R);
   size_t o = 0;
@@ -229,7 +248,8 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;  // e4m3 weights go through moe_forward_fp8
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
-  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT | kFormFlags)) return MOE_ERR_INVALID_ARG;
+  if (!form_flags_ok(flags)) return MOE_ERR_INVALID_ARG;
   if ((flags & MOE_DEBUG_FORCE_TIMEOUT) && dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
   if (T == 0) return MOE_OK;  // empty input: nothing to compute, x and y may be NULL
   if (!x || !Wg || !W1 || !W3 || !W2 || !y) return MOE_ERR_INVALID_ARG;
@@ -239,8 +259,9 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   if (T > 0 && overlaps(x, act_bytes, y, act_bytes)) return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   const int sms = sm_count_or_default();
-  const WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
+  WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  apply_form_flags(L, flags);
   st = check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -283,7 +304,7 @@ int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, c
   if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
-  if (flags & ~(MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT | kFormFlags)) return MOE_ERR_INVALID_ARG;
   if (!(eps > 0.f)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!h || !aligned16(h)) return MOE_ERR_INVALID_ARG;
@@ -328,7 +349,8 @@ static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, cons
   constexpr int dtype = MOE_FP8_E4M3;
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
-  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT | kFormFlags)) return MOE_ERR_INVALID_ARG;
+  if (!form_flags_ok(flags)) return MOE_ERR_INVALID_ARG;
   if (T == 0) return MOE_OK;
   if (!x || !Wg || !W1q || !W3q || !W2q || !s1 || !s3 || !s2 || !y) return MOE_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(Wg) || !aligned16(W1q) || !aligned16(W3q) || !aligned16(W2q) || !aligned16(y) ||
@@ -338,8 +360,9 @@ static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, cons
   if (overlaps(x, act_bytes, y, act_bytes)) return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   const int sms = sm_count_or_default();
-  const WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
+  WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  apply_form_flags(L, flags);
   st = check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);

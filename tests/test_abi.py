@@ -88,6 +88,7 @@ def _fwd(lib, **kw):
     (dict(W1=0x3008), _lib.MOE_ERR_INVALID_ARG),                   # misaligned
     (dict(y=0x1000 + 16 * 64 * 2 - 16), _lib.MOE_ERR_INVALID_ARG),  # y overlaps x
     (dict(flags=0x80), _lib.MOE_ERR_INVALID_ARG),
+    (dict(flags=0x18), _lib.MOE_ERR_INVALID_ARG),                  # two GEMM forms at once
     (dict(ws=0), _lib.MOE_ERR_WORKSPACE),
     (dict(ws=0x200008), _lib.MOE_ERR_WORKSPACE),
     (dict(ws_bytes=1024), _lib.MOE_ERR_WORKSPACE),

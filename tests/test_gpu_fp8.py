@@ -110,3 +110,14 @@ def test_fp8_full_size_decode_one_token(moe, cuda_device):
     err = parity.rel_linf(_np(y.float()), ref.y)
     print(f"\nfp8 full-size T=1: experts {sel}, rel err {err:.2e}")
     assert err <= 2e-2
+
+
+@pytest.mark.parametrize("T,d,f,E,K", [(1100, 512, 1024, 4, 2), (700, 256, 384, 2, 1)])
+def test_fp8_gemm_forms_agree_bit_for_bit(moe, T, d, f, E, K):
+    x, Wg, W1, W3, W2 = _fp8_case(T, d, f, E, K, seed=60 + T)
+    dev = torch.device("cuda:0")
+    q = [t for W_ in (W1, W3, W2) for t in moe.quantize_weights_fp8(W_.to(dev))]
+    outs = [moe.moe_forward_fp8(x.to(dev), Wg.to(dev), *q, K, flags=fl)
+            for fl in (moe.MOE_GEMM_MULTICAST_PAIRS, moe.MOE_GEMM_PAIR_MMA, moe.MOE_GEMM_QUAD)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])

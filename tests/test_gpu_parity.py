@@ -120,11 +120,11 @@ def test_bf16_e1_k1_is_plain_swiglu(moe):
     assert parity.rel_linf(_np(out.float()), want) <= 2e-2
 
 
-@pytest.mark.parametrize("T", [700, 2100])   # 128-row tiles (multicast pairs) and CTA-pair tiles
-def test_bf16_deterministic(moe, T):
+@pytest.mark.parametrize("T,form", [(700, 0), (2100, 0x8), (2100, 0x10)])  # default, CTA-pair, 2x2 forms
+def test_bf16_deterministic(moe, T, form):
     inp = _bf16_inputs(T, 512, 1024, 8, 2, seed=5)
-    a, ia, ga, pa, oa, sa = _run(moe, inp)
-    b, ib, gb, pb, ob, sb = _run(moe, inp)
+    a, ia, ga, pa, oa, sa = _run(moe, inp, flags=form)
+    b, ib, gb, pb, ob, sb = _run(moe, inp, flags=form)
     assert torch.equal(a, b) and torch.equal(ia, ib) and torch.equal(ga, gb) and torch.equal(pa, pb)
 
 
@@ -203,8 +203,8 @@ def test_block_stack_small(moe, dt, tol_key):
         print(f"layer {l}: rel err y {err_y:.2e}, residual {err_h:.2e}, {rep}")
 
 
-@pytest.mark.parametrize("T", [300, 2100])   # multicast-pair and CTA-pair GEMM forms
-def test_forced_timeout_is_reported_and_context_survives(moe, T):
+@pytest.mark.parametrize("T,form", [(300, 0), (2100, 0x8), (2100, 0x10)])  # all three GEMM forms
+def test_forced_timeout_is_reported_and_context_survives(moe, T, form):
     """The failure path of the bounded waits: with MOE_DEBUG_FORCE_TIMEOUT the
     gate/up GEMM waits on a barrier nothing signals; the wait expires, the
     call's status reads MOE_ERR_DEVICE_TIMEOUT, and the next call on the same
@@ -215,7 +215,7 @@ def test_forced_timeout_is_reported_and_context_survives(moe, T):
     g = inp.to(dev)
     ws = moe.Workspace(T, 512, 1024, 8, 2, torch.bfloat16, dev)
     t0 = time.time()
-    moe.moe_forward(g.x, g.Wg, g.W1, g.W3, g.W2, 2, workspace=ws, flags=moe.MOE_DEBUG_FORCE_TIMEOUT)
+    moe.moe_forward(g.x, g.Wg, g.W1, g.W3, g.W2, 2, workspace=ws, flags=moe.MOE_DEBUG_FORCE_TIMEOUT | form)
     assert moe.moe_read_status(ws) == 5          # MOE_ERR_DEVICE_TIMEOUT
     assert time.time() - t0 < 30.0
     y = moe.moe_forward(g.x, g.Wg, g.W1, g.W3, g.W2, 2, workspace=ws)
@@ -238,3 +238,22 @@ def test_host_pipeline_matches_device_calls(moe):
     for x, y in zip(xs, ys):
         want = moe.moe_forward(x.to(dev), inp.Wg, inp.W1, inp.W3, inp.W2, 2)
         assert torch.equal(y, want.cpu())
+
+
+@pytest.mark.parametrize("T,d,f,E,K", [
+    (2500, 520, 1032, 8, 2),    # odd n-tile counts in both GEMMs, ragged K
+    (700, 256, 384, 2, 1),      # odd m-tile counts (phantom / row-quad units), top-1
+    (1100, 512, 1024, 4, 2),
+    (3000, 256, 256, 8, 2),
+])
+def test_gemm_forms_agree_bit_for_bit(moe, T, d, f, E, K):
+    """The three expert-GEMM forms (multicast pairs, CTA-pair MMAs, 2x2
+    multicast tiles) compute every tile in the same order: identical bits,
+    and within the bar of the oracle."""
+    inp = _bf16_inputs(T, d, f, E, K, seed=40 + T)
+    outs = [_run(moe, inp, flags=fl)[0] for fl in (moe.MOE_GEMM_MULTICAST_PAIRS, moe.MOE_GEMM_PAIR_MMA,
+                                                    moe.MOE_GEMM_QUAD, 0)]
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+    ref = oracle.moe_layer(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K)
+    assert parity.rel_linf(_np(outs[0].float()), ref.y) <= parity.TOL["bf16"]
