@@ -77,10 +77,30 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *
   }
 }
 
-// Maximum of v over the block (blockDim.x a multiple of 32, at most 1024).
-__device__ __forceinline__ float block_max(float v, float *red) {
+// Rows are processed by teams: one warp per row when there are many rows,
+// the whole block per row when there are few (decode), so that either way
+// the row's loads spread over many threads.
+template <bool BLOCK_TEAM>
+struct Team {
+  int rank, size, first, stride;  // thread's rank in the team, team size, first row, row stride
+  __device__ Team() {
+    if (BLOCK_TEAM) {
+      rank = threadIdx.x; size = blockDim.x; first = blockIdx.x; stride = gridDim.x;
+    } else {
+      rank = threadIdx.x & 31; size = 32;
+      first = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+      stride = (gridDim.x * blockDim.x) >> 5;
+    }
+  }
+};
+
+// Maximum of v over the team (a warp, or the block: blockDim.x a multiple of
+// 32, at most 256).
+template <bool BLOCK_TEAM>
+__device__ __forceinline__ float team_max(float v, float *red) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if (!BLOCK_TEAM) return v;
   const int w = threadIdx.x >> 5, nw = blockDim.x >> 5;
   __syncthreads();  // red is free (an earlier row's readers are done)
   if ((threadIdx.x & 31) == 0) red[w] = v;
@@ -115,8 +135,8 @@ __device__ __forceinline__ float absmax8(uint4 u) {
 }
 
 // X_perm8[r, :] = e4m3(x[perm_tok[r], :] / xs[r]) with xs[r] the row's scale;
-// pad rows are zero with scale 0.  One block per grouped row (grid-stride),
-// so that a handful of rows (decode) still spreads over many threads.
+// pad rows are zero with scale 0.  One team per grouped row (grid-stride).
+template <bool BLOCK_TEAM>
 __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *__restrict__ x, int T, int d,
                                                            const int32_t *__restrict__ perm_tok,
                                                            const int32_t *__restrict__ poffsets, int E,
@@ -125,35 +145,36 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
   __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
+  const Team<BLOCK_TEAM> tm;
   const int rows = poffsets[E];
   const int nchunk = d / 8;  // 8 bf16 in, 8 codes out
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+  for (int r = tm.first; r < rows; r += tm.stride) {
     int tok = perm_tok[r];
     if (tok >= T) {
-      if (threadIdx.x == 0) atomicCAS(status, 0, MOE_ERR_DEVICE_BOUNDS);
+      if (tm.rank == 0) atomicCAS(status, 0, MOE_ERR_DEVICE_BOUNDS);
       tok = -1;
     }
     uint8_t *dst = xq + static_cast<size_t>(r) * d;
     if (tok < 0) {
-      for (int c = threadIdx.x; c < nchunk; c += blockDim.x) *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(0, 0);
-      if (threadIdx.x == 0) xs[r] = 0.f;
+      for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = make_uint2(0, 0);
+      if (tm.rank == 0) xs[r] = 0.f;
       continue;
     }
     const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * d);
     float m = 0.f;
-    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) m = fmaxf(m, absmax8(__ldg(src + c)));
-    const float s = scale_of(block_max(m, red));
-    for (int c = threadIdx.x; c < nchunk; c += blockDim.x)
-      *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(__ldg(src + c), s);
-    if (threadIdx.x == 0) xs[r] = s;
+    for (int c = tm.rank; c < nchunk; c += tm.size) m = fmaxf(m, absmax8(__ldg(src + c)));
+    const float s = scale_of(team_max<BLOCK_TEAM>(m, red));
+    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(__ldg(src + c), s);
+    if (tm.rank == 0) xs[r] = s;
   }
 }
 
 // Hq[r, :] = e4m3(H[r, :] / hs[r]) for every real grouped row, with hs[r] =
 // max over the row's n-tiles of the tile maxima habs[r, :] written by the
-// gate/up epilogue (the maxima of the bf16 H values), / 448.  One block per
+// gate/up epilogue (the maxima of the bf16 H values), / 448.  One team per
 // row (grid-stride); padding rows are left alone (the down projection drops
 // their output).
+template <bool BLOCK_TEAM>
 __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__restrict__ H, int f,
                                                       const float *__restrict__ habs, int n_tiles,
                                                       const int32_t *__restrict__ offsets,
@@ -162,20 +183,21 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__res
   __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
+  const Team<BLOCK_TEAM> tm;
   const int rows = poffsets[E];
   const int nchunk = f / 8;
-  for (int r = blockIdx.x; r < rows; r += gridDim.x) {
+  for (int r = tm.first; r < rows; r += tm.stride) {
     int e = 0;
     while (e < E - 1 && r >= poffsets[e + 1]) ++e;
-    if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row (uniform over the block)
+    if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row (uniform over the team)
     float m = 0.f;
-    for (int t = threadIdx.x; t < n_tiles; t += blockDim.x) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
-    const float s = scale_of(block_max(m, red));
+    for (int t = tm.rank; t < n_tiles; t += tm.size) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
+    const float s = scale_of(team_max<BLOCK_TEAM>(m, red));
     const uint4 *src = reinterpret_cast<const uint4 *>(H + static_cast<size_t>(r) * f);
     uint8_t *dst = hq + static_cast<size_t>(r) * f;
 #pragma unroll 4
-    for (int c = threadIdx.x; c < nchunk; c += blockDim.x) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], s);
-    if (threadIdx.x == 0) hs[r] = s;
+    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], s);
+    if (tm.rank == 0) hs[r] = s;
   }
 }
 
@@ -195,20 +217,24 @@ cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void
 
 cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const Ptrs &P, int num_sms,
                                 cudaStream_t s) {
-  int blocks = R;  // one block per grouped row
+  // a block per row while the rows fit in one wave of blocks, else a warp per row
+  const bool block_team = R <= num_sms * 8;
+  int blocks = block_team ? R : (R + 7) / 8;
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
-  return launch_kernel(gather_quant_kernel, dim3(blocks), dim3(256), 0, s, true,
+  return launch_kernel(block_team ? gather_quant_kernel<true> : gather_quant_kernel<false>, dim3(blocks), dim3(256),
+                       0, s, true,
                        static_cast<const __nv_bfloat16 *>(x), T, d, static_cast<const int32_t *>(P.perm_tok),
                        static_cast<const int32_t *>(P.poffsets), E, static_cast<uint8_t *>(P.xperm), P.xscale,
                        P.status);
 }
 
 cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
-  int blocks = R;  // one block per grouped row
+  const bool block_team = R <= num_sms * 8;
+  int blocks = block_team ? R : (R + 7) / 8;
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
-  return launch_kernel(quant_h_kernel, dim3(blocks), dim3(256), 0, s, true,
+  return launch_kernel(block_team ? quant_h_kernel<true> : quant_h_kernel<false>, dim3(blocks), dim3(256), 0, s, true,
                        static_cast<const __nv_bfloat16 *>(P.hbuf), f, static_cast<const float *>(P.habs), n_tiles,
                        static_cast<const int32_t *>(P.offsets), static_cast<const int32_t *>(P.poffsets), E,
                        static_cast<uint8_t *>(P.hq), P.hscale);

@@ -57,6 +57,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "tc_common.cuh"
 
 namespace moe {
 namespace {
@@ -94,7 +95,6 @@ struct FormInfo {
   static constexpr int CL = QUAD ? 4 : 2;           // CTAs per cluster
   static constexpr uint16_t ALL = QUAD ? 0xF : 0x3;
 };
-constexpr uint64_t kTimeoutNs = 1000000000ull;
 
 enum { MODE_GATE_UP = 0, MODE_DOWN = 1 };
 
@@ -210,25 +210,6 @@ __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S,
     t.npair = true;
   }
   return t;
-}
-
-// Bounded mbarrier wait.  Returns false if the CTA is aborting (when
-// honor_abort) or the wait expired; expiry records MOE_ERR_DEVICE_TIMEOUT and
-// raises the CTA's abort flag.
-__device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, Ctrl &c, int *status, bool honor_abort) {
-  if (ptx::mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = ptx::globaltimer_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (ptx::mbar_try_wait(bar, parity)) return true;
-    if ((it & 15u) == 0) {
-      if (honor_abort && *reinterpret_cast<volatile int *>(&c.abort)) return false;
-      if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
-        *reinterpret_cast<volatile int *>(&c.abort) = 1;
-        atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT);
-        return false;
-      }
-    }
-  }
 }
 
 __device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
@@ -794,74 +775,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ---------------------------------------------------------------- host side
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-  static std::once_flag once;
-  std::call_once(once, [] {
-    void *p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-  });
-  return fn;
-}
-
-// 2-D bf16 row-major [rows, cols] matrix, box = 64 columns x box_rows rows, 128-byte swizzle.
-bool tmap_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D bf16 bank [E, rows, cols] (cols contiguous), box = 64 x 64 x 1, 128-byte swizzle.
-bool tmap_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, E};
-  cuuint64_t strides[2] = {cols * 2, cols * rows * 2};
-  cuuint32_t box[3] = {64, 64, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 2-D e4m3 matrix [rows, cols] (cols contiguous), box = 128 columns (128
-// bytes) x box_rows rows, 128-byte swizzle.
-bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[2] = {cols, rows};
-  cuuint64_t strides[1] = {cols};
-  cuuint32_t box[2] = {128, box_rows};
-  cuuint32_t estr[2] = {1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-// 3-D e4m3 bank [E, rows, cols] (cols = the contraction, contiguous), box =
-// 128 x 128 x 1, 128-byte swizzle.
-bool tmap_3d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, E};
-  cuuint64_t strides[2] = {cols, cols * rows};
-  cuuint32_t box[3] = {128, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Per device: shared-memory attribute set, and how many 2-CTA clusters of
 // this kernel can be resident at once (the persistent grid size).
 struct DevState {
