@@ -21,6 +21,7 @@ synthetic tokens, with random-init Mixtral-shaped weights resident in HBM.
 from __future__ import annotations
 
 import argparse
+import ctypes
 import hashlib
 import json
 import math
@@ -53,6 +54,8 @@ CONFIGS = {
     # profiling stand-in: two experts of Mixtral size with ~1024 rows each, the
     # per-expert GEMM shape of the prefill layer at a quarter of its memory
     "prefill_e2": dict(T=1024, d=4096, f=14336, E=2, K=2),
+    # training step of the prefill layer: forward keeping activations + backward
+    "train": dict(T=4096, d=4096, f=14336, E=8, K=2, train=True),
 }
 # the same workloads with e4m3 expert weights (quantised once, untimed)
 for _n in ("prefill", "decode1", "decode8", "decode32", "decode128", "skew"):
@@ -64,6 +67,9 @@ WORKLOAD_TEXT = {
 }
 WORKLOAD_TEXT["stack32"] = ("32-layer attention-free MoE stack h <- h + MoE_l(RMSNorm(h)): T=8192 tokens, "
                             "d=4096, f=14336, E=8, top-2, bf16, own seeded weights per layer (90.2 GB resident)")
+WORKLOAD_TEXT["train"] = ("Mixtral-shaped MoE layer training step (forward keeping activations, then backward to "
+                          "dx, dWg, dW1, dW3, dW2 in fp32): T=4096 tokens, d=4096, f=14336, E=8, top-2, bf16")
+TRAIN_METRIC = "MoE layer training tokens/s (forward + backward) and TFLOP/s on 1 B300"
 WORKLOAD_TEXT["prefill_e2"] = "profiling stand-in: T=1024 tokens, d=4096, f=14336, E=2 experts, top-2, bf16"
 for _t in (1, 8, 32, 128):
     WORKLOAD_TEXT[f"decode{_t}"] = f"Mixtral-shaped MoE layer decode batch: T={_t} tokens, d=4096, f=14336, " \
@@ -319,7 +325,7 @@ def make_inputs(cfg_name: str, rank: int, dev, weights=None):
     seed = W.BASE_SEED + 1009 * rank     # replicas: own tokens per rank (same model weights)
     if weights is None:
         weights = W.mixtral_weights(c["d"], c["f"], c["E"], seed=W.BASE_SEED, device=dev)
-    if cfg_name in ("prefill", "prefill_e2"):
+    if cfg_name in ("prefill", "prefill_e2", "train"):
         return W.prefill(T=c["T"], seed=seed, device=dev, weights=weights), weights
     if cfg_name.startswith("decode"):
         return W.decode(c["T"], seed=seed, device=dev, weights=weights), weights
@@ -412,7 +418,7 @@ def run_reference_stack(args, world, c, dev, steps, warmup):
     value = n_tok / (ms / 1e3)
     sample = (f"{n_tok} tokens per step through layer 0's pre-norm block, time scaled by {L} layers "
               f"(weights upcast to float64 once, untimed)")
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": TRAIN_METRIC if train else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.config], **c},
@@ -440,11 +446,17 @@ def run_reference(args, world, rank):
     x = inp.x.float().cpu().numpy().astype(np.float64)
     Wg, W1, W3, W2 = f64_banks(inp)
     del inp
+    train = bool(c.get("train"))
+    if train:
+        n_tok = max(1, n_tok // 3)  # the backward costs about twice the forward
+        dy = W.randn((c["T"], c["d"]), 1.0, W.BASE_SEED + 77, "cpu").numpy().astype(np.float64)
     times = []
     for i in range(warmup + steps):
         lo = (i * n_tok) % max(1, c["T"] - n_tok + 1)
         t0 = time.perf_counter()
         oracle.moe_layer(x[lo:lo + n_tok], Wg, W1, W3, W2, c["K"])
+        if train:
+            oracle.moe_layer_backward(x[lo:lo + n_tok], Wg, W1, W3, W2, c["K"], dy[lo:lo + n_tok])
         dt = time.perf_counter() - t0
         if i >= warmup:
             times.append(dt)
@@ -452,7 +464,7 @@ def run_reference(args, world, rank):
     value = n_tok / (ms / 1e3)
     threads = blas_threads()
     sample = f"{n_tok} tokens of the {args.config} batch per step (weights upcast to float64 once, untimed)"
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    line = {"impl": "reference", "metric": TRAIN_METRIC if train else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.config], **c},
@@ -603,6 +615,146 @@ def run_ours_stack(args, world, rank, local):
 
 
 # ---------------------------------------------------------------------------
+BWD_STAGES = ("prep", "dgrad_h", "wgrad_w2", "dgrad_x", "wgrad_w13", "dx", "dwg")
+
+
+def run_ours_train(args, world, rank, local):
+    """Training step: moe_forward_train then moe_backward (fp32 gradients) on
+    the prefill batch with a fixed seeded output gradient."""
+    import sparse_mixture_experts_55_b300 as moe
+    from sparse_mixture_experts_55_b300 import build as _build
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    c = CONFIGS[args.config]
+    T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
+    inp, _ = make_inputs(args.config, rank, dev)
+    dy = W.randn((T, d), 1.0, W.BASE_SEED + 77 + 1009 * rank, dev, torch.bfloat16)
+    stream = torch.cuda.current_stream(dev)
+    steps, warmup = args.steps, max(args.warmup, 3)
+    ws = moe.TrainWorkspace(T, d, f, E, K, torch.bfloat16, dev)
+    y = torch.empty_like(inp.x)
+    z = dict(dtype=torch.float32, device=dev)
+    grads = moe.LayerGrads(torch.empty(T, d, **z), torch.empty(d, E, **z), torch.empty(E, d, f, **z),
+                           torch.empty(E, d, f, **z), torch.empty(E, f, d, **z))
+    lib = moe._lib.load()
+
+    def step(x, g_out, dyv):
+        moe.moe_forward_train(x, inp.Wg, inp.W1, inp.W3, inp.W2, K, ws, y=y, stream=stream)
+        moe.moe_backward(x, inp.Wg, inp.W1, inp.W3, inp.W2, dyv, K, ws, grads=g_out, stream=stream)
+
+    for _ in range(warmup):
+        step(inp.x, grads, dy)
+    torch.cuda.synchronize(dev)
+    if moe.moe_read_status(ws) != 0:
+        raise RuntimeError(f"device status {moe.moe_read_status(ws)}")
+    start, mid, end = (torch.cuda.Event(enable_timing=True) for _ in range(3))
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        start.record(stream)
+        for _ in range(steps):
+            step(inp.x, grads, dy)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world, dev)
+    if moe.moe_read_status(ws) != 0:
+        raise RuntimeError("device status set during timed run")
+
+    # per-stage durations: forward as one region, backward stages from the
+    # library's stage events (separate pass of the same steps)
+    nst = len(BWD_STAGES) + 1
+    fwd_ms, st_ms = [], {k: [] for k in BWD_STAGES}
+    for _ in range(steps):
+        evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst)]
+        mid.record(stream)
+        moe.moe_forward_train(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, ws, y=y, stream=stream)
+        for ev in evs:
+            ev.record(stream)  # create the handles; the library re-records them
+        arr = (ctypes.c_void_p * nst)(*[ev.cuda_event for ev in evs])
+        rc = lib.moe_backward_timed(*(ctypes.c_void_p(t.data_ptr()) for t in (inp.x, inp.Wg, inp.W1, inp.W3, inp.W2,
+                                                                              dy, *grads)),
+                                    T, d, f, E, K, moe.MOE_BF16, ctypes.c_void_p(ws.buf.data_ptr()), ws.nbytes, 0,
+                                    ctypes.c_void_p(stream.cuda_stream), arr)
+        moe._lib.check("moe_backward_timed", rc)
+        torch.cuda.synchronize(dev)
+        fwd_ms.append(mid.elapsed_time(evs[0]))
+        for j, k in enumerate(BWD_STAGES):
+            st_ms[k].append(evs[j].elapsed_time(evs[j + 1]))
+    stage_ms = {"forward_train": statistics.mean(fwd_ms), **{k: statistics.mean(v) for k, v in st_ms.items()}}
+
+    # end to end with host buffers: x and dy copied in from pinned memory,
+    # dx copied out, every step (the weight gradients stay on the device for
+    # the optimiser)
+    x_h, dy_h = inp.x.cpu().pin_memory(), dy.cpu().pin_memory()
+    dx_h = torch.empty(T, d, dtype=torch.float32).pin_memory()
+    xd, dyd = torch.empty_like(inp.x), torch.empty_like(dy)
+    e2e_steps = max(3, min(steps, 20))
+    for i in range(e2e_steps + 2):
+        if i == 2:
+            torch.cuda.synchronize(dev)
+            barrier(world)
+            t0 = time.perf_counter()
+        xd.copy_(x_h, non_blocking=True)
+        dyd.copy_(dy_h, non_blocking=True)
+        step(xd, grads, dyd)
+        dx_h.copy_(grads.dx, non_blocking=True)
+        torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, dev)
+
+    peaks, peak_src = load_peaks()
+    unit = 2.0 * T * K * d * f  # one expert-GEMM pass over the routed rows
+    flops = 9 * unit + 3 * 2.0 * T * d * E  # 3 forward + 6 backward products; router fwd, dx, dWg
+    prods = {"dgrad_h": unit, "wgrad_w2": unit, "dgrad_x": 2 * unit, "wgrad_w13": 2 * unit}
+    top = max(prods, key=lambda k: stage_ms[k])  # the longest product
+    achieved = prods[top] / (stage_ms[top] / 1e3) / 1e12
+    tensor_peak = peaks["bf16_tflops_sustained"]
+    roof = {"kernel": f"bwd_gemm_kernel ({top})", "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
+            "unit": "TFLOP/s", "frac": achieved / tensor_peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
+            "traffic": traffic_from_profiles(ROOT / "sparse_mixture_experts_55_b300" / "csrc" / "gemm_bwd.cu",
+                                             f"train_{top}_traffic_bytes_per_launch"),
+            "algorithmic_flops_per_launch": prods[top],
+            "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peak_src}; kernel timed inside a long run "
+                           f"of steps)"}
+    line = {
+        "metric": TRAIN_METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16 (fp32 accumulate, fp32 gradients)",
+        "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens, N(0,1) dy",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "inputs larger than L2: 2.82 GB of expert weights and 5.6 GB of fp32 weight gradients "
+                         "per step"},
+        "tflops": flops / (ms / 1e3) / 1e12 * world,
+        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
+        "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "roofline": roof,
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
+                "d2h_bytes_per_step": dx_h.numel() * dx_h.element_size()},
+        "gpu_launches": 14 * steps,
+        "stage_timing": "separate pass of the same steps with library-recorded backward stage events",
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        n_tok = max(1, min(T, args.cpu_tokens // 4))
+        x64 = inp.x[:n_tok].float().cpu().numpy().astype(np.float64)
+        dy64 = dy[:n_tok].float().cpu().numpy().astype(np.float64)
+        Wg64, W164, W364, W264 = f64_banks(inp)
+        t0 = time.perf_counter()
+        oracle.moe_layer(x64, Wg64, W164, W364, W264, K)
+        oracle.moe_layer_backward(x64, Wg64, W164, W364, W264, K, dy64)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"first {n_tok} tokens, float64 oracle forward + backward ({dt:.1f} s; "
+                                          f"weights upcast once, untimed)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def run_ours(args, world, rank, local):
     import sparse_mixture_experts_55_b300 as moe
     from sparse_mixture_experts_55_b300 import build as _build
@@ -773,6 +925,8 @@ def main():
             run_reference(args, world, rank)
         elif args.config == "stack32":
             run_ours_stack(args, world, rank, local)
+        elif CONFIGS[args.config].get("train"):
+            run_ours_train(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

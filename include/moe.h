@@ -219,6 +219,68 @@ MOE_API int moe_forward_fp8_timed(const void *x, const void *Wg, const void *W1q
                           void *const *events);
 
 /*
+ * Training: a forward pass that keeps what the backward pass needs, and the
+ * backward pass (gradients by the chain rule through y = sum over the K kept
+ * experts of G_i E_i(x): the SwiGLU experts, the softmax over the kept
+ * logits and the router x Wg; section 3.4 "MoE Layer Formulation" and
+ * "Expert Network Structure (SwiGLU)").  The selected set is held fixed: it
+ * has no gradient, so gradients reach only the K selected experts of each
+ * token and their K logits.
+ *
+ * Supported: dtype MOE_BF16 with d and f multiples of 64 (others return
+ * MOE_ERR_UNSUPPORTED); other limits as moe_forward.
+ *
+ * moe_train_workspace_bytes: workspace size for both calls (0 if invalid or
+ *   unsupported).  Besides the forward's buffers it holds the saved
+ *   pre-activations a = x W1, b = x W3 of every grouped row (bf16 [R, 2f])
+ *   and the backward's buffers: at T = 4096, d = 4096, f = 14336, E = 8,
+ *   K = 2 it is about 1.7 GB.
+ *
+ * moe_forward_train: moe_forward (same arguments, flags and outputs; the
+ *   gate/up contraction is never split) that also leaves in the workspace
+ *   the routing, the grouped x, H and the pre-activations.
+ *
+ * moe_backward: given dy = dL/dy [T, d] (dtype), computes
+ *   dx  [T, d]     fp32  dL/dx
+ *   dWg [d, E]     fp32  dL/dWg
+ *   dW1 [E, d, f]  fp32, dW3 [E, d, f] fp32, dW2 [E, f, d] fp32
+ *   from the state the last moe_forward_train on this workspace left (same
+ *   x, weights and sizes, ordered before this call; no other call on the
+ *   workspace in between -- otherwise the results are unspecified).  x and
+ *   the weights are the forward's.  With MOE_ACCUMULATE every gradient is
+ *   added to its output buffer instead of overwriting it (an expert that
+ *   received no token then leaves its gradients untouched; without the flag
+ *   they are written as zeros).  T = 0 writes zero weight gradients (none
+ *   with MOE_ACCUMULATE); x, dy and dx may then be NULL.  The outputs must
+ *   not overlap one another.  Device-side errors are recorded in the
+ *   workspace status word (moe_read_status); the backward does not clear it.
+ *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS.
+ */
+MOE_API size_t moe_train_workspace_bytes(int T, int d, int f, int E, int K, int dtype);
+MOE_API int moe_forward_train(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+                void *y, int T, int d, int f, int E, int K, int dtype,
+                void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+MOE_API int moe_backward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+                const void *dy, float *dx, float *dWg, float *dW1, float *dW3, float *dW2,
+                int T, int d, int f, int E, int K, int dtype,
+                void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
+ * moe_backward recording MOE_NUM_BWD_STAGE_EVENTS cudaEvent_t handles on the
+ * stream (for per-stage timing; otherwise identical): before the prep kernel
+ * (dL/dlogits and gate * dy per grouped row), after it, after each grouped
+ * product (dH with the SwiGLU backward, dW2, dX, dW1 | dW3), after dx and
+ * after dWg.  Returns MOE_ERR_INVALID_ARG if events or one of its entries is
+ * NULL.
+ */
+#define MOE_NUM_BWD_STAGE_EVENTS 8
+MOE_API int moe_backward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+                const void *dy, float *dx, float *dWg, float *dW1, float *dW3, float *dW2,
+                int T, int d, int f, int E, int K, int dtype,
+                void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                void *const *events);
+
+/*
  * Routing only, for inspection: the router and grouping kernels that
  * moe_forward runs, with their results copied out in unpadded form
  * (section 3.4 gating function; "Top-K Gating Mechanism and Routing").

@@ -23,7 +23,8 @@ from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_T
                    status_string)
 
 __all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "quantize_weights_fp8",
-           "moe_forward_fp8", "moe_forward_fp8_timed", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+           "moe_forward_fp8", "moe_forward_fp8_timed", "TrainWorkspace", "moe_forward_train", "moe_backward",
+           "LayerGrads", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
 
@@ -236,6 +237,83 @@ def moe_forward_fp8_timed(x, Wg, W1q, s1, W3q, s3, W2q, s2, K: int, events, y=No
                                            flags, ctypes.c_void_p(s.cuda_stream), arr)
     _lib.check("moe_forward_fp8_timed", rc)
     return y
+
+
+class TrainWorkspace(Workspace):
+    """A workspace sized by moe_train_workspace_bytes: the forward's buffers
+    plus what moe_forward_train keeps for moe_backward (bf16 only)."""
+
+    def __init__(self, T, d, f, E, K, dtype=torch.bfloat16, device=None):
+        self.nbytes = _lib.load().moe_train_workspace_bytes(T, d, f, E, K, _DTYPES.get(dtype, -1))
+        if self.nbytes == 0:
+            raise ValueError(f"unsupported training sizes T={T} d={d} f={f} E={E} K={K} dtype={dtype} "
+                             "(bf16, d and f multiples of 64)")
+        self.buf = torch.empty(self.nbytes, dtype=torch.uint8, device=device or "cuda")
+        self.key = (T, d, f, E, K, dtype)
+
+
+def _layer_args(x, Wg, W1, W3, W2):
+    dev, dt = x.device, x.dtype
+    for t, n in ((x, "x"), (Wg, "Wg"), (W1, "W1"), (W3, "W3"), (W2, "W2")):
+        _need(t, n, dt, dev)
+    T, d = x.shape
+    E, d1, f = W1.shape
+    if Wg.shape != (d, E) or W3.shape != (E, d, f) or W2.shape != (E, f, d) or d1 != d:
+        raise ValueError("shape mismatch: x [T,d], Wg [d,E], W1/W3 [E,d,f], W2 [E,f,d]")
+    return T, d, f, E
+
+
+def moe_forward_train(x, Wg, W1, W3, W2, K: int, workspace: TrainWorkspace, y=None, flags: int = 0, stream=None):
+    """moe_forward that keeps in ``workspace`` what moe_backward needs; returns y."""
+    T, d, f, E = _layer_args(x, Wg, W1, W3, W2)
+    if y is None:
+        y = torch.empty_like(x)
+    else:
+        _need(y, "y", x.dtype, x.device)
+    rc = _lib.load().moe_forward_train(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(y), T, d, f, E, K,
+                                       _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
+                                       _stream_ptr(stream, x.device))
+    _lib.check("moe_forward_train", rc)
+    return y
+
+
+class LayerGrads(tuple):
+    """(dx, dWg, dW1, dW3, dW2), fp32."""
+    __slots__ = ()
+
+    def __new__(cls, dx, dWg, dW1, dW3, dW2):
+        return super().__new__(cls, (dx, dWg, dW1, dW3, dW2))
+
+    dx = property(lambda s: s[0])
+    dWg = property(lambda s: s[1])
+    dW1 = property(lambda s: s[2])
+    dW3 = property(lambda s: s[3])
+    dW2 = property(lambda s: s[4])
+
+
+def moe_backward(x, Wg, W1, W3, W2, dy, K: int, workspace: TrainWorkspace, grads: LayerGrads | None = None,
+                 flags: int = 0, stream=None) -> LayerGrads:
+    """Gradients of the layer (fp32) from the state the last moe_forward_train
+    on ``workspace`` left; ``grads`` are written (or, with MOE_ACCUMULATE,
+    added to) in place if given."""
+    T, d, f, E = _layer_args(x, Wg, W1, W3, W2)
+    _need(dy, "dy", x.dtype, x.device)
+    if dy.shape != x.shape:
+        raise ValueError("dy must have the shape of x")
+    if grads is None:
+        z = dict(dtype=torch.float32, device=x.device)
+        grads = LayerGrads(torch.empty(T, d, **z), torch.empty(d, E, **z), torch.empty(E, d, f, **z),
+                           torch.empty(E, d, f, **z), torch.empty(E, f, d, **z))
+    shapes = ((T, d), (d, E), (E, d, f), (E, d, f), (E, f, d))
+    for g, shp, n in zip(grads, shapes, ("dx", "dWg", "dW1", "dW3", "dW2")):
+        _need(g, n, torch.float32, x.device)
+        if tuple(g.shape) != shp:
+            raise ValueError(f"{n} must have shape {shp}")
+    rc = _lib.load().moe_backward(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(dy), *map(_ptr, grads),
+                                  T, d, f, E, K, _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
+                                  _stream_ptr(stream, x.device))
+    _lib.check("moe_backward", rc)
+    return grads
 
 
 class HostPipeline:

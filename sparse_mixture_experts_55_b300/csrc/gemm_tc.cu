@@ -122,6 +122,10 @@ struct GemmArgs {
   const float *col_scale0;
   const float *col_scale1;
   float *habs;
+  // training forward (bf16 gate/up without splits): also store the
+  // pre-activations a = X W1 and b = X W3 as bf16 [R, 2 n_out] (a in columns
+  // [0, n_out), b after), for every row of the segments including padding
+  __nv_bfloat16 *save_ab;
   int *status;
 };
 
@@ -487,7 +491,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int ru = c.uoff[t.e] + seg_row;  // unpadded grouped row (valid if real)
       // A warp whose 32 rows are all padding has nothing anyone reads (the down
       // projection drops padding rows), so it skips its quarter entirely.
-      const bool warp_real = __ballot_sync(0xffffffffu, real) != 0;
+      // (The training forward keeps every row: the weight gradients contract
+      // over whole segments, so padding rows of H and of a, b must be zeros.)
+      const bool warp_real = __ballot_sync(0xffffffffu, real) != 0 || (!FP8 && args.save_ab != nullptr);
       const uint32_t tbase = tmem + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
       if (MODE == MODE_GATE_UP) {
         const int n0 = t.nt * (BN / 2);
@@ -523,6 +529,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                   }
                 }
               }
+              const int col = n0 + cc * 32;
+              if (!FP8 && args.save_ab != nullptr && in_seg) {
+                __nv_bfloat16 *pa = args.save_ab + static_cast<size_t>(row) * 2 * args.n_out + col;
+                __nv_bfloat16 *pb = pa + args.n_out;
+#pragma unroll
+                for (int vv = 0; vv < 4; ++vv)
+                  if (col + vv * 8 < args.n_out) {
+                    uint32_t wa[4], wb[4];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                      const int c2 = 8 * vv + 2 * j;
+                      __nv_bfloat162 ha = __floats2bfloat162_rn(__uint_as_float(g[c2]), __uint_as_float(g[c2 + 1]));
+                      __nv_bfloat162 hb2 = __floats2bfloat162_rn(__uint_as_float(v[c2]), __uint_as_float(v[c2 + 1]));
+                      wa[j] = *reinterpret_cast<uint32_t *>(&ha);
+                      wb[j] = *reinterpret_cast<uint32_t *>(&hb2);
+                    }
+                    *reinterpret_cast<uint4 *>(pa + vv * 8) = make_uint4(wa[0], wa[1], wa[2], wa[3]);
+                    *reinterpret_cast<uint4 *>(pb + vv * 8) = make_uint4(wb[0], wb[1], wb[2], wb[3]);
+                  }
+              }
               uint32_t packed[16];
 #pragma unroll
               for (int j = 0; j < 16; ++j) {
@@ -535,7 +561,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 packed[j] = *reinterpret_cast<uint32_t *>(&hb);
               }
-              const int col = n0 + cc * 32;
               __nv_bfloat16 *dst = H + static_cast<size_t>(row) * args.n_out + col;
               if (in_seg) {
 #pragma unroll
@@ -921,6 +946,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.splits = L.S_gu;
   g1.kb_per_split = L.kb_per_split_gu;
   g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
+  g1.save_ab = static_cast<__nv_bfloat16 *>(P.ab);  // training forward only (then splits == 1)
   g1.status = P.status;
   err = launch_form<MODE_GATE_UP, false>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
@@ -932,6 +958,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.part = nullptr;
   g2.tile_cnt = nullptr;
   g2.force_timeout = 0;
+  g2.save_ab = nullptr;
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + BK - 1) / BK;

@@ -49,6 +49,8 @@ struct WsLayout {
   size_t status, tile_cnt, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf, obuf,
       gu_part, xnorm;
   size_t xscale, habs, hq, hscale;  // e4m3 variant only (0 bytes otherwise)
+  size_t ab, dye, dab, dxc, dl, dwg_part;  // training only (0 bytes otherwise)
+  int dwg_chunks;     // token chunks of the router-weight gradient's partial sums
   size_t total;
   size_t zero_bytes;  // bytes from `status` that every call clears (status word + split counters)
   int TK;             // T*K: rows of the compact grouped buffers
@@ -58,6 +60,7 @@ struct WsLayout {
   int S_gu;           // split count over the contraction of the gate/up projection
   int kb_per_split_gu;
   int form;           // expert GEMM form: 0 multicast pairs, 1 CTA-pair MMA, 2 2x2 multicast tiles
+  bool train;         // training layout (bf16): saved pre-activations and backward buffers
   int route_tpb;      // tokens per router block
   int n_route_blocks;
 };
@@ -74,7 +77,9 @@ struct SplitPlan {
 // (part_ratio = partial bytes per split / weight bytes).  S = 1 unless a
 // split shortens the modelled time by at least 3%.
 SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, double part_ratio);
-WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms);
+// train: also lay out the saved pre-activations and the backward buffers
+// (and keep the gate/up contraction unsplit, which the saving epilogue needs).
+WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bool train = false);
 
 struct Ptrs {
   int *status;
@@ -93,6 +98,13 @@ struct Ptrs {
   float *habs;    // [R, gate/up n-tiles] max |bf16 H| per row and tile
   void *hq;       // [R, f] e4m3 codes of H
   float *hscale;  // [R] scale of each H row
+  // training (bf16): saved by the forward, then the backward's buffers
+  void *ab;         // [R, 2f] bf16 pre-activations a = X W1 | b = X W3
+  void *dye;        // [R, d] bf16 gate * dy per grouped row (padding rows zero)
+  void *dab;        // [R, 2f] bf16 dL/da | dL/db
+  float *dxc;       // [T*K, d] dL/dX per unpadded grouped row
+  float *dl;        // [T, E] dL/dlogits
+  float *dwg_part;  // [dwg_chunks, d, E] partial sums of dL/dWg
 };
 Ptrs carve(void *ws, const WsLayout &L);
 
@@ -126,6 +138,17 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
                                     void *const *mid_event);
 
 // -------- gemm_simt.cu (exact fp32 path)
+// -------- backward.cu / gemm_bwd.cu (bf16, d and f multiples of 64)
+cudaError_t launch_bwd_prep(const void *dy, int T, int d, int E, int K, int S, const WsLayout &L, const Ptrs &P,
+                            int num_sms, cudaStream_t s);
+// events (optional): recorded after each of the four products / after dx and after dWg
+cudaError_t launch_bwd_gemms(const void *W1, const void *W3, const void *W2, void *dW1, void *dW3, void *dW2, int d,
+                             int f, int E, bool accumulate, const WsLayout &L, const Ptrs &P, int num_sms,
+                             cudaStream_t s, void *const *events);
+cudaError_t launch_bwd_input(const void *x, const void *Wg, void *dx, void *dWg, int T, int d, int E, int K,
+                             bool accumulate, const WsLayout &L, const Ptrs &P, int num_sms, cudaStream_t s,
+                             void *const *events);
+
 cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                   const WsLayout &L, const Ptrs &P, cudaStream_t s, void *const *mid_event);
 

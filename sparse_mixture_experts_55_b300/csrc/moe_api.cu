@@ -130,8 +130,9 @@ SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, do
   return best;
 }
 
-WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
+WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bool train) {
   WsLayout L{};
+  L.train = train;
   const size_t eb = elem_bytes(dtype);
   L.R = static_cast<int>(align_up(static_cast<size_t>(T) * K + static_cast<size_t>(E) * (kSegPad - 1), kSegPad));
   {
@@ -157,7 +158,7 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
     // epilogue warp, whose latency grows with the real rows it owns; beyond
     // about four rows per expert it stalls the MMA pipeline more than the
     // balanced split saves, so larger batches keep one split.
-    if (TKl <= 4 * touched)
+    if (TKl <= 4 * touched && !train)  // the training forward saves a, b from the unsplit epilogue
       gu = plan_splits(TKl, E, (f + 127) / 128, (d + kbw - 1) / kbw, clusters,
                        8.0 / wb * static_cast<double>(TKl) / (static_cast<double>(touched) * d));
   }
@@ -202,6 +203,23 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms) {
   L.habs = take(fp8 ? R * nt_gu * 4 : 0);
   L.hq = take(fp8 ? R * f : 0);
   L.hscale = take(fp8 ? R * 4 : 0);
+  // training: saved pre-activations, then the backward's buffers; the router
+  // weight gradient is summed over token chunks (about four blocks per SM)
+  const size_t tr = train ? 1 : 0;
+  L.dwg_chunks = 1;
+  if (train) {
+    const int col_blocks = (d / 2 + 127) / 128;
+    int ch = (4 * num_sms + col_blocks - 1) / col_blocks;
+    const int max_ch = (T + 63) / 64;
+    if (ch > max_ch) ch = max_ch;
+    L.dwg_chunks = ch > 0 ? ch : 1;
+  }
+  L.ab = take(tr * R * 2 * f * 2);
+  L.dye = take(tr * R * d * 2);
+  L.dab = take(tr * R * 2 * f * 2);
+  L.dxc = take(tr * TK * d * 4);
+  L.dl = take(tr * static_cast<size_t>(T) * E * 4);
+  L.dwg_part = take(tr * static_cast<size_t>(L.dwg_chunks) * d * E * 4);
   L.total = o;
   return L;
 }
@@ -228,6 +246,12 @@ Ptrs carve(void *ws, const WsLayout &L) {
   P.habs = reinterpret_cast<float *>(b + L.habs);
   P.hq = b + L.hq;
   P.hscale = reinterpret_cast<float *>(b + L.hscale);
+  P.ab = L.train ? b + L.ab : nullptr;  // non-null switches the gate/up epilogue to saving
+  P.dye = L.train ? b + L.dye : nullptr;
+  P.dab = L.train ? b + L.dab : nullptr;
+  P.dxc = L.train ? reinterpret_cast<float *>(b + L.dxc) : nullptr;
+  P.dl = L.train ? reinterpret_cast<float *>(b + L.dl) : nullptr;
+  P.dwg_part = L.train ? reinterpret_cast<float *>(b + L.dwg_part) : nullptr;
   return P;
 }
 
@@ -242,11 +266,21 @@ size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
   return ws_layout(T, d, f, E, K, dtype, sm_count_or_default()).total;
 }
 
+// The training path (moe_forward_train / moe_backward) covers the bf16 layer
+// with d and f multiples of 64 (whole k-blocks in every backward product).
+static int check_train_shape(int T, int d, int f, int E, int K, int dtype) {
+  const int st = check_shape(T, d, f, E, K, dtype);
+  if (st != MOE_OK) return st;
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  if (d % 64 != 0 || f % 64 != 0) return MOE_ERR_UNSUPPORTED;
+  return MOE_OK;
+}
+
 static int forward_impl(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
                         int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
-                        unsigned flags, moe_stream_t stream, void *const *events) {
+                        unsigned flags, moe_stream_t stream, void *const *events, bool train = false) {
   if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;  // e4m3 weights go through moe_forward_fp8
-  int st = check_shape(T, d, f, E, K, dtype);
+  int st = train ? check_train_shape(T, d, f, E, K, dtype) : check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
   if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT | kFormFlags)) return MOE_ERR_INVALID_ARG;
   if (!form_flags_ok(flags)) return MOE_ERR_INVALID_ARG;
@@ -259,7 +293,7 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   if (T > 0 && overlaps(x, act_bytes, y, act_bytes)) return MOE_ERR_INVALID_ARG;
   if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
   const int sms = sm_count_or_default();
-  WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
+  WsLayout L = ws_layout(T, d, f, E, K, dtype, sms, train);
   if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
   apply_form_flags(L, flags);
   st = check_device();
@@ -329,6 +363,84 @@ int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void 
   for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
     if (!events[i]) return MOE_ERR_INVALID_ARG;
   return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, events);
+}
+
+size_t moe_train_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
+  if (check_train_shape(T, d, f, E, K, dtype) != MOE_OK) return 0;
+  return ws_layout(T, d, f, E, K, dtype, sm_count_or_default(), true).total;
+}
+
+int moe_forward_train(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y, int T,
+                      int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes, unsigned flags,
+                      moe_stream_t stream) {
+  return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, nullptr, true);
+}
+
+static int backward_impl(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+                         const void *dy, float *dx, float *dWg, float *dW1, float *dW3, float *dW2, int T, int d,
+                         int f, int E, int K, int dtype, void *workspace, size_t ws_bytes, unsigned flags,
+                         moe_stream_t stream, void *const *events) {
+  int st = check_train_shape(T, d, f, E, K, dtype);
+  if (st != MOE_OK) return st;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS)) return MOE_ERR_INVALID_ARG;
+  const bool acc = (flags & MOE_ACCUMULATE) != 0;
+  if (!Wg || !W1 || !W3 || !W2 || !dWg || !dW1 || !dW3 || !dW2) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(Wg) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(dWg) || !aligned16(dW1) ||
+      !aligned16(dW3) || !aligned16(dW2))
+    return MOE_ERR_INVALID_ARG;
+  const size_t wbytes = static_cast<size_t>(E) * d * f * 4;
+  const float *outs[4] = {dWg, dW1, dW3, dW2};
+  const size_t out_bytes[4] = {static_cast<size_t>(d) * E * 4, wbytes, wbytes, wbytes};
+  for (int i = 0; i < 4; ++i)
+    for (int j = i + 1; j < 4; ++j)
+      if (overlaps(outs[i], out_bytes[i], outs[j], out_bytes[j])) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (T == 0) {
+    // no tokens: the weight gradients are zero
+    st = check_device();
+    if (st != MOE_OK || acc) return st;
+    for (int i = 0; i < 4; ++i)
+      if (cudaMemsetAsync(const_cast<float *>(outs[i]), 0, out_bytes[i], s) != cudaSuccess) return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (!x || !dy || !dx) return MOE_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(dx)) return MOE_ERR_INVALID_ARG;
+  const size_t dx_bytes = static_cast<size_t>(T) * d * 4;
+  for (int i = 0; i < 4; ++i)
+    if (overlaps(dx, dx_bytes, outs[i], out_bytes[i])) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  const int sms = sm_count_or_default();
+  const WsLayout L = ws_layout(T, d, f, E, K, dtype, sms, true);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  st = check_device();
+  if (st != MOE_OK) return st;
+  const Ptrs P = carve(workspace, L);
+  cudaError_t err = events ? cudaEventRecord(static_cast<cudaEvent_t>(events[0]), s) : cudaSuccess;
+  if (err == cudaSuccess) err = launch_bwd_prep(dy, T, d, E, K, L.S, L, P, sms, s);
+  if (err == cudaSuccess && events) err = cudaEventRecord(static_cast<cudaEvent_t>(events[1]), s);
+  if (err == cudaSuccess)
+    err = launch_bwd_gemms(W1, W3, W2, dW1, dW3, dW2, d, f, E, acc, L, P, sms, s, events ? events + 2 : nullptr);
+  if (err == cudaSuccess)
+    err = launch_bwd_input(x, Wg, dx, dWg, T, d, E, K, acc, L, P, sms, s, events ? events + 6 : nullptr);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int moe_backward(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, const void *dy,
+                 float *dx, float *dWg, float *dW1, float *dW3, float *dW2, int T, int d, int f, int E, int K,
+                 int dtype, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream) {
+  return backward_impl(x, Wg, W1, W3, W2, dy, dx, dWg, dW1, dW3, dW2, T, d, f, E, K, dtype, workspace, ws_bytes,
+                       flags, stream, nullptr);
+}
+
+int moe_backward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, const void *dy,
+                       float *dx, float *dWg, float *dW1, float *dW3, float *dW2, int T, int d, int f, int E, int K,
+                       int dtype, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                       void *const *events) {
+  if (!events) return MOE_ERR_INVALID_ARG;
+  for (int i = 0; i < MOE_NUM_BWD_STAGE_EVENTS; ++i)
+    if (!events[i]) return MOE_ERR_INVALID_ARG;
+  return backward_impl(x, Wg, W1, W3, W2, dy, dx, dWg, dW1, dW3, dW2, T, d, f, E, K, dtype, workspace, ws_bytes,
+                       flags, stream, events);
 }
 
 int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, moe_stream_t stream) {

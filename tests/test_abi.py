@@ -30,6 +30,7 @@ def test_header_declares_the_boundary():
     names = _header_functions()
     assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_block_forward", "moe_route",
                             "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_timed",
+                            "moe_train_workspace_bytes", "moe_forward_train", "moe_backward", "moe_backward_timed",
                             "moe_route_noalloc", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
@@ -175,3 +176,46 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
     # codes overlapping the bank
     assert lib.moe_quantize_weights_fp8(vp(0x1000), 1, 64, 64, vp(0x1000 + 64), vp(0x90000), vp(0)) == \
         _lib.MOE_ERR_INVALID_ARG
+
+
+def test_training_entry_points_reject_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    # sizes: bf16 with d and f multiples of 64 only
+    assert lib.moe_train_workspace_bytes(16, 128, 256, 8, 2, _lib.MOE_BF16) > lib.moe_workspace_bytes(
+        16, 128, 256, 8, 2, _lib.MOE_BF16)
+    assert lib.moe_train_workspace_bytes(16, 136, 256, 8, 2, _lib.MOE_BF16) == 0
+    assert lib.moe_train_workspace_bytes(16, 128, 264, 8, 2, _lib.MOE_BF16) == 0
+    assert lib.moe_train_workspace_bytes(16, 128, 256, 8, 2, _lib.MOE_F32) == 0
+    assert lib.moe_train_workspace_bytes(16, 128, 256, 8, 2, _lib.MOE_FP8_E4M3) == 0
+    assert lib.moe_train_workspace_bytes(0, 128, 256, 8, 2, _lib.MOE_BF16) > 0
+    # the training forward checks like moe_forward, plus the training sizes
+    args = [vp(0x1000), vp(0x2000), vp(0x3000), vp(0x4000), vp(0x5000), vp(0x100000), 16, 128, 256, 8, 2,
+            _lib.MOE_BF16, vp(0x200000), 1 << 40, 0, vp(0)]
+    bad = list(args); bad[8] = 264
+    assert lib.moe_forward_train(*bad) == _lib.MOE_ERR_UNSUPPORTED
+    bad = list(args); bad[11] = _lib.MOE_F32
+    assert lib.moe_forward_train(*bad) == _lib.MOE_ERR_UNSUPPORTED
+    bad = list(args); bad[0] = vp(0)
+    assert lib.moe_forward_train(*bad) == _lib.MOE_ERR_INVALID_ARG
+    bad = list(args); bad[13] = 64
+    assert lib.moe_forward_train(*bad) == _lib.MOE_ERR_WORKSPACE
+
+    E, d, f = 8, 128, 256
+    wb = E * d * f * 4
+
+    def bwd(T=16, dx=0x10_000000, dWg=0x20_000000, dW1=0x30_000000, dW3=0x40_000000, dW2=0x50_000000, x=0x1000,
+            dy=0x8000, ws=0x60_000000, ws_bytes=1 << 40, flags=0, dt=_lib.MOE_BF16, dd=d):
+        return lib.moe_backward(vp(x), vp(0x2000), vp(0x3000), vp(0x4000), vp(0x5000), vp(dy), vp(dx), vp(dWg),
+                                vp(dW1), vp(dW3), vp(dW2), T, dd, f, E, 2, dt, vp(ws), ws_bytes, flags, vp(0))
+
+    assert bwd(dt=_lib.MOE_F32) == _lib.MOE_ERR_UNSUPPORTED
+    assert bwd(dd=192 + 8) == _lib.MOE_ERR_UNSUPPORTED
+    assert bwd(flags=0x4) == _lib.MOE_ERR_INVALID_ARG       # no forced timeout on the backward
+    assert bwd(flags=0x8) == _lib.MOE_ERR_INVALID_ARG       # no GEMM form flags either
+    assert bwd(dW1=0) == _lib.MOE_ERR_INVALID_ARG
+    assert bwd(dx=0) == _lib.MOE_ERR_INVALID_ARG
+    assert bwd(dy=0x8008) == _lib.MOE_ERR_INVALID_ARG      # misaligned
+    assert bwd(dW3=0x30_000000 + wb // 2) == _lib.MOE_ERR_INVALID_ARG   # dW3 overlaps dW1
+    assert bwd(dx=0x50_000000 + 64) == _lib.MOE_ERR_INVALID_ARG        # dx overlaps dW2
+    assert bwd(ws=0) == _lib.MOE_ERR_WORKSPACE
+    assert bwd(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
