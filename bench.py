@@ -56,6 +56,8 @@ CONFIGS = {
     "prefill_e2": dict(T=1024, d=4096, f=14336, E=2, K=2),
     # training step of the prefill layer: forward keeping activations + backward
     "train": dict(T=4096, d=4096, f=14336, E=8, K=2, train=True),
+    # profiling stand-in of the training step: two Mixtral-sized experts with ~1024 rows each
+    "train_e2": dict(T=1024, d=4096, f=14336, E=2, K=2, train=True),
 }
 # the same workloads with e4m3 expert weights (quantised once, untimed)
 for _n in ("prefill", "decode1", "decode8", "decode32", "decode128", "skew"):
@@ -69,6 +71,8 @@ WORKLOAD_TEXT["stack32"] = ("32-layer attention-free MoE stack h <- h + MoE_l(RM
                             "d=4096, f=14336, E=8, top-2, bf16, own seeded weights per layer (90.2 GB resident)")
 WORKLOAD_TEXT["train"] = ("Mixtral-shaped MoE layer training step (forward keeping activations, then backward to "
                           "dx, dWg, dW1, dW3, dW2 in fp32): T=4096 tokens, d=4096, f=14336, E=8, top-2, bf16")
+WORKLOAD_TEXT["train_e2"] = ("profiling stand-in of the training step: T=1024 tokens, d=4096, f=14336, E=2 experts, "
+                             "top-2, bf16")
 TRAIN_METRIC = "MoE layer training tokens/s (forward + backward) and TFLOP/s on 1 B300"
 WORKLOAD_TEXT["prefill_e2"] = "profiling stand-in: T=1024 tokens, d=4096, f=14336, E=2 experts, top-2, bf16"
 for _t in (1, 8, 32, 128):
@@ -91,9 +95,10 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def traffic_from_profiles(kernel_file: pathlib.Path, key: str):
-    """dram bytes per launch recorded by an ncu capture, if the kernel source is unchanged since."""
-    prof = ROOT / "profiles" / "gate_up_gemm_traffic.md"
+def traffic_from_profiles(kernel_file: pathlib.Path, key: str, summary: str = "gate_up_gemm_traffic.md"):
+    """dram bytes per launch recorded by an ncu capture (profiles/<summary>), if
+    the kernel source is unchanged since."""
+    prof = ROOT / "profiles" / summary
     if not prof.exists():
         return None
     text = prof.read_text()
@@ -325,7 +330,7 @@ def make_inputs(cfg_name: str, rank: int, dev, weights=None):
     seed = W.BASE_SEED + 1009 * rank     # replicas: own tokens per rank (same model weights)
     if weights is None:
         weights = W.mixtral_weights(c["d"], c["f"], c["E"], seed=W.BASE_SEED, device=dev)
-    if cfg_name in ("prefill", "prefill_e2", "train"):
+    if cfg_name in ("prefill", "prefill_e2", "train", "train_e2"):
         return W.prefill(T=c["T"], seed=seed, device=dev, weights=weights), weights
     if cfg_name.startswith("decode"):
         return W.decode(c["T"], seed=seed, device=dev, weights=weights), weights
@@ -714,7 +719,7 @@ def run_ours_train(args, world, rank, local):
     roof = {"kernel": f"bwd_gemm_kernel ({top})", "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
             "unit": "TFLOP/s", "frac": achieved / tensor_peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
             "traffic": traffic_from_profiles(ROOT / "sparse_mixture_experts_55_b300" / "csrc" / "gemm_bwd.cu",
-                                             f"train_{top}_traffic_bytes_per_launch"),
+                                             f"{args.config}_{top}_traffic_bytes_per_launch", "bwd_gemm_traffic.md"),
             "algorithmic_flops_per_launch": prods[top],
             "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peak_src}; kernel timed inside a long run "
                            f"of steps)"}
@@ -724,8 +729,8 @@ def run_ours_train(args, world, rank, local):
         "vs_baseline": None, "dtype": "bf16 (fp32 accumulate, fp32 gradients)",
         "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens, N(0,1) dy",
         "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
-                   "l2": "inputs larger than L2: 2.82 GB of expert weights and 5.6 GB of fp32 weight gradients "
-                         "per step"},
+                   "l2": "inputs larger than L2: %.2f GB of expert weights and %.2f GB of fp32 weight gradients "
+                         "per step" % (3 * E * d * f * 2 / 1e9, 3 * E * d * f * 4 / 1e9)},
         "tflops": flops / (ms / 1e3) / 1e12 * world,
         "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},

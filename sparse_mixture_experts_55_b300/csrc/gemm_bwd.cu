@@ -55,7 +55,12 @@ constexpr int B_BYTES = BN * BK * 2;   // 32 KiB
 constexpr int BOX_BYTES = 64 * 64 * 2; // one MN-major 64 x 64 box
 constexpr int STAGES = 4;
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 1024 /*Ctrl*/;
+// Epilogue staging: one 32 x 33 fp32 tile per epilogue warp (the odd row
+// pitch keeps both the row-per-lane and the segment-per-lane accesses free of
+// bank conflicts).
+constexpr int STAGE_PITCH = 33;
+constexpr int EPI_WARP_BYTES = 32 * STAGE_PITCH * 4;
+constexpr int SMEM = 1024 /*alignment slack*/ + STAGES * STAGE_BYTES + 1024 /*Ctrl*/ + 4 * EPI_WARP_BYTES;
 static_assert(SMEM <= 232448, "shared memory budget");
 constexpr int ACC_COLS = BN;
 constexpr int TMEM_COLS = 2 * ACC_COLS;
@@ -129,6 +134,87 @@ __device__ __forceinline__ BTile decode_tile(int u, const Ctrl &c, const BwdArgs
 }
 
 __device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + __expf(-v)); }
+
+// The epilogue holds a 32 x 32 block as one row per lane (what tcgen05.ld
+// 32x32b returns); global memory wants each instruction to cover whole row
+// segments.  These helpers move the block through the warp's staging tile.
+//
+// Rows r < rows_valid of the block to fp32 rows at dst + r * ld (32 floats
+// each): every instruction writes four 128-byte row segments.  With
+// accumulate the old values are added.
+__device__ __forceinline__ void store_block_f32(float *st, const uint32_t (&v)[32], float *dst, size_t ld,
+                                                int rows_valid, bool accumulate, int lane) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) st[lane * STAGE_PITCH + c] = __uint_as_float(v[c]);
+  __syncwarp();
+  const int cq = 4 * (lane & 7);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const int r = 4 * k + (lane >> 3);
+    if (r < rows_valid) {
+      const float *sr = st + r * STAGE_PITCH + cq;
+      float4 val = make_float4(sr[0], sr[1], sr[2], sr[3]);
+      float4 *p = reinterpret_cast<float4 *>(dst + r * ld + cq);
+      if (accumulate) {
+        const float4 o = *p;
+        val.x += o.x; val.y += o.y; val.z += o.z; val.w += o.w;
+      }
+      *p = val;
+    }
+  }
+  __syncwarp();
+}
+
+// A bf16 block of 32 rows x 32 columns (src + r * ld) in segment layout:
+// lane l holds the 8 columns 8 (l & 3) .. +7 of rows 8 k + (l >> 2), k < 4, so
+// every load instruction reads eight 64-byte row segments.
+__device__ __forceinline__ void load_segments_bf16(const __nv_bfloat16 *src, size_t ld, uint4 (&w)[4], int lane) {
+#pragma unroll
+  for (int k = 0; k < 4; ++k) w[k] = *reinterpret_cast<const uint4 *>(src + (8 * k + (lane >> 2)) * ld + 8 * (lane & 3));
+}
+
+// The block loaded by load_segments_bf16 as fp32, one row per lane.
+__device__ __forceinline__ void segments_to_rows(float *st, const uint4 (&w)[4], float (&v)[32], int lane) {
+  const int cq = 8 * (lane & 3);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2);
+    const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ws[j]));
+      st[r * STAGE_PITCH + cq + 2 * j] = f2.x;
+      st[r * STAGE_PITCH + cq + 2 * j + 1] = f2.y;
+    }
+  }
+  __syncwarp();
+#pragma unroll
+  for (int c = 0; c < 32; ++c) v[c] = st[lane * STAGE_PITCH + c];
+  __syncwarp();
+}
+
+// v (one row per lane) to bf16 rows 0..31 at dst + r * ld, rounded to nearest
+// even: every instruction writes eight 64-byte row segments.
+__device__ __forceinline__ void store_block_bf16(float *st, const float (&v)[32], __nv_bfloat16 *dst, size_t ld,
+                                                 int lane) {
+#pragma unroll
+  for (int c = 0; c < 32; ++c) st[lane * STAGE_PITCH + c] = v[c];
+  __syncwarp();
+  const int cq = 8 * (lane & 3);
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const int r = 8 * k + (lane >> 2);
+    const float *sr = st + r * STAGE_PITCH + cq;
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(sr[2 * j], sr[2 * j + 1]);
+      w[j] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(dst + r * ld + cq) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+  __syncwarp();
+}
 
 template <int KIND>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -287,6 +373,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
+    float *stage_tile = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&c) + 1024 + q * EPI_WARP_BYTES);
     int local = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const BTile t = decode_tile<KIND>(u, c, args);
@@ -302,46 +389,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (KIND == KIND_DGRAD_H) {
         // every row of the segment, padding included (its dH is zero, and so
         // are its a and b: the weight gradients read these rows)
-        const int row = c.poff[t.e] + t.mt * BM + q * 32 + lane;
+        const int row0 = c.poff[t.e] + t.mt * BM + q * 32;  // the warp's first row
         const size_t rstride = 2 * static_cast<size_t>(args.f);
-        const __nv_bfloat16 *pa = args.ab + row * rstride;
-        __nv_bfloat16 *pd = args.dab + row * rstride;
+        const __nv_bfloat16 *pa = args.ab + row0 * rstride;
+        __nv_bfloat16 *pd = args.dab + row0 * rstride;
+        // a and b of the next chunk are in flight while this one is computed
+        uint4 wa[4], wb[4];
+        if (n0 < args.n_out) {
+          load_segments_bf16(pa + n0, rstride, wa, lane);
+          load_segments_bf16(pa + args.f + n0, rstride, wb, lane);
+        }
 #pragma unroll 1
         for (int cc = 0; cc < BN / 32; ++cc) {
           const int col = n0 + cc * 32;
           if (col >= args.n_out) break;  // f is a multiple of 64: a chunk is all in or all out
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
-          ptx::tmem_wait_ld();
-#pragma unroll
-          for (int g = 0; g < 4; ++g) {
-            const uint4 a8 = *reinterpret_cast<const uint4 *>(pa + col + 8 * g);
-            const uint4 b8 = *reinterpret_cast<const uint4 *>(pa + args.f + col + 8 * g);
-            const uint32_t aw[4] = {a8.x, a8.y, a8.z, a8.w}, bw[4] = {b8.x, b8.y, b8.z, b8.w};
-            uint32_t da[4], db[4];
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-              const float2 av = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&aw[j]));
-              const float2 bv = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&bw[j]));
-              const float dh0 = __uint_as_float(v[8 * g + 2 * j]), dh1 = __uint_as_float(v[8 * g + 2 * j + 1]);
-              const float s0 = sigmoid_f(av.x), s1 = sigmoid_f(av.y);
-              // SiLU(a) = a s, SiLU'(a) = s (1 + a (1 - s)), s = sigmoid(a)
-              const __nv_bfloat162 ga = __floats2bfloat162_rn(dh0 * bv.x * s0 * (1.f + av.x * (1.f - s0)),
-                                                              dh1 * bv.y * s1 * (1.f + av.y * (1.f - s1)));
-              const __nv_bfloat162 gb = __floats2bfloat162_rn(dh0 * av.x * s0, dh1 * av.y * s1);
-              da[j] = *reinterpret_cast<const uint32_t *>(&ga);
-              db[j] = *reinterpret_cast<const uint32_t *>(&gb);
-            }
-            *reinterpret_cast<uint4 *>(pd + col + 8 * g) = make_uint4(da[0], da[1], da[2], da[3]);
-            *reinterpret_cast<uint4 *>(pd + args.f + col + 8 * g) = make_uint4(db[0], db[1], db[2], db[3]);
+          float a[32], b[32];
+          segments_to_rows(stage_tile, wa, a, lane);
+          segments_to_rows(stage_tile, wb, b, lane);
+          if (cc + 1 < BN / 32 && col + 32 < args.n_out) {
+            load_segments_bf16(pa + col + 32, rstride, wa, lane);
+            load_segments_bf16(pa + args.f + col + 32, rstride, wb, lane);
           }
+          ptx::tmem_wait_ld();
+          // SiLU(a) = a s, SiLU'(a) = s (1 + a (1 - s)), s = sigmoid(a):
+          // da = dH b SiLU'(a) into a, db = dH SiLU(a) into b
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const float dh = __uint_as_float(v[j]);
+            const float sg = sigmoid_f(a[j]);
+            const float da = dh * b[j] * sg * (1.f + a[j] * (1.f - sg));
+            b[j] = dh * a[j] * sg;
+            a[j] = da;
+          }
+          store_block_bf16(stage_tile, a, pd + col, rstride, lane);
+          store_block_bf16(stage_tile, b, pd + args.f + col, rstride, lane);
         }
       } else if (KIND == KIND_DGRAD_X) {
-        // real rows to the unpadded grouped row; padding rows are dropped
-        const int seg_row = t.mt * BM + q * 32 + lane;
-        const bool real = seg_row < c.uoff[t.e + 1] - c.uoff[t.e];
-        const int ru = c.uoff[t.e] + seg_row;
-        if (__ballot_sync(0xffffffffu, real) != 0) {
+        // real rows (a prefix of the segment) to their unpadded grouped rows;
+        // padding rows are dropped
+        const int seg0 = t.mt * BM + q * 32;  // the warp's first segment row
+        const int rows_valid = min(32, c.uoff[t.e + 1] - c.uoff[t.e] - seg0);
+        if (rows_valid > 0) {
+          float *dst = args.out0 + static_cast<size_t>(c.uoff[t.e] + seg0) * args.n_out;
 #pragma unroll 1
           for (int cc = 0; cc < BN / 32; ++cc) {
             const int col = n0 + cc * 32;
@@ -349,22 +440,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
             ptx::tmem_wait_ld();
-            if (real) {
-              float *dst = args.out0 + static_cast<size_t>(ru) * args.n_out + col;
-#pragma unroll
-              for (int j = 0; j < 8; ++j)
-                *reinterpret_cast<float4 *>(dst + 4 * j) =
-                    make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-            }
+            store_block_f32(stage_tile, v, dst + col, args.n_out, rows_valid, false, lane);
           }
         }
       } else {
-        // weight gradient rows m of expert e (fp32, n contiguous)
-        const int m = t.mt * BM + q * 32 + lane;
-        const bool in = m < args.m_total;
+        // weight gradient rows m0.. of expert e (fp32, n contiguous)
+        const int m0 = t.mt * BM + q * 32;  // the warp's first row
+        const int rows_valid = min(32, args.m_total - m0);
         const bool empty = t.nkb == 0;
-        if (!(empty && args.accumulate)) {
+        if (!(empty && args.accumulate) && rows_valid > 0) {
 #pragma unroll 1
           for (int cc = 0; cc < BN / 32; ++cc) {
             const int col = n0 + cc * 32;
@@ -377,26 +461,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
               for (int j = 0; j < 32; ++j) v[j] = 0u;
             }
-            if (!in) continue;
             float *dst;
+            size_t ld;
             if (KIND == KIND_WGRAD_W2) {
-              dst = args.out0 + (static_cast<size_t>(t.e) * args.m_total + m) * args.n_out + col;
+              ld = args.n_out;
+              dst = args.out0 + (static_cast<size_t>(t.e) * args.m_total + m0) * ld + col;
             } else {
               // columns [0, f) are dW1's, [f, 2f) dW3's (f a multiple of 64)
               const bool w3 = col >= args.f;
-              dst = (w3 ? args.out1 : args.out0) + (static_cast<size_t>(t.e) * args.m_total + m) * args.f +
+              ld = args.f;
+              dst = (w3 ? args.out1 : args.out0) + (static_cast<size_t>(t.e) * args.m_total + m0) * ld +
                     (w3 ? col - args.f : col);
             }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-              float4 r = make_float4(__uint_as_float(v[4 * j]), __uint_as_float(v[4 * j + 1]),
-                                     __uint_as_float(v[4 * j + 2]), __uint_as_float(v[4 * j + 3]));
-              if (args.accumulate) {
-                const float4 o = *reinterpret_cast<const float4 *>(dst + 4 * j);
-                r.x += o.x; r.y += o.y; r.z += o.z; r.w += o.w;
-              }
-              *reinterpret_cast<float4 *>(dst + 4 * j) = r;
-            }
+            store_block_f32(stage_tile, v, dst, ld, rows_valid, args.accumulate != 0, lane);
           }
         }
       }
