@@ -56,6 +56,10 @@ CONFIGS = {
     "prefill_e2": dict(T=1024, d=4096, f=14336, E=2, K=2),
     # training step of the prefill layer: forward keeping activations + backward
     "train": dict(T=4096, d=4096, f=14336, E=8, K=2, train=True),
+    # decode with the expert banks in pinned host memory and C device slots
+    # (LRU), over a trace with the pages' temporal locality, or without it
+    "decode1_cache": dict(T=1, d=4096, f=14336, E=8, K=2, cache_slots=4, keep=0.35),
+    "decode1_cache_nolocality": dict(T=1, d=4096, f=14336, E=8, K=2, cache_slots=4, keep=0.0),
     # profiling stand-in of the training step: two Mixtral-sized experts with ~1024 rows each
     "train_e2": dict(T=1024, d=4096, f=14336, E=2, K=2, train=True),
 }
@@ -73,6 +77,11 @@ WORKLOAD_TEXT["train"] = ("Mixtral-shaped MoE layer training step (forward keepi
                           "dx, dWg, dW1, dW3, dW2 in fp32): T=4096 tokens, d=4096, f=14336, E=8, top-2, bf16")
 WORKLOAD_TEXT["train_e2"] = ("profiling stand-in of the training step: T=1024 tokens, d=4096, f=14336, E=2 experts, "
                              "top-2, bf16")
+for _n, _k in (("decode1_cache", "65% of consecutive tokens sharing an expert, as the pages' Table 5"),
+               ("decode1_cache_nolocality", "independent routing, ~46% sharing by chance")):
+    WORKLOAD_TEXT[_n] = ("Mixtral-shaped MoE layer decode, one token per step, expert banks in pinned host memory "
+                         f"with 4 of 8 experts cached on the GPU (LRU); routing trace: {_k}; bf16")
+CACHE_METRIC = "MoE layer decode tokens/s with experts offloaded to host memory (4 of 8 cached) on 1 B300"
 TRAIN_METRIC = "MoE layer training tokens/s (forward + backward) and TFLOP/s on 1 B300"
 WORKLOAD_TEXT["prefill_e2"] = "profiling stand-in: T=1024 tokens, d=4096, f=14336, E=2 experts, top-2, bf16"
 for _t in (1, 8, 32, 128):
@@ -620,6 +629,119 @@ def run_ours_stack(args, world, rank, local):
 
 
 # ---------------------------------------------------------------------------
+def run_ours_cache(args, world, rank, local):
+    """Decode steps through moe_forward_cached over a seeded locality trace."""
+    import sparse_mixture_experts_55_b300 as moe
+    from sparse_mixture_experts_55_b300 import build as _build
+    if rank == 0:
+        _build.build()
+    barrier(world)
+    dev = torch.device("cuda", local)
+    c = CONFIGS[args.config]
+    T, d, f, E, K, C = c["T"], c["d"], c["f"], c["E"], c["K"], c["cache_slots"]
+    Wg, W1, W3, W2 = W.mixtral_weights(d, f, E, seed=W.BASE_SEED, device=dev)
+    steps, warmup = args.steps, max(args.warmup, 3)
+    xs, _ = W.decode_trace(warmup + steps, Wg, T=T, keep=c["keep"], seed=W.BASE_SEED + 1009 * rank, device=dev)
+    cache = moe.ExpertCache(W1, W3, W2, C, dev)
+    ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
+    y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    # host-to-device link: pinned copies of one expert matrix, event-timed
+    mat = cache.host[0][0]
+    dst = torch.empty_like(mat, device=dev)
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dst.copy_(mat, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for _ in range(5):
+        dst.copy_(mat, non_blocking=True)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    link_gbs = 5 * mat.numel() * 2 / (ev0.elapsed_time(ev1) / 1e3) / 1e9
+    del dst
+
+    for i in range(warmup):
+        cache.forward(xs[i], Wg, K, y=y, workspace=ws, stream=stream)
+    torch.cuda.synchronize(dev)
+    st = cache.state
+    h0, m0, b0 = st.hits, st.misses, st.bytes_loaded
+    barrier(world)
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        start.record(stream)
+        for i in range(warmup, warmup + steps):
+            cache.forward(xs[i], Wg, K, y=y, workspace=ws, stream=stream)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+        wall_ms = 1e3 * (time.perf_counter() - t0) / steps
+    barrier(world)
+    ms = max_over_ranks(start.elapsed_time(end) / steps, world, dev)
+    if moe.moe_read_status(ws) != 0:
+        raise RuntimeError("device status set during timed run")
+    hits, misses, loaded = st.hits - h0, st.misses - m0, st.bytes_loaded - b0
+
+    # the same steps with every expert resident (moe_forward on the full banks)
+    for i in range(warmup):
+        moe.moe_forward(xs[i], Wg, W1, W3, W2, K, y=y, workspace=ws, stream=stream)
+    start.record(stream)
+    for i in range(warmup, warmup + steps):
+        moe.moe_forward(xs[i], Wg, W1, W3, W2, K, y=y, workspace=ws, stream=stream)
+    end.record(stream)
+    torch.cuda.synchronize(dev)
+    resident_ms = start.elapsed_time(end) / steps
+
+    # end to end: each step's token copied in from pinned memory and its output back
+    x_h = xs[warmup:warmup + steps].cpu().pin_memory()
+    y_h = torch.empty(steps, T, d, dtype=torch.bfloat16).pin_memory()
+    xd = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for i in range(steps):
+        xd.copy_(x_h[i], non_blocking=True)
+        cache.forward(xd, Wg, K, y=y, workspace=ws, stream=stream)
+        y_h[i].copy_(y, non_blocking=True)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / steps, world, dev)
+
+    achieved = loaded / (ms * steps / 1e3) / 1e9
+    line = {
+        "metric": CACHE_METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic: seeded random-init Mixtral-shaped weights, Markov-chain locality trace of steered tokens",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+                   "l2": "expert matrices of 117 MB each, larger than L2"},
+        "cache": {"slots": C, "experts": E, "hits": hits, "misses": misses,
+                  "hit_rate": hits / max(1, hits + misses), "bytes_loaded_per_step": loaded / steps,
+                  "wall_ms_per_step": wall_ms, "all_resident_ms_per_step": resident_ms,
+                  "device_weight_bytes": 3 * C * d * f * 2, "full_bank_bytes": 3 * E * d * f * 2},
+        "roofline": {"kernel": "host-to-device expert copies", "bound": "h2d", "achieved": achieved,
+                     "peak": link_gbs, "unit": "GB/s", "frac": achieved / link_gbs, "traffic": None,
+                     "peak_source": "pinned host-to-device copy of one 117 MB expert matrix, timed in this run"},
+        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
+        "gpu_launches": 6 * steps,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        import numpy as np
+        import oracle
+        n_tok = 8
+        x64 = xs[:n_tok, 0].float().cpu().numpy().astype(np.float64)
+        banks = [t.float().cpu().numpy().astype(np.float64) for t in (Wg, W1, W3, W2)]
+        t0 = time.perf_counter()
+        for j in range(n_tok):
+            oracle.moe_layer(x64[j:j + 1], *banks, K)
+        dt = time.perf_counter() - t0
+        line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                                "sample": f"first {n_tok} trace tokens one at a time, float64 oracle with every "
+                                          f"expert in host memory ({dt:.1f} s; weights upcast once, untimed)"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 BWD_STAGES = ("prep", "dgrad_h", "wgrad_w2", "dgrad_x", "wgrad_w13", "dx", "dwg")
 
 
@@ -932,6 +1054,8 @@ def main():
             run_ours_stack(args, world, rank, local)
         elif CONFIGS[args.config].get("train"):
             run_ours_train(args, world, rank, local)
+        elif "cache_slots" in CONFIGS[args.config]:
+            run_ours_cache(args, world, rank, local)
         else:
             run_ours(args, world, rank, local)
     finally:

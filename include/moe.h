@@ -281,6 +281,67 @@ MOE_API int moe_backward_timed(const void *x, const void *Wg, const void *W1, co
                 void *const *events);
 
 /*
+ * Decode-time expert cache (offload).  The routing analysis of the pages finds
+ * strong temporal locality -- consecutive tokens often go to the same experts
+ * ("Expert caching hint"; the Table 5 discussion) -- and names caching the
+ * frequently used experts in GPU memory, with the rest in CPU memory, as the
+ * optimisation it enables.  Here all E experts' weights live in pinned host
+ * memory and C <= E device slots hold copies; each call loads the experts its
+ * tokens need that are not resident, by least-recently-used replacement:
+ *   - the needed set N is the experts with at least one routed token;
+ *   - resident experts of N are hits; the others are misses, taken in
+ *     increasing expert index, each into the lowest-index empty slot or else
+ *     the slot of the least recently used resident expert outside N (ties
+ *     to the lowest slot index);
+ *   - every expert of N is marked used at the current step, then the step
+ *     advances; |N| > C is an error (MOE_ERR_UNSUPPORTED, nothing loaded).
+ * The state is a plain struct the caller owns; the library keeps none.
+ */
+#define MOE_CACHE_MAX_E 32
+typedef struct moe_expert_cache {
+  int E;                                /* experts */
+  int C;                                /* device slots */
+  int slot_of[MOE_CACHE_MAX_E];         /* expert -> slot, -1 if not resident */
+  int expert_in[MOE_CACHE_MAX_E];       /* slot -> expert, -1 if empty */
+  long long last_use[MOE_CACHE_MAX_E];  /* slot -> step of its last use, -1 if never */
+  long long step;                       /* steps planned so far */
+  long long hits, misses;               /* expert lookups so far */
+  long long bytes_loaded;               /* host-to-device weight bytes enqueued by moe_forward_cached */
+} moe_expert_cache;
+
+/* Empty cache of C slots for E experts (1 <= C <= E <= 32).  Host only. */
+MOE_API int moe_expert_cache_init(moe_expert_cache *cache, int E, int C);
+
+/*
+ * One step of the policy, host only: needed[E] (non-zero = needed) ->
+ * the loads to make, load_expert[i] into load_slot[i] for i < *n_loads
+ * (arrays of at least E entries), in the order above; updates the state.
+ * Returns MOE_ERR_UNSUPPORTED if more than C experts are needed (the state is
+ * then unchanged), MOE_ERR_INVALID_ARG for a null pointer or a state that is
+ * not consistent.
+ */
+MOE_API int moe_expert_cache_plan(moe_expert_cache *cache, const int *needed, int *load_expert, int *load_slot,
+                int *n_loads);
+
+/*
+ * moe_forward with the expert banks in host memory and a device cache:
+ *   W1_host, W3_host [E, d, f], W2_host [E, f, d]   pinned host memory (dtype)
+ *   W1_dev, W3_dev [C, d, f], W2_dev [C, f, d]      device slots, contents as
+ *                                                   the cache state says
+ * Routing runs first; the call then waits (on the host) for the per-expert
+ * token counts, plans the step with moe_expert_cache_plan, enqueues one
+ * host-to-device copy per missed expert and bank into its slot, and runs the
+ * expert GEMMs on the slots.  The result equals moe_forward's bit for bit.
+ * bf16 only (other dtypes: MOE_ERR_UNSUPPORTED); flags: MOE_ACCUMULATE |
+ * MOE_DEBUG_CHECKS; the workspace is moe_forward's.  A failed call may leave
+ * the cache state ahead of the device slots: re-initialise it.
+ */
+MOE_API int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const void *W3_host,
+                const void *W2_host, void *W1_dev, void *W3_dev, void *W2_dev, moe_expert_cache *cache,
+                void *y, int T, int d, int f, int E, int K, int dtype,
+                void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+
+/*
  * Routing only, for inspection: the router and grouping kernels that
  * moe_forward runs, with their results copied out in unpadded form
  * (section 3.4 gating function; "Top-K Gating Mechanism and Routing").

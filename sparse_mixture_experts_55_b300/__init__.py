@@ -24,7 +24,7 @@ from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_T
 
 __all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "quantize_weights_fp8",
            "moe_forward_fp8", "moe_forward_fp8_timed", "TrainWorkspace", "moe_forward_train", "moe_backward",
-           "LayerGrads", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
+           "LayerGrads", "ExpertCache", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
 
@@ -314,6 +314,43 @@ def moe_backward(x, Wg, W1, W3, W2, dy, K: int, workspace: TrainWorkspace, grads
                                   _stream_ptr(stream, x.device))
     _lib.check("moe_backward", rc)
     return grads
+
+
+class ExpertCache:
+    """Decode-time expert offload: the expert banks in pinned host memory, C
+    device slots, least-recently-used replacement (moe_forward_cached).
+
+    ``W1, W3, W2`` are the full banks (any device; copied to pinned host
+    memory once).  ``forward`` runs one batch; ``state`` exposes the policy's
+    counters (hits, misses, bytes_loaded) and maps."""
+
+    def __init__(self, W1, W3, W2, C: int, device=None):
+        if W1.dtype != torch.bfloat16:
+            raise TypeError("the expert cache holds bf16 banks")
+        E, d, f = W1.shape
+        self.E, self.d, self.f, self.C = E, d, f, C
+        self.device = torch.device(device) if device is not None else torch.device("cuda")
+        self.host = [w.detach().to("cpu").contiguous().pin_memory() for w in (W1, W3, W2)]
+        self.slots = [torch.empty((C,) + tuple(w.shape[1:]), dtype=w.dtype, device=self.device)
+                      for w in (W1, W3, W2)]
+        self.state = _lib.ExpertCacheState()
+        _lib.check("moe_expert_cache_init", _lib.load().moe_expert_cache_init(ctypes.byref(self.state), E, C))
+
+    def forward(self, x, Wg, K: int, y=None, workspace: Workspace | None = None, flags: int = 0, stream=None):
+        _need(x, "x", torch.bfloat16, self.device)
+        _need(Wg, "Wg", torch.bfloat16, self.device)
+        T, d = x.shape
+        if d != self.d or Wg.shape != (d, self.E):
+            raise ValueError("shape mismatch: x [T,d], Wg [d,E]")
+        if y is None:
+            y = torch.empty_like(x)
+        if workspace is None:
+            workspace = Workspace(T, d, self.f, self.E, K, torch.bfloat16, self.device)
+        rc = _lib.load().moe_forward_cached(_ptr(x), _ptr(Wg), *map(_ptr, self.host), *map(_ptr, self.slots),
+                                            ctypes.byref(self.state), _ptr(y), T, d, self.f, self.E, K, MOE_BF16,
+                                            workspace.ptr(), workspace.nbytes, flags, _stream_ptr(stream, x.device))
+        _lib.check("moe_forward_cached", rc)
+        return y
 
 
 class HostPipeline:

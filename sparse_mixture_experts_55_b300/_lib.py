@@ -36,6 +36,18 @@ MOE_GEMM_MULTICAST_PAIRS = 0x20
 
 # name -> (restype, argtypes), one entry per function declared in include/moe.h
 _vp, _i, _sz, _u = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t, ctypes.c_uint
+class ExpertCacheState(ctypes.Structure):
+    """Mirror of moe_expert_cache (include/moe.h)."""
+    _fields_ = [("E", ctypes.c_int), ("C", ctypes.c_int),
+                ("slot_of", ctypes.c_int * 32), ("expert_in", ctypes.c_int * 32),
+                ("last_use", ctypes.c_longlong * 32), ("step", ctypes.c_longlong),
+                ("hits", ctypes.c_longlong), ("misses", ctypes.c_longlong),
+                ("bytes_loaded", ctypes.c_longlong)]
+
+
+_ip = ctypes.POINTER(ctypes.c_int)
+_cp = ctypes.POINTER(ExpertCacheState)
+
 SIGNATURES = {
     "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
@@ -52,6 +64,10 @@ SIGNATURES = {
                           _vp]),
     "moe_backward_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp,
                                 _sz, _u, _vp, _vp]),
+    "moe_expert_cache_init": (_i, [_cp, _i, _i]),
+    "moe_expert_cache_plan": (_i, [_cp, _ip, _ip, _ip, _ip]),
+    "moe_forward_cached": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _cp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz,
+                                _u, _vp]),
     "moe_route": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "moe_route_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
     "moe_rmsnorm": (_i, [_vp, _vp, _i, _i, ctypes.c_float, _i, _vp]),

@@ -127,6 +127,10 @@ struct GemmArgs {
   // [0, n_out), b after), for every row of the segments including padding
   __nv_bfloat16 *save_ab;
   int *status;
+  // weight banks indexed by slot: expert e's matrices are slot wslot[e] of
+  // the banks (use_slots; otherwise slot e)
+  int use_slots;
+  int wslot[kMaxE];
 };
 
 struct Ctrl {
@@ -144,6 +148,7 @@ struct Ctrl {
   int mtiles[kMaxE];
   int poff[kMaxE + 1];
   int uoff[kMaxE + 1];
+  int wslot[kMaxE];
 };
 
 static_assert(sizeof(Ctrl) <= 1024, "control block too large");
@@ -274,6 +279,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int e = 0; e < args.E; ++e) {
       const int p0 = args.poffsets[e], p1 = args.poffsets[e + 1];
       if (p1 < p0 || (p1 - p0) % BM != 0 || p1 > args.rows_bound) bad = true;
+      c.wslot[e] = args.use_slots ? args.wslot[e] : e;
+      if (p1 > p0 && c.wslot[e] < 0) bad = true;  // rows routed to an expert that is not resident
       const int mt = bad ? 0 : (p1 - p0) / BM;
       c.poff[e] = p0;
       c.uoff[e] = args.offsets[e];
@@ -350,10 +357,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + rank * (BN / 2);
             if (FP8) {
               // e4m3 banks are K-contiguous ([E, N, K]): one 128 x 128 box, 16 KiB
-              ptx::tma_load_3d_pair(b_dst, mb, bar, k0, nb, t.e, pol_b);
+              ptx::tma_load_3d_pair(b_dst, mb, bar, k0, nb, c.wslot[t.e], pol_b);
             } else {
-              ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, t.e, pol_b);
-              ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, t.e, pol_b);
+              ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, c.wslot[t.e], pol_b);
+              ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, c.wslot[t.e], pol_b);
             }
           } else {
             // multicast forms: this CTA's share of the A and B tiles, each
@@ -378,16 +385,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const CUtensorMap *mb = (MODE == MODE_GATE_UP && h == 1) ? &tmB1 : &tmB0;
               const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + h * (BN / 2);
               uint8_t *dst = b_dst + h * (2 * B_CHUNK);
+              const int wz = c.wslot[t.e];  // the bank slot holding expert e's weights
               if (FP8) {
-                if (mask) ptx::tma_load_3d_mc(dst, mb, bar, k0, nb, t.e, mask, pol_b);
-                else ptx::tma_load_3d(dst, mb, bar, k0, nb, t.e, pol_b);
+                if (mask) ptx::tma_load_3d_mc(dst, mb, bar, k0, nb, wz, mask, pol_b);
+                else ptx::tma_load_3d(dst, mb, bar, k0, nb, wz, pol_b);
               } else {
                 if (mask) {
-                  ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, t.e, mask, pol_b);
-                  ptx::tma_load_3d_mc(dst + B_CHUNK, mb, bar, nb + 64, k0, t.e, mask, pol_b);
+                  ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, wz, mask, pol_b);
+                  ptx::tma_load_3d_mc(dst + B_CHUNK, mb, bar, nb + 64, k0, wz, mask, pol_b);
                 } else {
-                  ptx::tma_load_3d(dst, mb, bar, nb, k0, t.e, pol_b);
-                  ptx::tma_load_3d(dst + B_CHUNK, mb, bar, nb + 64, k0, t.e, pol_b);
+                  ptx::tma_load_3d(dst, mb, bar, nb, k0, wz, pol_b);
+                  ptx::tma_load_3d(dst + B_CHUNK, mb, bar, nb + 64, k0, wz, pol_b);
                 }
               }
             };
@@ -917,16 +925,18 @@ cudaError_t launch_form(int form, const Grids &g, cudaStream_t s, bool pdl, cons
 
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
-                                     cudaStream_t s, void *const *mid_event) {
+                                     cudaStream_t s, void *const *mid_event, const int *slot_of, int n_slots) {
   Grids grids;
   cudaError_t err = device_state(num_sms, &grids);
   if (err != cudaSuccess) return err;
   const int form = pick_form(L, grids);
+  const int banks = slot_of ? n_slots : E;  // matrices held by each weight bank
   CUtensorMap tm_x, tm_xh, tm_xq, tm_w1, tm_w3, tm_h, tm_hh, tm_hq, tm_w2;
   if (!tmap_2d(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d(&tm_xh, P.xperm, d, L.R, BM / 2) ||
-      !tmap_2d(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_3d(&tm_w1, W1, f, d, E) || !tmap_3d(&tm_w3, W3, f, d, E) ||
-      !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) || !tmap_2d(&tm_hh, P.hbuf, f, L.R, BM / 2) ||
-      !tmap_2d(&tm_hq, P.hbuf, f, L.R, BM / 4) || !tmap_3d(&tm_w2, W2, d, f, E))
+      !tmap_2d(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_3d(&tm_w1, W1, f, d, banks) ||
+      !tmap_3d(&tm_w3, W3, f, d, banks) || !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) ||
+      !tmap_2d(&tm_hh, P.hbuf, f, L.R, BM / 2) || !tmap_2d(&tm_hq, P.hbuf, f, L.R, BM / 4) ||
+      !tmap_3d(&tm_w2, W2, d, f, banks))
     return cudaErrorInvalidValue;
 
   GemmArgs g1{};
@@ -948,6 +958,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
   g1.save_ab = static_cast<__nv_bfloat16 *>(P.ab);  // training forward only (then splits == 1)
   g1.status = P.status;
+  g1.use_slots = slot_of ? 1 : 0;
+  for (int e = 0; e < E && slot_of; ++e) g1.wslot[e] = slot_of[e];
   err = launch_form<MODE_GATE_UP, false>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;

@@ -122,9 +122,13 @@ cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, in
 
 // -------- gemm_tc.cu (bf16 tensor-core path)
 // mid_event (optional): recorded between the gate/up and the down kernel.
+// slot_of (host array of E entries, or null): expert e's matrices are slot
+// slot_of[e] of banks holding n_slots matrices each (the expert cache);
+// without it, slot e of banks of E.
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
-                                     cudaStream_t s, void *const *mid_event);
+                                     cudaStream_t s, void *const *mid_event, const int *slot_of = nullptr,
+                                     int n_slots = 0);
 
 // -------- fp8.cu (e4m3 expert weights)
 cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, cudaStream_t s);

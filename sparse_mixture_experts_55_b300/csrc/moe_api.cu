@@ -365,6 +365,60 @@ int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void 
   return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, events);
 }
 
+int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const void *W3_host, const void *W2_host,
+                       void *W1_dev, void *W3_dev, void *W2_dev, moe_expert_cache *cache, void *y, int T, int d,
+                       int f, int E, int K, int dtype, void *workspace, size_t ws_bytes, unsigned flags,
+                       moe_stream_t stream) {
+  if (dtype != MOE_BF16) return MOE_ERR_UNSUPPORTED;
+  int st = check_shape(T, d, f, E, K, dtype);
+  if (st != MOE_OK) return st;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS)) return MOE_ERR_INVALID_ARG;
+  if (!cache || cache->E != E || cache->C < 1 || cache->C > E) return MOE_ERR_INVALID_ARG;
+  if (T == 0) return MOE_OK;
+  const void *ptrs[] = {x, Wg, W1_host, W3_host, W2_host, W1_dev, W3_dev, W2_dev, y};
+  for (const void *p : ptrs)
+    if (!p || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+  const size_t act_bytes = static_cast<size_t>(T) * d * 2;
+  if (overlaps(x, act_bytes, y, act_bytes)) return MOE_ERR_INVALID_ARG;
+  if (!workspace || !aligned16(workspace)) return MOE_ERR_WORKSPACE;
+  const int sms = sm_count_or_default();
+  WsLayout L = ws_layout(T, d, f, E, K, dtype, sms);
+  if (ws_bytes < L.total) return MOE_ERR_WORKSPACE;
+  st = check_device();
+  if (st != MOE_OK) return st;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const Ptrs P = carve(workspace, L);
+  if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_group(T, E, K, L, flags, P, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // the experts this batch needs: wait for the grouping's segment offsets
+  int32_t offs[kMaxE + 1];
+  if (cudaMemcpyAsync(offs, P.offsets, (E + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int needed[kMaxE], load_e[kMaxE], load_s[kMaxE], n_loads = 0;
+  for (int e = 0; e < E; ++e) needed[e] = offs[e + 1] > offs[e] ? 1 : 0;
+  st = moe_expert_cache_plan(cache, needed, load_e, load_s, &n_loads);
+  if (st != MOE_OK) return st;
+  // one copy per missed expert and bank, into its slot (ordered before the GEMMs)
+  const size_t mat = static_cast<size_t>(d) * f * 2;
+  const char *hosts[3] = {static_cast<const char *>(W1_host), static_cast<const char *>(W3_host),
+                          static_cast<const char *>(W2_host)};
+  char *devs[3] = {static_cast<char *>(W1_dev), static_cast<char *>(W3_dev), static_cast<char *>(W2_dev)};
+  for (int i = 0; i < n_loads; ++i)
+    for (int b = 0; b < 3; ++b)
+      if (cudaMemcpyAsync(devs[b] + load_s[i] * mat, hosts[b] + load_e[i] * mat, mat, cudaMemcpyHostToDevice, s) !=
+          cudaSuccess)
+        return MOE_ERR_CUDA;
+  cache->bytes_loaded += static_cast<long long>(n_loads) * 3 * static_cast<long long>(mat);
+  cudaError_t err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
+  if (err == cudaSuccess)
+    err = launch_expert_gemms_bf16(W1_dev, W3_dev, W2_dev, d, f, E, L, P, flags, sms, s, nullptr, cache->slot_of,
+                                   cache->C);
+  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
+  return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
 size_t moe_train_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
   if (check_train_shape(T, d, f, E, K, dtype) != MOE_OK) return 0;
   return ws_layout(T, d, f, E, K, dtype, sm_count_or_default(), true).total;

@@ -31,6 +31,7 @@ def test_header_declares_the_boundary():
     assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_block_forward", "moe_route",
                             "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_timed",
                             "moe_train_workspace_bytes", "moe_forward_train", "moe_backward", "moe_backward_timed",
+                            "moe_expert_cache_init", "moe_expert_cache_plan", "moe_forward_cached",
                             "moe_route_noalloc", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
@@ -219,3 +220,24 @@ def test_training_entry_points_reject_bad_arguments(lib):
     assert bwd(dx=0x50_000000 + 64) == _lib.MOE_ERR_INVALID_ARG        # dx overlaps dW2
     assert bwd(ws=0) == _lib.MOE_ERR_WORKSPACE
     assert bwd(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
+
+
+def test_cached_forward_rejects_bad_arguments(lib):
+    vp = ctypes.c_void_p
+    st = _lib.ExpertCacheState()
+    assert lib.moe_expert_cache_init(ctypes.byref(st), 8, 4) == 0
+
+    def fwd(E=8, dt=_lib.MOE_BF16, w1h=0x3000, w1d=0x30_000000, flags=0, ws=0x60_000000, ws_bytes=1 << 40, cache=True):
+        return lib.moe_forward_cached(vp(0x1000), vp(0x2000), vp(w1h), vp(0x4000), vp(0x5000), vp(w1d),
+                                      vp(0x40_000000), vp(0x50_000000), ctypes.byref(st) if cache else None,
+                                      vp(0x100000), 4, 128, 256, E, 2, dt, vp(ws), ws_bytes, flags, vp(0))
+
+    assert fwd(dt=_lib.MOE_F32) == _lib.MOE_ERR_UNSUPPORTED
+    assert fwd(E=6) == _lib.MOE_ERR_INVALID_ARG            # the cache was made for 8 experts
+    assert fwd(cache=False) == _lib.MOE_ERR_INVALID_ARG
+    assert fwd(w1h=0) == _lib.MOE_ERR_INVALID_ARG
+    assert fwd(w1d=0x30_000008) == _lib.MOE_ERR_INVALID_ARG  # misaligned slot bank
+    assert fwd(flags=0x8) == _lib.MOE_ERR_INVALID_ARG        # GEMM form flags are not taken here
+    assert fwd(ws=0) == _lib.MOE_ERR_WORKSPACE
+    assert fwd(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
+    assert st.step == 0

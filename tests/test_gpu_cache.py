@@ -1,0 +1,58 @@
+"""GPU checks of the decode-time expert cache (moe_forward_cached): over a
+locality trace the cached layer equals moe_forward bit for bit at every step
+(the same kernels, reading expert e from its slot), and the cache's decisions
+(loads, hits, misses, maps) equal the oracle LRU policy's on the needed sets
+the GPU routing produced.  A step that needs more experts than there are
+slots is refused without changing the state."""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle.cache_oracle import LRUCache
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def moe(cuda_device):
+    from sparse_mixture_experts_55_b300 import build
+    build.build()
+    import sparse_mixture_experts_55_b300 as m
+    return m
+
+
+@pytest.mark.parametrize("T,C,steps,keep", [(1, 3, 24, 0.35), (1, 2, 16, 0.0), (2, 4, 12, 0.35), (1, 8, 10, 0.35)])
+def test_cached_forward_equals_forward_and_policy_matches_oracle(moe, cuda_device, T, C, steps, keep):
+    d, f, E, K = 256, 512, 8, 2
+    Wg, W1, W3, W2 = (t.to(cuda_device) for t in W.mixtral_weights(d, f, E, seed=21, device="cpu"))
+    xs, _ = W.decode_trace(steps, Wg, T=T, keep=keep, seed=21, device=cuda_device)
+    cache = moe.ExpertCache(W1, W3, W2, C, cuda_device)
+    ref = LRUCache(E, C)
+    ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, cuda_device)
+    for i in range(steps):
+        x = xs[i].contiguous()
+        y = cache.forward(x, Wg, K, workspace=ws)
+        y_ref = moe.moe_forward(x, Wg, W1, W3, W2, K)
+        torch.cuda.synchronize()
+        assert torch.equal(y, y_ref), i
+        idx, *_ = moe.moe_route(x, Wg, K)
+        ref.plan(sorted(set(idx.flatten().tolist())))
+        st = cache.state
+        assert list(st.slot_of)[:E] == ref.slot_of and list(st.expert_in)[:C] == ref.expert_in, i
+        assert (st.hits, st.misses) == (ref.hits, ref.misses)
+    assert cache.state.bytes_loaded == ref.misses * 3 * d * f * 2
+    assert moe.moe_read_status(ws) == 0
+
+
+def test_step_needing_more_experts_than_slots_is_refused(moe, cuda_device):
+    d, f, E, K = 256, 512, 8, 2
+    Wg, W1, W3, W2 = (t.to(cuda_device) for t in W.mixtral_weights(d, f, E, seed=22, device="cpu"))
+    x = W.rms_rows(64, d, 5, cuda_device)  # 64 tokens reach more than 2 experts
+    cache = moe.ExpertCache(W1, W3, W2, 2, cuda_device)
+    with pytest.raises(moe.MoEError) as ei:
+        cache.forward(x, Wg, K)
+    assert ei.value.code == moe._lib.MOE_ERR_UNSUPPORTED
+    assert cache.state.step == 0 and cache.state.misses == 0 and cache.state.bytes_loaded == 0

@@ -34,7 +34,7 @@ MIXTRAL = dict(d=4096, f=14336, E=8, K=2)
 GOLDEN_DIR = pathlib.Path(__file__).resolve().parent / "tests" / "golden"
 
 # Tensor tags: one generator stream per tensor so subsets can be regenerated.
-_TAG = {"x": 1, "Wg": 2, "W1": 3, "W3": 4, "W2": 5, "tie": 6, "h0": 7}
+_TAG = {"x": 1, "Wg": 2, "W1": 3, "W3": 4, "W2": 5, "tie": 6, "h0": 7, "trace": 8}
 
 
 def _seed(seed: int, tag: str, sub: int = 0) -> int:
@@ -240,3 +240,46 @@ def stack_h0(T=8192, d=4096, seed=BASE_SEED, device="cpu", dtype=torch.bfloat16)
 
 def stack_layer_weights(l: int, d=4096, f=14336, E=8, seed=BASE_SEED, device="cpu", dtype=torch.bfloat16):
     return mixtral_weights(d, f, E, stack_layer_seed(l, seed), device, dtype)
+
+
+# ---------------------------------------------------------------------------
+# decode traces with temporal locality (expert cache)
+# ---------------------------------------------------------------------------
+# The pages' routing analysis (Table 5) reports that consecutive tokens share
+# their first or second expert 61.6-67.0% of the time at layer 15, against
+# ~46% for independent choices (1 - C(6,2)/C(8,2) = 46.4% for 8 experts, top
+# 2).  A chain that keeps the previous step's expert pair with probability
+# `keep` and otherwise draws a uniform pair shares one with probability
+# keep + (1 - keep) * 0.464; keep = 0.35 gives 65%.
+TRACE_KEEP = 0.35
+TRACE_STEER = 5.0
+
+
+def decode_trace(steps: int, Wg: torch.Tensor, T: int = 1, keep: float = TRACE_KEEP, seed=BASE_SEED,
+                 device="cpu", dtype=torch.bfloat16, steer: float = TRACE_STEER):
+    """Token rows for `steps` decode steps of T tokens each ([steps, T, d]).
+
+    Each of the T token streams walks a Markov chain over expert pairs
+    (above); its token at a step is z + steer * (u_a + u_b), RMS-normalised,
+    with z ~ N(0, I) and u_e = Wg[:, e] / |Wg[:, e]|^2, which raises the
+    logits of experts a and b by about `steer` over N(0, 1) noise, so the
+    router mostly picks the chain's pair.  Returns (x, pairs) with pairs
+    [steps, T, 2] the chain's intended experts (the router decides the
+    actual ones)."""
+    d, E = Wg.shape
+    g = torch.Generator(device="cpu")
+    g.manual_seed(_seed(seed, "trace", T))
+    pairs = torch.empty((steps, T, 2), dtype=torch.long)
+    for t in range(T):
+        cur = torch.randperm(E, generator=g)[:2]
+        for i in range(steps):
+            if i > 0 and torch.rand((), generator=g).item() >= keep:
+                cur = torch.randperm(E, generator=g)[:2]
+            pairs[i, t] = cur
+    W = Wg.detach().to("cpu", torch.float32)
+    U = W / (W * W).sum(dim=0, keepdim=True)
+    z = randn((steps * T, d), 1.0, _seed(seed, "trace", 10_000 + T), "cpu")
+    flat = pairs.reshape(-1, 2)
+    x = z + steer * (U[:, flat[:, 0]].T + U[:, flat[:, 1]].T)
+    x = x * torch.rsqrt(x.pow(2).mean(dim=1, keepdim=True) + 1e-5)
+    return x.reshape(steps, T, d).to(device=device, dtype=dtype), pairs
