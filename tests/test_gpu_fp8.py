@@ -112,6 +112,30 @@ def test_fp8_full_size_decode_one_token(moe, cuda_device):
     assert err <= 2e-2
 
 
+def test_fp8_full_size_prefill_sampled_tokens(moe, cuda_device):
+    """The bench's prefill_fp8 workload (T=4096, Mixtral sizes), checked on
+    eight tokens that chose the most common expert pair {a, b}: their outputs
+    depend only on experts a and b (activation and H scales are per row), and
+    with the router restricted to columns a and b they keep the same pair and
+    gates, so the oracle quantises and evaluates those two experts only."""
+    Wg, W1, W3, W2 = W.mixtral_weights(device=cuda_device)
+    inp = W.prefill(device=cuda_device, weights=(Wg, W1, W3, W2))
+    q = [t for B in (W1, W3, W2) for t in moe.quantize_weights_fp8(B)]
+    y = moe.moe_forward_fp8(inp.x, Wg, *q, 2)
+    x = inp.x.cpu()
+    g = oracle.gating(x, Wg.cpu(), 2)
+    pairs = [tuple(sorted(r)) for r in g.idx.tolist()]
+    a, b = max(set(pairs), key=pairs.count)
+    gap, _ = oracle.logit_gaps(oracle.router_logits(oracle.f64(x), oracle.f64(Wg.cpu())), 2)
+    toks = [t for t, p in enumerate(pairs) if p == (a, b) and gap[t] > 1e-4][::17][:8]
+    sel = [a, b]
+    banks = [t for B in (W1, W3, W2) for t in F8.quantize_weight_columns(B[sel].cpu())]
+    ref = F8.moe_layer_fp8(x[toks], Wg.cpu()[:, sel], *banks, 2)
+    err = parity.rel_linf(_np(y[toks].float()), ref.y)
+    print(f"\nfp8 full-size prefill: experts {sel}, tokens {toks}, rel err {err:.2e}")
+    assert err <= 2e-2
+
+
 @pytest.mark.parametrize("T,d,f,E,K", [(1100, 512, 1024, 4, 2), (700, 256, 384, 2, 1)])
 def test_fp8_gemm_forms_agree_bit_for_bit(moe, T, d, f, E, K):
     x, Wg, W1, W3, W2 = _fp8_case(T, d, f, E, K, seed=60 + T)

@@ -116,3 +116,19 @@ def test_planted_backward_mistake_is_caught(name, monkeypatch):
     monkeypatch.setattr(OM, attr, fn)
     with pytest.raises(AssertionError):
         test_gradients_match_finite_differences(2, 4)
+
+
+def test_weight_gradients_separate_over_columns_and_dx_over_tokens():
+    # The full-size GPU check samples these: restricting every expert to a set
+    # J of intermediate columns leaves the routing and the gradients of the
+    # kept weights unchanged, and a token subset keeps its dx rows.
+    x, Wg, W1, W3, W2, dy = _case(T=9, d=8, f=12, E=4, K=2, seed=8)
+    full = oracle.moe_layer_backward(x, Wg, W1, W3, W2, 2, dy)
+    J = [0, 5, 11]
+    part = oracle.moe_layer_backward(x, Wg, W1[:, :, J], W3[:, :, J], W2[:, J, :], 2, dy)
+    np.testing.assert_allclose(part.dW1, full.dW1[:, :, J], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(part.dW3, full.dW3[:, :, J], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(part.dW2, full.dW2[:, J, :], rtol=0, atol=1e-12)
+    S = [1, 4, 8]
+    sub = oracle.moe_layer_backward(x[S], Wg, W1, W3, W2, 2, dy[S])
+    np.testing.assert_allclose(sub.dx, full.dx[S], rtol=0, atol=1e-12)
