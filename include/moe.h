@@ -254,7 +254,9 @@ MOE_API int moe_forward_fp8_timed(const void *x, const void *Wg, const void *W1q
  *   with MOE_ACCUMULATE); x, dy and dx may then be NULL.  The outputs must
  *   not overlap one another.  Device-side errors are recorded in the
  *   workspace status word (moe_read_status); the backward does not clear it.
- *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS.
+ *   flags: MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT (the
+ *   first grouped product's bounded wait expires: MOE_ERR_DEVICE_TIMEOUT is
+ *   recorded and the gradients are unspecified).
  */
 MOE_API size_t moe_train_workspace_bytes(int T, int d, int f, int E, int K, int dtype);
 MOE_API int moe_forward_train(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,

@@ -33,7 +33,9 @@
 //
 // Every mbarrier wait is bounded (about one second); on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT, stops issuing work, waits (bounded) for its own
-// copies and MMAs in flight, frees TMEM and returns.
+// copies and MMAs in flight, frees TMEM and returns.  MOE_DEBUG_FORCE_TIMEOUT
+// makes the dH product's MMA thread first wait on a barrier that nothing
+// signals, which runs that path.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -84,6 +86,7 @@ struct BwdArgs {
   float *out0;              // dX [T*K, d]; dW2 [E, f, d]; dW1 [E, d, f]
   float *out1;              // dW3 [E, d, f]
   int accumulate;           // weight gradients: add to out0 / out1
+  int force_timeout;        // failure-path test: wait on a barrier nothing signals first
   int *status;
 };
 
@@ -93,6 +96,7 @@ struct Ctrl {
   uint64_t tfull[2];
   uint64_t tempty[2];
   uint64_t drain;
+  uint64_t stall;  // never signalled (failure-path test)
   uint32_t tmem_base;
   int abort;
   int total_units;
@@ -239,6 +243,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ptx::mbar_init(&c.tempty[a], 4);  // one arrival per epilogue warp
     }
     ptx::mbar_init(&c.drain, 1);
+    ptx::mbar_init(&c.stall, 1);
     ptx::fence_barrier_init();
   }
   ptx::grid_dependency_wait();  // the previous kernel's outputs are read below
@@ -334,6 +339,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t phase = 0;
       int local = 0;
       bool ok = true;
+      // failure-path test: this wait expires, raising the CTA's abort flag
+      if (args.force_timeout) ok = wait_bounded(&c.stall, 0, c, args.status, true);
       for (int u = blockIdx.x; ok && u < total; u += gridDim.x) {
         const BTile t = decode_tile<KIND>(u, c, args);
         const int acc = local & 1;
@@ -529,8 +536,8 @@ cudaError_t launch_one(int num_sms, cudaStream_t s, const CUtensorMap &a, const 
 }  // namespace
 
 cudaError_t launch_bwd_gemms(const void *W1, const void *W3, const void *W2, void *dW1, void *dW3, void *dW2, int d,
-                             int f, int E, bool accumulate, const WsLayout &L, const Ptrs &P, int num_sms,
-                             cudaStream_t s, void *const *events) {
+                             int f, int E, bool accumulate, bool force_timeout, const WsLayout &L, const Ptrs &P,
+                             int num_sms, cudaStream_t s, void *const *events) {
   // events (optional): recorded after each of the four products
   auto mark = [&](int i) -> cudaError_t {
     return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
@@ -560,6 +567,7 @@ cudaError_t launch_bwd_gemms(const void *W1, const void *W3, const void *W2, voi
   g.num_kb = d / BK;
   g.ab = static_cast<const __nv_bfloat16 *>(P.ab);
   g.dab = static_cast<__nv_bfloat16 *>(P.dab);
+  g.force_timeout = force_timeout ? 1 : 0;
   cudaError_t err = launch_one<KIND_DGRAD_H>(num_sms, s, tm_dye_k, tm_w2_k, tm_w2_k, g);
   if (err == cudaSuccess) err = mark(0);
   if (err != cudaSuccess) return err;

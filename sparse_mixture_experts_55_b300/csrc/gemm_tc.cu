@@ -131,6 +131,15 @@ struct GemmArgs {
   // the banks (use_slots; otherwise slot e)
   int use_slots;
   int wslot[kMaxE];
+  // fused combine (down GEMM without splits): y [T, n_out] bf16 gets, per
+  // token and 256-column tile, the sum over its K slot rows of O in slot
+  // order, formed by whichever slot's epilogue arrives last on tok_cnt
+  __nv_bfloat16 *y;
+  int y_accumulate;
+  const int32_t *pos;       // [T*K] unpadded grouped row of each (token, slot)
+  const int32_t *perm_tok;  // [R] token of each padded grouped row
+  int *tok_cnt;             // [T, num_n_tiles], zero at launch
+  int T, K;
 };
 
 struct Ctrl {
@@ -161,7 +170,9 @@ struct Tile {
 // Units of expert e: its M-pairs ordered (pair group, split, n-tile, pair in
 // group) with the pair fastest, so clusters running together share weight
 // panels; then, for an odd m-tile count, the N-pairs of its last m-tile
-// (multicast pairs) or one more M-pair with a phantom second tile (pair MMA).
+// (multicast pairs; interleaved with the M-pairs of their n-tiles when the
+// expert has one pair group) or one more M-pair with a phantom second tile
+// (pair MMA).
 template <int FORM>
 __device__ __forceinline__ int units_of(int mt_e, int NT, int S) {
   if (FORM == FORM_PAIR) return ((mt_e + 1) >> 1) * NT * S;
@@ -177,6 +188,30 @@ __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S,
   int r = u - c.ustart[e];
   const int mt_e = c.mtiles[e];
   const int mp = FORM == FORM_PAIR ? (mt_e + 1) >> 1 : mt_e >> 1;
+  if (FORM == FORM_MC2 && (mt_e & 1) && mp <= GROUP_PAIRS) {
+    // Multicast pairs, odd tile count, one pair group: per split, blocks of
+    // the M-pairs of n-tiles 2j and 2j+1 (pair fastest) followed by the
+    // N-pair of those two n-tiles on the last m-tile, so the N-pair reads the
+    // weight panels while the M-pairs still hold them in L2.
+    const int per_s = NT * mp + ((NT + 1) >> 1);
+    t.e = e;
+    t.s = r / per_s;
+    r -= t.s * per_s;
+    const int blk = 2 * mp + 1;
+    const int j = r / blk;
+    const int w = r - j * blk;
+    if (w < min(2, NT - 2 * j) * mp) {
+      const int q = w / mp;  // mp > 0 here
+      t.nt = 2 * j + q;
+      t.mt = 2 * (w - q * mp) + rank;
+      t.npair = false;
+    } else {
+      t.nt = 2 * j + rank;  // may reach NT: all its loads and stores fall outside
+      t.mt = mt_e - 1;
+      t.npair = true;
+    }
+    return t;
+  }
   // n positions per M-pair unit: every n-tile, or n-tile pairs for 2x2 tiles
   const int nu = FORM == FORM_MC4 ? (NT + 1) >> 1 : NT;
   const int per = nu * S;
@@ -752,6 +787,91 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
+        if (args.y != nullptr && n0 < args.n_out) {
+          // Fused combine: the slot that completes this token's 256 columns
+          // last adds the K slot rows in slot order (the combine kernel's
+          // order, so y is the same bit for bit) and stores y.  The warp
+          // finishes its rows that arrived last together, four at a time,
+          // lane l taking columns [8l, 8l + 8) of each.
+          int tok = -1, last = 0;
+          if (real) {
+            __threadfence();  // this row's O stores precede the arrival
+            tok = args.perm_tok[row];
+            if (tok < 0 || tok >= args.T) {
+              atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
+            } else {
+              last = atomicAdd(args.tok_cnt + static_cast<size_t>(tok) * NT + t.nt, 1) == args.K - 1;
+            }
+          }
+          unsigned m = __ballot_sync(0xffffffffu, last);
+          if (m) __threadfence();  // the other slots' stores are visible to every lane
+          const int c8 = 8 * lane;
+          const bool col_in = c8 < args.n_out - n0;  // n_out is a multiple of 8
+          static_assert(kMaxK == 2, "the fused combine adds at most two slot rows");
+          while (m) {
+            int tk[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              const int src = m ? __ffs(m) - 1 : -1;
+              m &= m ? m - 1 : 0u;
+              tk[q] = __shfl_sync(0xffffffffu, tok, src < 0 ? 0 : src);
+              if (src < 0) tk[q] = -1;
+            }
+            float4 a[4][2], b[4][2];
+            bool ok[4];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              ok[q] = false;
+              if (tk[q] < 0) continue;
+              const int p0 = args.pos[tk[q] * args.K];
+              const int p1 = args.K > 1 ? args.pos[tk[q] * args.K + 1] : 0;
+              ok[q] = p0 >= 0 && p0 < args.tk && p1 >= 0 && p1 < args.tk;
+              if (!ok[q] || !col_in) continue;
+              const float *s0 = O + static_cast<size_t>(p0) * args.n_out + n0 + c8;
+              const float *s1 = O + static_cast<size_t>(p1) * args.n_out + n0 + c8;
+              a[q][0] = __ldcg(reinterpret_cast<const float4 *>(s0));
+              a[q][1] = __ldcg(reinterpret_cast<const float4 *>(s0 + 4));
+              if (args.K > 1) {
+                b[q][0] = __ldcg(reinterpret_cast<const float4 *>(s1));
+                b[q][1] = __ldcg(reinterpret_cast<const float4 *>(s1 + 4));
+              }
+            }
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+              if (tk[q] < 0) continue;
+              if (!ok[q]) {
+                if (lane == 0) atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
+                continue;
+              }
+              if (!col_in) continue;
+              float v[8] = {a[q][0].x, a[q][0].y, a[q][0].z, a[q][0].w, a[q][1].x, a[q][1].y, a[q][1].z, a[q][1].w};
+              if (args.K > 1) {
+                const float w[8] = {b[q][0].x, b[q][0].y, b[q][0].z, b[q][0].w,
+                                    b[q][1].x, b[q][1].y, b[q][1].z, b[q][1].w};
+#pragma unroll
+                for (int i = 0; i < 8; ++i) v[i] += w[i];
+              }
+              uint4 *yp = reinterpret_cast<uint4 *>(args.y + static_cast<size_t>(tk[q]) * args.n_out + n0 + c8);
+              if (args.y_accumulate) {
+                const uint4 o = *yp;
+                const uint32_t ow[4] = {o.x, o.y, o.z, o.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[i]));
+                  v[2 * i] = f2.x + v[2 * i];
+                  v[2 * i + 1] = f2.y + v[2 * i + 1];
+                }
+              }
+              uint32_t yw[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * i], v[2 * i + 1]);
+                yw[i] = *reinterpret_cast<const uint32_t *>(&h);
+              }
+              *yp = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+            }
+          }
+        }
       }
       ++local;
     }
@@ -921,10 +1041,22 @@ cudaError_t launch_form(int form, const Grids &g, cudaStream_t s, bool pdl, cons
   return launch_gemm<MODE, FORM_MC2, FP8>(g, s, pdl, a, ah, aq, b0, b1, args);
 }
 
+// The down GEMM's fused-combine arguments (y formed in its epilogue).
+void set_fused_combine(GemmArgs &g, const WsLayout &L, const Ptrs &P, void *y, unsigned flags) {
+  if (!L.fuse_combine) return;
+  g.y = static_cast<__nv_bfloat16 *>(y);
+  g.y_accumulate = (flags & MOE_ACCUMULATE) ? 1 : 0;
+  g.pos = P.pos;
+  g.perm_tok = P.perm_tok;
+  g.tok_cnt = P.tok_cnt;
+  g.T = L.T;
+  g.K = L.K;
+}
+
 }  // namespace
 
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
-                                     const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
+                                     const WsLayout &L, const Ptrs &P, void *y, unsigned flags, int num_sms,
                                      cudaStream_t s, void *const *mid_event, const int *slot_of, int n_slots) {
   Grids grids;
   cudaError_t err = device_state(num_sms, &grids);
@@ -971,6 +1103,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.tile_cnt = nullptr;
   g2.force_timeout = 0;
   g2.save_ab = nullptr;
+  set_fused_combine(g2, L, P, y, flags);
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + BK - 1) / BK;
@@ -981,7 +1114,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
 
 cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
                                     const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
-                                    const Ptrs &P, unsigned flags, int num_sms, cudaStream_t s,
+                                    const Ptrs &P, void *y, unsigned flags, int num_sms, cudaStream_t s,
                                     void *const *mid_event) {
   Grids grids;
   cudaError_t err = device_state(num_sms, &grids);
@@ -1028,6 +1161,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g2.out_split_stride = static_cast<long long>(L.TK) * d;
   g2.part = nullptr;
   g2.tile_cnt = nullptr;
+  set_fused_combine(g2, L, P, y, flags);
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + 127) / 128;

@@ -46,14 +46,16 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 struct WsLayout {
   // byte offsets into the workspace
-  size_t status, tile_cnt, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf, obuf,
-      gu_part, xnorm;
+  size_t status, tile_cnt, tok_cnt, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf,
+      obuf, gu_part, xnorm;
   size_t xscale, habs, hq, hscale;  // e4m3 variant only (0 bytes otherwise)
   size_t ab, dye, dab, dxc, dl, dwg_part;  // training only (0 bytes otherwise)
   int dwg_chunks;     // token chunks of the router-weight gradient's partial sums
   size_t total;
   size_t zero_bytes;  // bytes from `status` that every call clears (status word + split counters)
+  int T, K;
   int TK;             // T*K: rows of the compact grouped buffers
+  bool fuse_combine;  // the down GEMM's epilogue also forms y (unsplit tensor-core paths)
   int R;              // padded grouped rows (upper bound): T*K + E*(kSegPad-1), rounded up to kSegPad
   int S;              // split count over the contraction of the down projection
   int kb_per_split;
@@ -79,11 +81,15 @@ struct SplitPlan {
 SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, double part_ratio);
 // train: also lay out the saved pre-activations and the backward buffers
 // (and keep the gate/up contraction unsplit, which the saving epilogue needs).
-WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bool train = false);
+// routing_only: the caller runs the routing kernels only (no fused-combine
+// counters in front of the routing arrays).
+WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bool train = false,
+                   bool routing_only = false);
 
 struct Ptrs {
   int *status;
   int *tile_cnt;  // arrival counters of split gate/up tiles
+  int *tok_cnt;   // [T, down n-tiles] slot arrivals of the fused combine
   int32_t *idx;
   float *gate;
   int32_t *blockcounts, *offsets, *poffsets, *pos, *perm_tok;
@@ -125,8 +131,10 @@ cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, in
 // slot_of (host array of E entries, or null): expert e's matrices are slot
 // slot_of[e] of banks holding n_slots matrices each (the expert cache);
 // without it, slot e of banks of E.
+// y: the layer output, formed by the down GEMM's epilogue when L.fuse_combine
+// (then no combine kernel runs).
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
-                                     const WsLayout &L, const Ptrs &P, unsigned flags, int num_sms,
+                                     const WsLayout &L, const Ptrs &P, void *y, unsigned flags, int num_sms,
                                      cudaStream_t s, void *const *mid_event, const int *slot_of = nullptr,
                                      int n_slots = 0);
 
@@ -138,7 +146,7 @@ cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int 
 // gemm_tc.cu, e4m3 operands: gate/up GEMM, H quantisation, down GEMM
 cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
                                     const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
-                                    const Ptrs &P, unsigned flags, int num_sms, cudaStream_t s,
+                                    const Ptrs &P, void *y, unsigned flags, int num_sms, cudaStream_t s,
                                     void *const *mid_event);
 
 // -------- gemm_simt.cu (exact fp32 path)
@@ -147,8 +155,8 @@ cudaError_t launch_bwd_prep(const void *dy, int T, int d, int E, int K, int S, c
                             int num_sms, cudaStream_t s);
 // events (optional): recorded after each of the four products / after dx and after dWg
 cudaError_t launch_bwd_gemms(const void *W1, const void *W3, const void *W2, void *dW1, void *dW3, void *dW2, int d,
-                             int f, int E, bool accumulate, const WsLayout &L, const Ptrs &P, int num_sms,
-                             cudaStream_t s, void *const *events);
+                             int f, int E, bool accumulate, bool force_timeout, const WsLayout &L, const Ptrs &P,
+                             int num_sms, cudaStream_t s, void *const *events);
 cudaError_t launch_bwd_input(const void *x, const void *Wg, void *dx, void *dWg, int T, int d, int E, int K,
                              bool accumulate, const WsLayout &L, const Ptrs &P, int num_sms, cudaStream_t s,
                              void *const *events);

@@ -130,7 +130,7 @@ SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, do
   return best;
 }
 
-WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bool train) {
+WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bool train, bool routing_only) {
   WsLayout L{};
   L.train = train;
   const size_t eb = elem_bytes(dtype);
@@ -142,6 +142,8 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bo
     L.n_route_blocks = (T + L.route_tpb - 1) / L.route_tpb;
   }
   const long long TKl = static_cast<long long>(T) * K;
+  L.T = T;
+  L.K = K;
   L.TK = static_cast<int>(TKl);
   const long long touched = TKl < E ? TKl : E;
   const bool fp8 = dtype == MOE_FP8_E4M3;
@@ -184,6 +186,9 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bo
   // one arrival counter per (128-row m-tile, n-tile, 32-row quarter) of the split gate/up GEMM
   const size_t n_cnt = L.S_gu > 1 ? (R / kSegPad) * static_cast<size_t>((f + 127) / 128) * 4 : 0;
   L.tile_cnt = take(n_cnt * sizeof(int));
+  // fused combine: one slot-arrival counter per (token, 256-column tile of y)
+  L.fuse_combine = dtype != MOE_F32 && L.S == 1 && !routing_only;
+  L.tok_cnt = take(L.fuse_combine ? static_cast<size_t>(T) * ((d + 255) / 256) * sizeof(int) : 0);
   L.zero_bytes = o - L.status;
   L.idx = take(TK * 4);
   L.gate = take(TK * 4);
@@ -229,6 +234,7 @@ Ptrs carve(void *ws, const WsLayout &L) {
   Ptrs P;
   P.status = reinterpret_cast<int *>(b + L.status);
   P.tile_cnt = reinterpret_cast<int *>(b + L.tile_cnt);
+  P.tok_cnt = reinterpret_cast<int *>(b + L.tok_cnt);
   P.idx = reinterpret_cast<int32_t *>(b + L.idx);
   P.gate = reinterpret_cast<float *>(b + L.gate);
   P.blockcounts = reinterpret_cast<int32_t *>(b + L.blockcounts);
@@ -316,12 +322,12 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   if (err == cudaSuccess) err = mark(3);
   if (err == cudaSuccess) {
     if (dtype == MOE_BF16)
-      err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, flags, sms, s, events ? events + 4 : nullptr);
+      err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, y, flags, sms, s, events ? events + 4 : nullptr);
     else
       err = launch_expert_ffn_f32(W1, W3, W2, d, f, E, L, P, s, events ? events + 4 : nullptr);
   }
   if (err == cudaSuccess) err = mark(5);
-  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
+  if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
   if (err == cudaSuccess) err = mark(6);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -413,9 +419,9 @@ int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const
   cache->bytes_loaded += static_cast<long long>(n_loads) * 3 * static_cast<long long>(mat);
   cudaError_t err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
   if (err == cudaSuccess)
-    err = launch_expert_gemms_bf16(W1_dev, W3_dev, W2_dev, d, f, E, L, P, flags, sms, s, nullptr, cache->slot_of,
+    err = launch_expert_gemms_bf16(W1_dev, W3_dev, W2_dev, d, f, E, L, P, y, flags, sms, s, nullptr, cache->slot_of,
                                    cache->C);
-  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
+  if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -436,7 +442,7 @@ static int backward_impl(const void *x, const void *Wg, const void *W1, const vo
                          moe_stream_t stream, void *const *events) {
   int st = check_train_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
-  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS)) return MOE_ERR_INVALID_ARG;
+  if (flags & ~(MOE_ACCUMULATE | MOE_DEBUG_CHECKS | MOE_DEBUG_FORCE_TIMEOUT)) return MOE_ERR_INVALID_ARG;
   const bool acc = (flags & MOE_ACCUMULATE) != 0;
   if (!Wg || !W1 || !W3 || !W2 || !dWg || !dW1 || !dW3 || !dW2) return MOE_ERR_INVALID_ARG;
   if (!aligned16(Wg) || !aligned16(W1) || !aligned16(W3) || !aligned16(W2) || !aligned16(dWg) || !aligned16(dW1) ||
@@ -473,7 +479,8 @@ static int backward_impl(const void *x, const void *Wg, const void *W1, const vo
   if (err == cudaSuccess) err = launch_bwd_prep(dy, T, d, E, K, L.S, L, P, sms, s);
   if (err == cudaSuccess && events) err = cudaEventRecord(static_cast<cudaEvent_t>(events[1]), s);
   if (err == cudaSuccess)
-    err = launch_bwd_gemms(W1, W3, W2, dW1, dW3, dW2, d, f, E, acc, L, P, sms, s, events ? events + 2 : nullptr);
+    err = launch_bwd_gemms(W1, W3, W2, dW1, dW3, dW2, d, f, E, acc, (flags & MOE_DEBUG_FORCE_TIMEOUT) != 0, L, P,
+                           sms, s, events ? events + 2 : nullptr);
   if (err == cudaSuccess)
     err = launch_bwd_input(x, Wg, dx, dWg, T, d, E, K, acc, L, P, sms, s, events ? events + 6 : nullptr);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
@@ -546,9 +553,10 @@ static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, cons
   if (err == cudaSuccess) err = launch_gather_quant(x, T, d, E, L.R, P, sms, s);
   if (err == cudaSuccess) err = mark(3);
   if (err == cudaSuccess)
-    err = launch_expert_gemms_fp8(W1q, s1, W3q, s3, W2q, s2, d, f, E, L, P, flags, sms, s, events ? events + 4 : nullptr);
+    err = launch_expert_gemms_fp8(W1q, s1, W3q, s3, W2q, s2, d, f, E, L, P, y, flags, sms, s,
+                                  events ? events + 4 : nullptr);
   if (err == cudaSuccess) err = mark(5);
-  if (err == cudaSuccess) err = launch_combine(y, T, d, K, L.S, MOE_BF16, flags, P, sms, s);
+  if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, MOE_BF16, flags, P, sms, s);
   if (err == cudaSuccess) err = mark(6);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

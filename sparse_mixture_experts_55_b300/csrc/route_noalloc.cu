@@ -83,7 +83,7 @@ extern "C" int moe_route_noalloc(const void *x, const void *Wg, int T, int d, in
 
   // Only the routing part of the workspace layout is used: everything before
   // the grouped activation buffers.
-  const WsLayout L = ws_layout(T, d, dtype == MOE_BF16 ? 8 : 4, E, K, dtype, 148);
+  const WsLayout L = ws_layout(T, d, dtype == MOE_BF16 ? 8 : 4, E, K, dtype, 148, false, /*routing_only=*/true);
   if (L.xperm > kNoAllocBytes) return MOE_ERR_UNSUPPORTED;
   void *scratch = nullptr;
   if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;

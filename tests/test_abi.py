@@ -211,8 +211,8 @@ def test_training_entry_points_reject_bad_arguments(lib):
 
     assert bwd(dt=_lib.MOE_F32) == _lib.MOE_ERR_UNSUPPORTED
     assert bwd(dd=192 + 8) == _lib.MOE_ERR_UNSUPPORTED
-    assert bwd(flags=0x4) == _lib.MOE_ERR_INVALID_ARG       # no forced timeout on the backward
-    assert bwd(flags=0x8) == _lib.MOE_ERR_INVALID_ARG       # no GEMM form flags either
+    assert bwd(flags=0x8) == _lib.MOE_ERR_INVALID_ARG       # no GEMM form flags
+    assert bwd(flags=0x40) == _lib.MOE_ERR_INVALID_ARG
     assert bwd(dW1=0) == _lib.MOE_ERR_INVALID_ARG
     assert bwd(dx=0) == _lib.MOE_ERR_INVALID_ARG
     assert bwd(dy=0x8008) == _lib.MOE_ERR_INVALID_ARG      # misaligned

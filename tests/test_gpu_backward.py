@@ -166,3 +166,26 @@ def test_backward_empty_batch(moe, cuda_device):
     torch.cuda.synchronize()
     for t in grads[1:]:
         assert not t.any()
+
+
+def test_forced_timeout_is_reported_and_the_next_call_is_correct(moe):
+    # The dH product's MMA thread waits on a barrier nothing signals; after
+    # about a second the wait gives up, the CTAs drain their copies, free
+    # TMEM and exit, and the status word reads MOE_ERR_DEVICE_TIMEOUT.  The
+    # context stays usable: a clean call on the same workspace is correct.
+    T, d, f, E, K = 300, 256, 512, 8, 2
+    x, Wg, W1, W3, W2, dy = _case(T, d, f, E, K, 11)
+    dev = torch.device("cuda:0")
+    xs, Wgs, W1s, W3s, W2s, dys = (t.to(dev) for t in (x, Wg, W1, W3, W2, dy))
+    ws = moe.TrainWorkspace(T, d, f, E, K, torch.bfloat16, dev)
+    moe.moe_forward_train(xs, Wgs, W1s, W3s, W2s, K, ws)
+    moe.moe_backward(xs, Wgs, W1s, W3s, W2s, dys, K, ws, flags=moe.MOE_DEBUG_FORCE_TIMEOUT)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(ws) == moe._lib.MOE_ERR_DEVICE_TIMEOUT
+    moe.moe_forward_train(xs, Wgs, W1s, W3s, W2s, K, ws)  # clears the status word
+    g = moe.moe_backward(xs, Wgs, W1s, W3s, W2s, dys, K, ws)
+    torch.cuda.synchronize()
+    assert moe.moe_read_status(ws) == 0
+    ref = oracle.moe_layer_backward(x, Wg, W1, W3, W2, K, dy)
+    for gg, rr in ((g.dx, ref.dx), (g.dW1, ref.dW1), (g.dW2, ref.dW2)):
+        assert _errors(_np(gg), rr)[0] <= NORM_TOL
