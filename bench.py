@@ -306,16 +306,28 @@ class ClockSampler:
 
 # ---------------------------------------------------------------------------
 def setup_dist():
+    """Replicas: one process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE);
+    the process group only carries the timing barrier and the max-over-ranks
+    reduction (NCCL on GPUs, gloo on a host without CUDA)."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     local = int(os.environ.get("LOCAL_RANK", "0"))
     if world > 1:
         import torch.distributed as dist
-        torch.cuda.set_device(local)
-        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
     elif torch.cuda.is_available():
         torch.cuda.set_device(local)
     return world, rank, local
+
+
+def rank_seed(rank: int) -> int:
+    """Seed of a replica's token batch: every rank routes its own tokens
+    through the same model weights (drawn from the base seed)."""
+    return W.BASE_SEED + 1009 * rank
 
 
 def barrier(world):
@@ -336,7 +348,7 @@ def max_over_ranks(v: float, world: int, dev) -> float:
 def make_inputs(cfg_name: str, rank: int, dev, weights=None):
     c = CONFIGS[cfg_name]
     cfg_name = cfg_name.replace("_fp8", "")
-    seed = W.BASE_SEED + 1009 * rank     # replicas: own tokens per rank (same model weights)
+    seed = rank_seed(rank)  # replicas: own tokens per rank (same model weights)
     if weights is None:
         weights = W.mixtral_weights(c["d"], c["f"], c["E"], seed=W.BASE_SEED, device=dev)
     if cfg_name in ("prefill", "prefill_e2", "train", "train_e2"):
@@ -432,7 +444,8 @@ def run_reference_stack(args, world, c, dev, steps, warmup):
     value = n_tok / (ms / 1e3)
     sample = (f"{n_tok} tokens per step through layer 0's pre-norm block, time scaled by {L} layers "
               f"(weights upcast to float64 once, untimed)")
-    line = {"impl": "reference", "metric": TRAIN_METRIC if train else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    metric = TRAIN_METRIC if train else (CACHE_METRIC if "cache_slots" in c else METRIC)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.config], **c},
@@ -478,7 +491,8 @@ def run_reference(args, world, rank):
     value = n_tok / (ms / 1e3)
     threads = blas_threads()
     sample = f"{n_tok} tokens of the {args.config} batch per step (weights upcast to float64 once, untimed)"
-    line = {"impl": "reference", "metric": TRAIN_METRIC if train else METRIC, "value": value, "unit": "tokens/s", "n_gpus": world,
+    metric = TRAIN_METRIC if train else (CACHE_METRIC if "cache_slots" in c else METRIC)
+    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
             "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": WORKLOAD_TEXT[args.config], **c},
@@ -508,7 +522,7 @@ def oracle_block_rate(h_rows, layer_weights, K: int):
 
 def stack_inputs(c, rank, dev):
     layers = [W.stack_layer_weights(l, c["d"], c["f"], c["E"], device=dev) for l in range(c["layers"])]
-    h0 = W.stack_h0(c["T"], c["d"], seed=W.BASE_SEED + 1009 * rank, device=dev)
+    h0 = W.stack_h0(c["T"], c["d"], seed=rank_seed(rank), device=dev)
     return layers, h0
 
 
@@ -641,7 +655,7 @@ def run_ours_cache(args, world, rank, local):
     T, d, f, E, K, C = c["T"], c["d"], c["f"], c["E"], c["K"], c["cache_slots"]
     Wg, W1, W3, W2 = W.mixtral_weights(d, f, E, seed=W.BASE_SEED, device=dev)
     steps, warmup = args.steps, max(args.warmup, 3)
-    xs, _ = W.decode_trace(warmup + steps, Wg, T=T, keep=c["keep"], seed=W.BASE_SEED + 1009 * rank, device=dev)
+    xs, _ = W.decode_trace(warmup + steps, Wg, T=T, keep=c["keep"], seed=rank_seed(rank), device=dev)
     cache = moe.ExpertCache(W1, W3, W2, C, dev)
     ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
     y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
@@ -757,7 +771,7 @@ def run_ours_train(args, world, rank, local):
     c = CONFIGS[args.config]
     T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
     inp, _ = make_inputs(args.config, rank, dev)
-    dy = W.randn((T, d), 1.0, W.BASE_SEED + 77 + 1009 * rank, dev, torch.bfloat16)
+    dy = W.randn((T, d), 1.0, rank_seed(rank) + 77, dev, torch.bfloat16)
     stream = torch.cuda.current_stream(dev)
     steps, warmup = args.steps, max(args.warmup, 3)
     ws = moe.TrainWorkspace(T, d, f, E, K, torch.bfloat16, dev)

@@ -365,11 +365,15 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x
     }
     uint4 *dst = xperm + static_cast<size_t>(r) * vec_per_row;
     if (tok >= 0) {
+      // eight 16-byte loads per lane in flight (a 4096-wide bf16 row is 16 per lane)
       const uint4 *src = x + static_cast<size_t>(tok) * vec_per_row;
       int v = lane;
-      for (; v + 96 < vec_per_row; v += 128) {
-        uint4 a = __ldg(src + v), b = __ldg(src + v + 32), c = __ldg(src + v + 64), dd = __ldg(src + v + 96);
-        dst[v] = a; dst[v + 32] = b; dst[v + 64] = c; dst[v + 96] = dd;
+      for (; v + 224 < vec_per_row; v += 256) {
+        uint4 a[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) a[i] = __ldg(src + v + 32 * i);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) dst[v + 32 * i] = a[i];
       }
       for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
     } else {
