@@ -217,8 +217,10 @@ cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void
 
 cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const Ptrs &P, int num_sms,
                                 cudaStream_t s) {
-  // a block per row while the rows fit in one wave of blocks, else a warp per row
-  const bool block_team = R <= num_sms * 8;
+  // A block per row until there are enough rows to give every resident warp
+  // about half a row (prefill sizes); a lone warp per row is slow on the few,
+  // long rows of decode batches.
+  const bool block_team = R <= num_sms * 32;
   int blocks = block_team ? R : (R + 7) / 8;
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
@@ -230,7 +232,7 @@ cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const
 }
 
 cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
-  const bool block_team = R <= num_sms * 8;
+  const bool block_team = R <= num_sms * 32;  // as launch_gather_quant
   int blocks = block_team ? R : (R + 7) / 8;
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
