@@ -405,15 +405,37 @@ def blas_threads() -> int:
 
 def cpu_oracle_rate(inp, n_tokens: int):
     """Time the unchanged float64 oracle on the first n_tokens tokens of the batch.
-    Weights are copied to the host and upcast once, before timing."""
+    Weights are copied to the host and upcast once, before timing.  Returns
+    the rate, the time, the threads and the oracle's output on those tokens."""
     import numpy as np
     import oracle
     x = inp.x[:n_tokens].float().cpu().numpy().astype(np.float64)
     Wg, W1, W3, W2 = f64_banks(inp)
     t0 = time.perf_counter()
-    oracle.moe_layer(x, Wg, W1, W3, W2, inp.K)
+    ref = oracle.moe_layer(x, Wg, W1, W3, W2, inp.K)
     dt = time.perf_counter() - t0
-    return n_tokens / dt, dt, blas_threads()
+    return n_tokens / dt, dt, blas_threads(), ref.y
+
+
+def oracle_check(inp, idx_gpu, y_gpu, y_ref):
+    """The bench line's parity record: the GPU output on the oracle's sampled
+    tokens, and the routing of every token against the oracle's (tokens whose
+    K-th/(K+1)-th logit gap is below 1e-3 are counted as near ties, not
+    compared)."""
+    import numpy as np
+    import oracle
+    x = inp.x.float().cpu().numpy().astype(np.float64)
+    Wg = inp.Wg.float().cpu().numpy().astype(np.float64)
+    g = oracle.gating(x, Wg, inp.K)
+    gap_io, _ = oracle.logit_gaps(oracle.router_logits(x, Wg), inp.K)
+    near = (gap_io > 0) & (gap_io < 1e-3)
+    gpu = np.sort(np.asarray(idx_gpu), axis=1)
+    ref = np.sort(g.idx, axis=1)
+    mism = int(np.sum(np.any(gpu != ref, axis=1) & ~near))
+    y = np.asarray(y_gpu, dtype=np.float64)
+    err = float(np.abs(y - y_ref).max() / (np.abs(y_ref).max() + 1e-6))
+    return {"tokens_checked": int(y_ref.shape[0]), "max_rel_err": err, "tolerance": 2e-2,
+            "routing_tokens": int(x.shape[0]), "near_ties": int(near.sum()), "index_mismatches": mism}
 
 
 def run_reference_stack(args, world, c, dev, steps, warmup):
@@ -931,7 +953,7 @@ def run_ours(args, world, rank, local):
             moe.moe_forward_timed(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, evs, y=out, workspace=ws, stream=stream)
 
     # touched experts of this routing (algorithmic bytes at decode sizes)
-    _, _, _, offs, _ = moe.moe_route(inp.x, inp.Wg, K)
+    route_idx, _, _, offs, _ = moe.moe_route(inp.x, inp.Wg, K)
     counts = (offs[1:] - offs[:-1]).cpu()
     n_touched = int((counts > 0).sum())
 
@@ -1040,10 +1062,11 @@ def run_ours(args, world, rank, local):
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
         n_tok = min(T, args.cpu_tokens)
-        rate, dt, threads = cpu_oracle_rate(inp, n_tok)
+        rate, dt, threads, y_ref = cpu_oracle_rate(inp, n_tok)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {n_tok} tokens of the batch, float64 oracle ({dt:.1f} s; "
                                           f"weights upcast once, untimed)"}
+        line["parity"] = oracle_check(inp, route_idx.cpu().numpy(), y[:n_tok].float().cpu().numpy(), y_ref)
     if rank == 0:
         print(json.dumps(line), flush=True)
 
