@@ -56,3 +56,22 @@ def test_step_needing_more_experts_than_slots_is_refused(moe, cuda_device):
         cache.forward(x, Wg, K)
     assert ei.value.code == moe._lib.MOE_ERR_UNSUPPORTED
     assert cache.state.step == 0 and cache.state.misses == 0 and cache.state.bytes_loaded == 0
+
+
+def test_cached_forward_at_full_size(moe, cuda_device):
+    # Mixtral-sized banks (2.8 GB in pinned host memory), 2 of 8 experts on
+    # the GPU, six decode steps of the bench's locality trace: bit for bit
+    # moe_forward, decisions as the oracle policy's.
+    Wg, W1, W3, W2 = W.mixtral_weights(device=cuda_device)
+    E, K, C = 8, 2, 2
+    xs, _ = W.decode_trace(6, Wg, T=1, seed=W.BASE_SEED, device=cuda_device)
+    cache = moe.ExpertCache(W1, W3, W2, C, cuda_device)
+    ref = LRUCache(E, C)
+    for i in range(xs.shape[0]):
+        y = cache.forward(xs[i], Wg, K)
+        assert torch.equal(y, moe.moe_forward(xs[i], Wg, W1, W3, W2, K)), i
+        idx, *_ = moe.moe_route(xs[i], Wg, K)
+        ref.plan(sorted(set(idx.flatten().tolist())))
+        assert list(cache.state.slot_of)[:E] == ref.slot_of, i
+    assert (cache.state.hits, cache.state.misses) == (ref.hits, ref.misses)
+    assert cache.state.bytes_loaded == ref.misses * 3 * 4096 * 14336 * 2

@@ -136,6 +136,27 @@ def test_fp8_full_size_prefill_sampled_tokens(moe, cuda_device):
     assert err <= 2e-2
 
 
+def test_fp8_full_size_decode32_sampled_tokens(moe, cuda_device):
+    """The decode32_fp8 workload (32 tokens, split GEMMs), checked on the
+    tokens that chose the most common expert pair, as in the prefill case."""
+    Wg, W1, W3, W2 = W.mixtral_weights(device=cuda_device)
+    inp = W.decode(32, device=cuda_device, weights=(Wg, W1, W3, W2))
+    q = [t for B in (W1, W3, W2) for t in moe.quantize_weights_fp8(B)]
+    y = moe.moe_forward_fp8(inp.x, Wg, *q, 2)
+    x = inp.x.cpu()
+    g = oracle.gating(x, Wg.cpu(), 2)
+    pairs = [tuple(sorted(r)) for r in g.idx.tolist()]
+    gap, _ = oracle.logit_gaps(oracle.router_logits(oracle.f64(x), oracle.f64(Wg.cpu())), 2)
+    pairs = [p if gap[t] > 1e-4 else None for t, p in enumerate(pairs)]
+    a, b = max(set(p for p in pairs if p), key=pairs.count)
+    toks = [t for t, p in enumerate(pairs) if p == (a, b)]
+    banks = [t for B in (W1, W3, W2) for t in F8.quantize_weight_columns(B[[a, b]].cpu())]
+    ref = F8.moe_layer_fp8(x[toks], Wg.cpu()[:, [a, b]], *banks, 2)
+    err = parity.rel_linf(_np(y[toks].float()), ref.y)
+    print(f"\nfp8 full-size decode T=32: experts {[a, b]}, tokens {toks}, rel err {err:.2e}")
+    assert err <= 2e-2
+
+
 @pytest.mark.parametrize("T,d,f,E,K", [(1100, 512, 1024, 4, 2), (700, 256, 384, 2, 1)])
 def test_fp8_gemm_forms_agree_bit_for_bit(moe, T, d, f, E, K):
     x, Wg, W1, W3, W2 = _fp8_case(T, d, f, E, K, seed=60 + T)
