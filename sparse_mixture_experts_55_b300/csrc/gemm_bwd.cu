@@ -137,7 +137,9 @@ __device__ __forceinline__ BTile decode_tile(int u, const Ctrl &c, const BwdArgs
   return t;
 }
 
-__device__ __forceinline__ float sigmoid_f(float v) { return 1.0f / (1.0f + __expf(-v)); }
+// Logistic function with the fast reciprocal division (a few fp32 ulps; its
+// results are rounded to bf16).
+__device__ __forceinline__ float sigmoid_f(float v) { return __fdividef(1.0f, 1.0f + __expf(-v)); }
 
 // The epilogue holds a 32 x 32 block as one row per lane (what tcgen05.ld
 // 32x32b returns); global memory wants each instruction to cover whole row
@@ -177,45 +179,52 @@ __device__ __forceinline__ void load_segments_bf16(const __nv_bfloat16 *src, siz
   for (int k = 0; k < 4; ++k) w[k] = *reinterpret_cast<const uint4 *>(src + (8 * k + (lane >> 2)) * ld + 8 * (lane & 3));
 }
 
-// The block loaded by load_segments_bf16 as fp32, one row per lane.
-__device__ __forceinline__ void segments_to_rows(float *st, const uint4 (&w)[4], float (&v)[32], int lane) {
-  const int cq = 8 * (lane & 3);
+// bf16 blocks move through the staging tile as 16-byte pieces, rows
+// ROW_BYTES apart (80: every 8 lanes of a row-per-lane access hit distinct
+// banks).
+constexpr int ROW_BYTES = 80;
+static_assert(32 * ROW_BYTES <= EPI_WARP_BYTES, "bf16 staging tile");
+
+// The block loaded by load_segments_bf16 as fp32, one row (32 columns) per lane.
+__device__ __forceinline__ void segments_to_rows(uint8_t *st, const uint4 (&w)[4], float (&v)[32], int lane) {
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const int r = 8 * k + (lane >> 2);
-    const uint32_t ws[4] = {w[k].x, w[k].y, w[k].z, w[k].w};
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ws[j]));
-      st[r * STAGE_PITCH + cq + 2 * j] = f2.x;
-      st[r * STAGE_PITCH + cq + 2 * j + 1] = f2.y;
-    }
-  }
+  for (int k = 0; k < 4; ++k)
+    *reinterpret_cast<uint4 *>(st + (8 * k + (lane >> 2)) * ROW_BYTES + 16 * (lane & 3)) = w[k];
   __syncwarp();
 #pragma unroll
-  for (int c = 0; c < 32; ++c) v[c] = st[lane * STAGE_PITCH + c];
+  for (int j = 0; j < 4; ++j) {
+    const uint4 r = *reinterpret_cast<const uint4 *>(st + lane * ROW_BYTES + 16 * j);
+    const uint32_t rw[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&rw[i]));
+      v[8 * j + 2 * i] = f2.x;
+      v[8 * j + 2 * i + 1] = f2.y;
+    }
+  }
   __syncwarp();
 }
 
 // v (one row per lane) to bf16 rows 0..31 at dst + r * ld, rounded to nearest
-// even: every instruction writes eight 64-byte row segments.
-__device__ __forceinline__ void store_block_bf16(float *st, const float (&v)[32], __nv_bfloat16 *dst, size_t ld,
+// even: every store instruction writes eight 64-byte row segments.
+__device__ __forceinline__ void store_block_bf16(uint8_t *st, const float (&v)[32], __nv_bfloat16 *dst, size_t ld,
                                                  int lane) {
 #pragma unroll
-  for (int c = 0; c < 32; ++c) st[lane * STAGE_PITCH + c] = v[c];
+  for (int j = 0; j < 4; ++j) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __nv_bfloat162 h = __floats2bfloat162_rn(v[8 * j + 2 * i], v[8 * j + 2 * i + 1]);
+      w[i] = *reinterpret_cast<const uint32_t *>(&h);
+    }
+    *reinterpret_cast<uint4 *>(st + lane * ROW_BYTES + 16 * j) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
   __syncwarp();
-  const int cq = 8 * (lane & 3);
 #pragma unroll
   for (int k = 0; k < 4; ++k) {
     const int r = 8 * k + (lane >> 2);
-    const float *sr = st + r * STAGE_PITCH + cq;
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      const __nv_bfloat162 h = __floats2bfloat162_rn(sr[2 * j], sr[2 * j + 1]);
-      w[j] = *reinterpret_cast<const uint32_t *>(&h);
-    }
-    *reinterpret_cast<uint4 *>(dst + r * ld + cq) = make_uint4(w[0], w[1], w[2], w[3]);
+    *reinterpret_cast<uint4 *>(dst + r * ld + 8 * (lane & 3)) =
+        *reinterpret_cast<const uint4 *>(st + r * ROW_BYTES + 16 * (lane & 3));
   }
   __syncwarp();
 }
@@ -380,7 +389,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // ------------------------------------------------------------ epilogue
     const int q = warp & 3;
-    float *stage_tile = reinterpret_cast<float *>(reinterpret_cast<uint8_t *>(&c) + 1024 + q * EPI_WARP_BYTES);
+    uint8_t *stage_bytes = reinterpret_cast<uint8_t *>(&c) + 1024 + q * EPI_WARP_BYTES;  // 16-byte aligned
+    float *stage_tile = reinterpret_cast<float *>(stage_bytes);
     int local = 0;
     for (int u = blockIdx.x; u < total; u += gridDim.x) {
       const BTile t = decode_tile<KIND>(u, c, args);
@@ -413,8 +423,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           uint32_t v[32];
           ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
           float a[32], b[32];
-          segments_to_rows(stage_tile, wa, a, lane);
-          segments_to_rows(stage_tile, wb, b, lane);
+          segments_to_rows(stage_bytes, wa, a, lane);
+          segments_to_rows(stage_bytes, wb, b, lane);
           if (cc + 1 < BN / 32 && col + 32 < args.n_out) {
             load_segments_bf16(pa + col + 32, rstride, wa, lane);
             load_segments_bf16(pa + args.f + col + 32, rstride, wb, lane);
@@ -430,8 +440,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             b[j] = dh * a[j] * sg;
             a[j] = da;
           }
-          store_block_bf16(stage_tile, a, pd + col, rstride, lane);
-          store_block_bf16(stage_tile, b, pd + args.f + col, rstride, lane);
+          store_block_bf16(stage_bytes, a, pd + col, rstride, lane);
+          store_block_bf16(stage_bytes, b, pd + args.f + col, rstride, lane);
         }
       } else if (KIND == KIND_DGRAD_X) {
         // real rows (a prefix of the segment) to their unpadded grouped rows;
