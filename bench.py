@@ -104,19 +104,30 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
+def code_sha256(path: pathlib.Path) -> str:
+    """sha256 of a C++/CUDA source with its // comments, trailing blanks and
+    empty lines removed: it changes when the code does, not when a comment
+    does (the kernel sources hold no // inside string literals)."""
+    lines = []
+    for line in path.read_text().splitlines():
+        code = line.split("//", 1)[0].rstrip()
+        if code:
+            lines.append(code)
+    return hashlib.sha256("\n".join(lines).encode()).hexdigest()
+
+
 def traffic_from_profiles(kernel_file: pathlib.Path, key: str, summary: str = "gate_up_gemm_traffic.md"):
     """dram bytes per launch recorded by an ncu capture (profiles/<summary>), if
-    the kernel source is unchanged since."""
+    the kernel's code is unchanged since (code_sha256)."""
     prof = ROOT / "profiles" / summary
     if not prof.exists():
         return None
     text = prof.read_text()
-    m_sha = re.search(r"source_sha256:\s*([0-9a-f]{64})", text)
+    m_sha = re.search(r"code_sha256:\s*([0-9a-f]{64})", text)
     m_val = re.search(rf"{key}:\s*([0-9.eE+]+)", text)
     if not m_sha or not m_val:
         return None
-    sha = hashlib.sha256(kernel_file.read_bytes()).hexdigest()
-    return float(m_val.group(1)) if sha == m_sha.group(1) else None
+    return float(m_val.group(1)) if code_sha256(kernel_file) == m_sha.group(1) else None
 
 
 class _CtypesNVML:

@@ -1,17 +1,21 @@
-// gemm_tc.cu -- the two grouped expert GEMMs of the bf16 path on 5th-generation
-// tensor cores (tcgen05.mma, accumulators in TMEM, operands staged by TMA).
+// gemm_tc.cu -- the two grouped expert GEMMs of the forward pass on
+// 5th-generation tensor cores (tcgen05.mma, accumulators in TMEM, operands
+// staged by TMA), for bf16 weights and for e4m3 weights (FP8).
 //
 //   gate/up:  for each expert e and its grouped rows X_e (padded segment of
 //             X_perm):  H_e = SiLU(X_e W1[e]) (.) (X_e W3[e])      (bf16 out)
-//   down:     O_e = gate (.) (H_e W2[e]), fp32, optionally split over K
+//   down:     O_e = gate (.) (H_e W2[e]), fp32, optionally split over K; when
+//             not split, the epilogue also adds each token's K slot rows and
+//             stores y (the combine)
 //             ("Expert Network Structure (SwiGLU)" and the gate-weighted sum of
 //             section 3.4 "MoE Layer Formulation", Mixtral of Experts summary
 //             pages).
 //
-// One persistent kernel per GEMM, launched as clusters of two CTAs (one CTA
-// of 192 threads per SM), in one of two forms chosen per call:
+// One persistent kernel per GEMM, launched as clusters (one CTA of 192
+// threads per SM), in one of three forms chosen per call (all compute every
+// tile in the same order, so their results are bitwise identical):
 //
-// Pair MMA (PAIR = true; batches with at least two 128-row tiles per expert):
+// Pair MMA (FORM_PAIR; default once experts average 16 or more 128-row tiles):
 //   the two CTAs run one 256x256 tile together with tcgen05.mma.cta_group::2:
 //   rows 128r..128r+127 come from CTA r's A tile and CTA r holds half of the
 //   256 B columns, so each CTA stages 16 KiB of A and 16 KiB of B per
@@ -21,10 +25,10 @@
 //   commits release the stage (and hand the accumulator to the epilogue) in
 //   both CTAs.  An expert with an odd tile count pairs its last tile with a
 //   phantom tile whose rows are computed but never stored.
-// Multicast pairs (PAIR = false; decode-sized batches): each CTA computes
-//   its own 128x256 tile with cta_group::1 MMAs; the two CTAs work on a pair
-//   of tiles that share an operand, and each loads half of the shared
-//   operand and multicasts it to both:
+// Multicast pairs (FORM_MC2; default below that): each CTA computes its own
+//   128x256 tile with cta_group::1 MMAs; the two CTAs work on a pair of
+//   tiles that share an operand, and each loads half of the shared operand
+//   and multicasts it to both:
 //   M-pair  tiles (m, n) and (m+1, n) of one expert share the 64x256 weight
 //           tile: each CTA loads its own 128x64 A tile and two of the four
 //           64-column B boxes, multicast (32 KiB per CTA per k-block
@@ -33,17 +37,23 @@
 //           (m, n) and (m, n+1) share the A tile: each CTA loads 64 of its
 //           128 rows multicast and its own B tile.
 //   A stage is refilled only after both CTAs' MMAs have read it (4 stages).
+// 2x2 multicast (FORM_MC4; MOE_GEMM_QUAD only): 4-CTA clusters, CTA (i, j)
+//   runs tile (2p+i, 2q+j); rows share A and columns share B, each CTA
+//   loading half of both.
 // Roles per CTA:
 //   warp 0      TMA producer (one elected thread), shared-memory ring
-//               (A 128x64 K-major, B in 64x64 N-major boxes since the
-//               weights are stored [E, K, N]; 128-byte swizzle);
+//               (A 128x64 K-major; bf16 B in 64x64 N-major boxes since the
+//               weights are stored [E, K, N], e4m3 B K-major; 128-byte
+//               swizzle); weight banks are addressed by slot (wslot[e]) so
+//               that an expert cache can hold them in any order;
 //   warp 1      TMEM allocator + MMA issuer (one thread) into one of two
 //               256-column accumulators;
 //   warps 2..5  epilogue: tcgen05.ld of their 32-lane quarter, SwiGLU or gate
 //               scale, global stores; the second accumulator lets the next
 //               tile's MMAs run under this tile's epilogue.
 // For gate/up the 256 accumulator columns hold 128 columns of X W1 followed by
-// the same 128 columns of X W3, so one MMA feeds both SwiGLU branches.
+// the same 128 columns of X W3, so one MMA feeds both SwiGLU branches.  The
+// training forward also stores a = X W1 and b = X W3 (save_ab).
 //
 // Every mbarrier wait is bounded (about one second); on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, stops issuing work, waits (again
