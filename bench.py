@@ -660,7 +660,8 @@ def run_ours_stack(args, world, rank, local):
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h0_host.numel() * h0_host.element_size(),
                 "d2h_bytes_per_step": h_host.numel() * h_host.element_size()},
-        "gpu_launches": 7 * L * steps,
+        # per layer: RMSNorm, then the layer's kernels
+        "gpu_launches": (1 + moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16)) * L * steps,
         "stage_timing": "separate pass of one step with RMSNorm and library-recorded stage events per layer",
         "clocks": clk.summary(),
     }
@@ -769,7 +770,7 @@ def run_ours_cache(args, world, rank, local):
                      "peak_source": "pinned host-to-device copy of one 117 MB expert matrix, timed in this run"},
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
-        "gpu_launches": 6 * steps,
+        "gpu_launches": moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16) * steps,
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -907,7 +908,7 @@ def run_ours_train(args, world, rank, local):
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
                 "d2h_bytes_per_step": dx_h.numel() * dx_h.element_size()},
-        "gpu_launches": 14 * steps,
+        "gpu_launches": (moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16) + 8) * steps,
         "stage_timing": "separate pass of the same steps with library-recorded backward stage events",
         "clocks": clk.summary(),
     }
@@ -1067,7 +1068,8 @@ def run_ours(args, world, rank, local):
         "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
-        "gpu_launches": (7 if fp8 else 6) * steps,
+        "gpu_launches": moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_FP8_E4M3 if fp8 else moe.MOE_BF16)
+        * steps,
         "stage_timing": "separate pass of the same K forwards with library-recorded stage events",
         "clocks": clk.summary(),
     }

@@ -109,6 +109,15 @@ enum { MOE_BF16 = 0, MOE_F32 = 1, MOE_FP8_E4M3 = 2 };
 MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype);
 
 /*
+ * Number of kernels one moe_forward (dtype MOE_BF16 or MOE_F32) or
+ * moe_forward_fp8 (dtype MOE_FP8_E4M3) call with these sizes enqueues: 5 when
+ * the down GEMM's epilogue forms y (bf16 and e4m3 calls whose down projection
+ * is not split over its contraction), 6 otherwise, one more for e4m3 (the H
+ * quantiser); 0 for T = 0 or invalid sizes.  Host only.
+ */
+MOE_API int moe_forward_launches(int T, int d, int f, int E, int K, int dtype);
+
+/*
  * The MoE layer forward pass: y = sum over the K selected experts of
  * gate * SwiGLU_expert(x) (section 3.4 "MoE Layer Formulation", output
  * combination; "Expert Network Structure (SwiGLU)").

@@ -50,6 +50,7 @@ _cp = ctypes.POINTER(ExpertCacheState)
 
 SIGNATURES = {
     "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
+    "moe_forward_launches": (_i, [_i, _i, _i, _i, _i, _i]),
     "moe_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
     "moe_forward_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp, _vp]),
     "moe_block_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _sz, _u,

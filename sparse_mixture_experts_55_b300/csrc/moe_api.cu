@@ -425,6 +425,15 @@ int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+int moe_forward_launches(int T, int d, int f, int E, int K, int dtype) {
+  if (check_shape(T, d, f, E, K, dtype) != MOE_OK) return 0;
+  if (T == 0) return 0;
+  const WsLayout L = ws_layout(T, d, f, E, K, dtype, sm_count_or_default());
+  // route, group, gather (e4m3: gather + quantise), the two expert GEMMs (e4m3:
+  // plus the H quantiser), and the combine unless the down GEMM forms y
+  return 5 + (dtype == MOE_FP8_E4M3 ? 1 : 0) + (L.fuse_combine ? 0 : 1);
+}
+
 size_t moe_train_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
   if (check_train_shape(T, d, f, E, K, dtype) != MOE_OK) return 0;
   return ws_layout(T, d, f, E, K, dtype, sm_count_or_default(), true).total;

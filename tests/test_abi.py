@@ -32,6 +32,7 @@ def test_header_declares_the_boundary():
                             "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_timed",
                             "moe_train_workspace_bytes", "moe_forward_train", "moe_backward", "moe_backward_timed",
                             "moe_expert_cache_init", "moe_expert_cache_plan", "moe_forward_cached",
+                            "moe_forward_launches",
                             "moe_route_noalloc", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
@@ -241,3 +242,16 @@ def test_cached_forward_rejects_bad_arguments(lib):
     assert fwd(ws=0) == _lib.MOE_ERR_WORKSPACE
     assert fwd(ws_bytes=64) == _lib.MOE_ERR_WORKSPACE
     assert st.step == 0
+
+
+def test_forward_launch_counts(lib):
+    # prefill: the down projection is not split, so its epilogue forms y
+    assert lib.moe_forward_launches(4096, 4096, 14336, 8, 2, _lib.MOE_BF16) == 5
+    assert lib.moe_forward_launches(4096, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 6
+    # one token: split down projection, separate combine
+    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_BF16) == 6
+    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 7
+    # fp32: two SIMT FFN kernels and the combine
+    assert lib.moe_forward_launches(64, 64, 128, 8, 2, _lib.MOE_F32) == 6
+    assert lib.moe_forward_launches(0, 64, 128, 8, 2, _lib.MOE_BF16) == 0
+    assert lib.moe_forward_launches(16, 63, 128, 8, 2, _lib.MOE_BF16) == 0
