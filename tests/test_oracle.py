@@ -14,6 +14,10 @@
 | tie-break              | exact rational arithmetic (fractions.Fraction) on tie tokens     |
 | RMSNorm                | closed form on a 3-4-5 row; torch.nn.functional.rms_norm         |
 | shapes / params        | 3*4096*14336 = 176,160,768 per expert; 45.1B over 32 layers      |
+| logit_gaps             | hand-built rows with known order statistics (exact ties too);    |
+|                        | the gap as min over the kept logits minus max over the rest      |
+| moe_layer_tokens       | the full layer's rows at the same tokens (unsorted, repeated)    |
+| moe_block (pre-norm)   | hand-derived two-token block example (tests/golden)              |
 
 The mutation tests at the end plant plausible mistakes in the oracle (on the
 CPU) and check that at least one pin fails for each.
@@ -23,6 +27,7 @@ from __future__ import annotations
 import json
 import math
 import pathlib
+import re
 from fractions import Fraction
 
 import numpy as np
@@ -220,10 +225,84 @@ def pin_param_accounting():
     assert Wg.shape == (64, 8) and W1.shape == (8, 64, 96) and W2.shape == (8, 96, 64)
 
 
+def pin_logit_gaps():
+    # hand-built rows: (sorted values) -> (K-th minus (K+1)-th, 1st minus 2nd)
+    rows = np.array([[1.0, 2.0, 4.0, 0.5, 3.0],     # 4 > 3 > 2 > 1 > .5
+                     [5.0, 3.0, 3.0, 1.0, -2.0],    # tie between the 2nd and 3rd
+                     [2.0, 2.0, 1.0, 0.0, 0.0],     # tie between the 1st and 2nd
+                     [-1.0, -1.0, -1.0, -1.0, -1.0],
+                     [0.0, 10.0, -10.0, 7.5, 7.25]])
+    gio, g12 = oracle.logit_gaps(rows, 2)
+    assert gio.tolist() == [1.0, 0.0, 1.0, 0.0, 0.25]
+    assert g12.tolist() == [1.0, 2.0, 0.0, 0.0, 2.5]
+    gio1, g121 = oracle.logit_gaps(rows, 1)
+    assert gio1.tolist() == [1.0, 2.0, 0.0, 0.0, 2.5]
+    assert np.isinf(g121).all()
+    gio3, _ = oracle.logit_gaps(rows, 3)
+    assert gio3.tolist() == [1.0, 2.0, 1.0, 0.0, 7.25]
+    # K = n: nothing is left out, so the gap is undefined
+    assert np.isinf(oracle.logit_gaps(rows[:, :2], 2)[0]).all()
+    # a second characterisation: the smallest kept logit minus the largest
+    # logit left out, and the two kept logits' difference, with the kept set
+    # from the (pinned) TopK
+    rng = np.random.default_rng(13)
+    for E, K in [(8, 2), (8, 1), (5, 3)]:
+        logits = rng.integers(-4, 5, size=(400, E)).astype(np.float64) / 4.0
+        idx = oracle.topk_indices(logits, K)
+        gio, g12 = oracle.logit_gaps(logits, K)
+        for t in range(logits.shape[0]):
+            kept = set(idx[t].tolist())
+            want = min(logits[t, i] for i in kept) - max(logits[t, j] for j in range(E) if j not in kept)
+            assert gio[t] == want
+            if K >= 2:
+                assert g12[t] == logits[t, idx[t, 0]] - logits[t, idx[t, 1]]
+
+
+def pin_layer_tokens_restriction():
+    inp = _tiny()
+    full = oracle.moe_layer(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, inp.K)
+    for tokens in ([5, 0, 63, 5, 17], [63], list(range(64))[::-3]):
+        sub = oracle.moe_layer_tokens(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, inp.K, tokens)
+        assert sub.y.shape == (len(tokens), full.y.shape[1])
+        assert np.abs(sub.y - full.y[tokens]).max() <= 1e-13 * np.abs(full.y).max()
+        assert (sub.gating.idx == full.gating.idx[tokens]).all()
+        assert np.allclose(sub.gating.gate, full.gating.gate[tokens], rtol=0, atol=1e-15)
+
+
+_LN3_TERM = re.compile(r"^\s*([+-]?\s*[0-9.]+)?\s*(\*\s*ln3)?\s*$")
+
+
+def _ln3_expr(v) -> float:
+    """Value of a golden-file entry: a number, or a sum of terms 'c' and 'c*ln3'."""
+    if not isinstance(v, str):
+        return float(v)
+    total = 0.0
+    for term in re.findall(r"[+-]?[^+-]+", v.replace(" ", "")):
+        m = _LN3_TERM.match(term)
+        assert m, f"bad golden term {term!r}"
+        coef = float(m.group(1).replace(" ", "")) if m.group(1) not in (None, "+", "-") else \
+            (-1.0 if m.group(1) == "-" else 1.0)
+        total += coef * (math.log(3.0) if m.group(2) else 1.0)
+    return total
+
+
+def pin_block_hand_example():
+    b = json.loads((GOLDEN / "block_example.json").read_text())
+    conv = lambda a: np.vectorize(_ln3_expr, otypes=[np.float64])(np.array(a, dtype=object))
+    h, Wg, W1, W3, W2 = (conv(b[k]) for k in ("h", "Wg", "W1", "W3", "W2"))
+    assert np.allclose(oracle.rmsnorm(h, eps=b["eps"]), conv(b["expected_xnorm"]), rtol=0, atol=1e-15)
+    g = oracle.gating(oracle.rmsnorm(h, eps=b["eps"]), Wg, b["K"])
+    assert g.idx.tolist() == b["expected_idx"]
+    assert np.allclose(g.gate, b["expected_gate"], rtol=0, atol=1e-15)
+    out = oracle.moe_block(h, Wg, W1, W3, W2, b["K"], eps=b["eps"])
+    assert np.allclose(out, conv(b["expected_out"]), rtol=0, atol=1e-13)
+
+
 PINS = [pin_gate_closed_form, pin_gate_invariants, pin_topk_bruteforce, pin_routed_equals_dense,
         pin_expert_library, pin_silu_library, pin_k1_reduces_to_swiglu, pin_hand_example,
         pin_linearity_and_equivariance, pin_permutation_bruteforce, pin_rmsnorm,
-        pin_tie_tokens_exact, pin_param_accounting]
+        pin_tie_tokens_exact, pin_param_accounting, pin_logit_gaps, pin_layer_tokens_restriction,
+        pin_block_hand_example]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -306,9 +385,49 @@ def _moe_layer_swapped_gates(x, Wg, W1, W3, W2, K):
     return OM.LayerResult(y, g)
 
 
+def _gaps_first_minus_third(logits, K):
+    s = -np.sort(-logits, axis=1)
+    T, E = logits.shape
+    gap_in_out = s[:, 0] - s[:, K] if E > K else np.full(T, np.inf)
+    gap_12 = s[:, 0] - s[:, 1] if (K >= 2 and E >= 2) else np.full(T, np.inf)
+    return gap_in_out, gap_12
+
+
+def _gaps_off_by_one(logits, K):
+    s = -np.sort(-logits, axis=1)
+    T, E = logits.shape
+    gap_in_out = s[:, K] - s[:, K + 1] if E > K + 1 else np.full(T, np.inf)
+    gap_12 = s[:, 0] - s[:, 1] if (K >= 2 and E >= 2) else np.full(T, np.inf)
+    return gap_in_out, gap_12
+
+
+def _layer_tokens_first_n(x, Wg, W1, W3, W2, K, tokens):
+    return OM.moe_layer(OM.f64(x)[:len(tokens)], Wg, W1, W3, W2, K)
+
+
+def _layer_tokens_sorted(x, Wg, W1, W3, W2, K, tokens):
+    return OM.moe_layer(OM.f64(x)[np.sort(np.asarray(tokens))], Wg, W1, W3, W2, K)
+
+
+def _block_residual_before_norm(h, Wg, W1, W3, W2, K, eps=1e-5):
+    # post-norm: the residual sum is normalised instead of the block input
+    h64 = OM.f64(h)
+    return OM.rmsnorm(h64 + OM.moe_layer(h64, Wg, W1, W3, W2, K).y, eps)
+
+
+def _block_residual_of_normed(h, Wg, W1, W3, W2, K, eps=1e-5):
+    n = OM.rmsnorm(OM.f64(h), eps)
+    return n + OM.moe_layer(n, Wg, W1, W3, W2, K).y
+
+
+def _block_no_norm(h, Wg, W1, W3, W2, K, eps=1e-5):
+    h64 = OM.f64(h)
+    return h64 + OM.moe_layer(h64, Wg, W1, W3, W2, K).y
+
+
 _ORIG = {name: getattr(OM, name) for name in
          ("silu", "expert", "topk_indices", "topk_mask", "softmax", "router_logits", "permutation",
-          "rmsnorm", "moe_layer")}
+          "rmsnorm", "moe_layer", "logit_gaps", "moe_layer_tokens", "moe_block")}
 
 MUTANTS = {
     "silu_wrong_sign": ("silu", _silu_wrong_sign),
@@ -323,6 +442,13 @@ MUTANTS = {
     "permutation_unstable": ("permutation", _perm_unstable),
     "rmsnorm_no_sqrt": ("rmsnorm", _rmsnorm_no_sqrt),
     "combine_gates_swapped": ("moe_layer", _moe_layer_swapped_gates),
+    "gaps_first_minus_third": ("logit_gaps", _gaps_first_minus_third),
+    "gaps_off_by_one": ("logit_gaps", _gaps_off_by_one),
+    "layer_tokens_first_n": ("moe_layer_tokens", _layer_tokens_first_n),
+    "layer_tokens_sorted": ("moe_layer_tokens", _layer_tokens_sorted),
+    "block_residual_before_norm": ("moe_block", _block_residual_before_norm),
+    "block_residual_of_normed": ("moe_block", _block_residual_of_normed),
+    "block_no_norm": ("moe_block", _block_no_norm),
 }
 
 
