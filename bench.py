@@ -1,22 +1,27 @@
-"""Benchmark of the MoE layer forward on B300: one JSON line on rank 0.
+"""Benchmark of the MoE layer forward on one B300: one JSON line.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--config prefill] [--impl ours|reference]
+    python bench.py [--gpus 1] [--steps K] [--warmup W] [--config prefill] [--impl ours|reference]
 
 A step is one full forward pass of the layer (router, grouping, gather,
 gate/up GEMM + SwiGLU, down GEMM x gate, combine) over one batch of seeded
 synthetic tokens, with random-init Mixtral-shaped weights resident in HBM.
+The run uses one GPU from one process; multi-process launches are refused.
 
-  value        tokens/s over all ranks (each rank runs its own replica of the
-               layer on its own batch; no data-path collective), device-timed
-               with CUDA events around K steps, max over ranks
+  value        tokens/s, device-timed with CUDA events around K back-to-back
+               forwards
+  stages_ms    each kernel's span inside that same region, from the
+               global-timer stamps every kernel writes (moe_forward_stamped)
+  roofline     the gate/up expert GEMM (the dominant kernel): algorithmic
+               FLOPs (or bytes at decode sizes) per launch over its in-run
+               span, against MEASURED_PEAKS.json (burst or sustained peak as
+               the run's own clocks say)
+  decode       (prefill line) the decode batch sizes 1, 8, 32, 128 through the
+               same weights: ms per step and achieved HBM bandwidth of the
+               layer and of each expert GEMM
   e2e          the same metric through the C ABI with host buffers: pinned x
                copied in, the layer, y copied out, every step
-  roofline     the gate/up expert GEMM (the dominant kernel): algorithmic
-               FLOPs (or bytes at decode sizes) per launch over its average
-               launch time, measured by events recorded around it in the
-               timed region, against MEASURED_PEAKS.json
   cpu_baseline the float64 oracle on a token sample, timed on the host cores
-  --impl reference   the oracle alone, timed on the host cores (rank 0)
+  --impl reference   the oracle alone, timed on the host cores
 """
 from __future__ import annotations
 
@@ -316,58 +321,62 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------
-def setup_dist():
-    """Replicas: one process per GPU (torchrun's RANK / LOCAL_RANK / WORLD_SIZE);
-    the process group only carries the timing barrier and the max-over-ranks
-    reduction (NCCL on GPUs, gloo on a host without CUDA)."""
+def launch_rank(args) -> int:
+    """This benchmark drives one GPU from one process.  The layer shards by
+    tokens with no exchange, so N GPUs would be N independent replicas; this
+    build runs none: the expert GEMMs use cluster multicast, which is for
+    one-GPU calls only.  A multi-process launch (WORLD_SIZE > 1) or --gpus
+    other than 1 is refused for our arm.  The reference arm (the oracle on the
+    host cores, no GPU kernel of this library) runs on rank 0 of such a launch
+    and the other ranks exit without work.  Returns this process's rank."""
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        import torch.distributed as dist
-        if torch.cuda.is_available():
-            torch.cuda.set_device(local)
-            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
-        else:
-            dist.init_process_group("gloo")
-    elif torch.cuda.is_available():
-        torch.cuda.set_device(local)
-    return world, rank, local
+    if args.impl == "reference":
+        return rank
+    if world != 1 or args.gpus != 1:
+        sys.stderr.write(f"bench.py: refusing --gpus {args.gpus} with WORLD_SIZE={world}: this build runs one GPU "
+                         "per process and no multi-GPU path\n")
+        sys.exit(2)
+    return rank
 
 
-def rank_seed(rank: int) -> int:
-    """Seed of a replica's token batch: every rank routes its own tokens
-    through the same model weights (drawn from the base seed)."""
-    return W.BASE_SEED + 1009 * rank
+def tensor_peak(peaks, clocks, ratio: float = 1.0):
+    """The tensor roofline that matches the run's own clocks: the burst peak
+    when the median SM clock under load stayed within 3% of its maximum with no
+    power-cap event, else the sustained (power-capped) peak.  ratio scales the
+    measured bf16 figures (2 for e4m3, the nominal dense-rate ratio).  Returns
+    (peak, kind, reason)."""
+    sm, mx = clocks.get("sm_mhz"), clocks.get("sm_max_mhz")
+    capped = "sw_power_cap" in (clocks.get("reasons") or [])
+    if sm and mx and sm >= 0.97 * mx and not capped:
+        return (peaks["bf16_tflops"] * ratio, "burst",
+                f"median SM clock {sm:.0f} MHz of {mx:.0f} MHz with no power cap during the timed region")
+    why = "sw_power_cap active" if capped else f"median SM clock {sm} MHz below its maximum {mx}"
+    return peaks["bf16_tflops_sustained"] * ratio, "sustained", f"{why} during the timed region"
 
 
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-        dist.barrier()
+def stage_stats(moe, stamps, steps: int):
+    """Per-stage mean kernel span (ms) over the stamped steps, the mean span
+    from the first kernel's start to the last kernel's end of a step, and the
+    launch gaps (step span minus the sum of the stage spans)."""
+    spans = moe.stage_spans(stamps)
+    names = [n for n in moe._lib.STAGES if any(n in s for s in spans)]
+    out = {n: statistics.mean((s[n][1] - s[n][0]) / 1e6 for s in spans if n in s) for n in names}
+    step = statistics.mean((max(e for _, e in s.values()) - min(b for b, _ in s.values())) / 1e6 for s in spans)
+    return out, step, step - sum(out.values())
 
 
-def max_over_ranks(v: float, world: int, dev) -> float:
-    if world == 1:
-        return v
-    import torch.distributed as dist
-    t = torch.tensor([v], dtype=torch.float64, device=dev)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return float(t.item())
-
-
-def make_inputs(cfg_name: str, rank: int, dev, weights=None):
+def make_inputs(cfg_name: str, dev, weights=None):
     c = CONFIGS[cfg_name]
     cfg_name = cfg_name.replace("_fp8", "")
-    seed = rank_seed(rank)  # replicas: own tokens per rank (same model weights)
     if weights is None:
         weights = W.mixtral_weights(c["d"], c["f"], c["E"], seed=W.BASE_SEED, device=dev)
     if cfg_name in ("prefill", "prefill_e2", "train", "train_e2"):
-        return W.prefill(T=c["T"], seed=seed, device=dev, weights=weights), weights
+        return W.prefill(T=c["T"], seed=W.BASE_SEED, device=dev, weights=weights), weights
     if cfg_name.startswith("decode"):
-        return W.decode(c["T"], seed=seed, device=dev, weights=weights), weights
+        return W.decode(c["T"], seed=W.BASE_SEED, device=dev, weights=weights), weights
     if cfg_name == "skew":
-        return W.skew(T=c["T"], seed=seed, device=dev, weights=weights), weights
+        return W.skew(T=c["T"], seed=W.BASE_SEED, device=dev, weights=weights), weights
     raise ValueError(cfg_name)
 
 
@@ -383,6 +392,13 @@ def algorithmic(c, n_touched):
     bytes_step = n_touched * (3 * d * f * wb + scales) + 2 * d * E + 2 * T * d * 2
     gate_up_bytes = n_touched * (2 * d * f * wb + 2 * f * 4)
     return flops, gate_up_flops, bytes_step, gate_up_bytes
+
+
+def down_bytes(c, n_touched):
+    """Algorithmic bytes of the down GEMM: each touched expert's W2 once (e4m3:
+    one byte per weight plus the fp32 column scales)."""
+    d, f = c["d"], c["f"]
+    return n_touched * (f * d * (1 if c.get("fp8") else 2) + (d * 4 if c.get("fp8") else 0))
 
 
 # ---------------------------------------------------------------------------
@@ -449,7 +465,17 @@ def oracle_check(inp, idx_gpu, y_gpu, y_ref):
             "routing_tokens": int(x.shape[0]), "near_ties": int(near.sum()), "index_mismatches": mism}
 
 
-def run_reference_stack(args, world, c, dev, steps, warmup):
+def reference_line(args, c, value, ms, steps, warmup, sample, metric):
+    return {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": 1,
+            "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": WORKLOAD_TEXT[args.config], **c},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+
+
+def run_reference_stack(args, c, dev, steps, warmup):
     """stack32 reference arm: the float64 oracle's pre-norm block on a few
     tokens through layer 0 per step, scaled to the stack's layer count."""
     import numpy as np
@@ -477,18 +503,10 @@ def run_reference_stack(args, world, c, dev, steps, warmup):
     value = n_tok / (ms / 1e3)
     sample = (f"{n_tok} tokens per step through layer 0's pre-norm block, time scaled by {L} layers "
               f"(weights upcast to float64 once, untimed)")
-    metric = TRAIN_METRIC if train else (CACHE_METRIC if "cache_slots" in c else METRIC)
-    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.config], **c},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(reference_line(args, c, value, ms, steps, warmup, sample, METRIC)), flush=True)
 
 
-def run_reference(args, world, rank):
+def run_reference(args, rank):
     """The oracle as the reference arm: host cores only, bounded sample per step."""
     if rank != 0:
         return
@@ -498,8 +516,8 @@ def run_reference(args, world, rank):
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     steps, warmup = args.steps, max(args.warmup, 3)
     if args.config == "stack32":
-        return run_reference_stack(args, world, c, dev, steps, warmup)
-    inp, _ = make_inputs(args.config, 0, dev)
+        return run_reference_stack(args, c, dev, steps, warmup)
+    inp, _ = make_inputs(args.config, dev)
     # sample per step: bounded so the whole run stays within a few minutes
     per_step_budget_s = min(2.0, 150.0 / (steps + warmup))
     n_tok = max(1, min(c["T"], int(per_step_budget_s / 0.02)))
@@ -522,17 +540,9 @@ def run_reference(args, world, rank):
             times.append(dt)
     ms = 1e3 * sum(times) / len(times)
     value = n_tok / (ms / 1e3)
-    threads = blas_threads()
     sample = f"{n_tok} tokens of the {args.config} batch per step (weights upcast to float64 once, untimed)"
     metric = TRAIN_METRIC if train else (CACHE_METRIC if "cache_slots" in c else METRIC)
-    line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world,
-            "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-            "config": {"workload": WORKLOAD_TEXT[args.config], **c},
-            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": threads, "kind": "oracle",
-                             "sample": sample},
-            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
-    print(json.dumps(line), flush=True)
+    print(json.dumps(reference_line(args, c, value, ms, steps, warmup, sample, metric)), flush=True)
 
 
 # ---------------------------------------------------------------------------
@@ -553,32 +563,31 @@ def oracle_block_rate(h_rows, layer_weights, K: int):
     return time.perf_counter() - t0
 
 
-def stack_inputs(c, rank, dev):
-    layers = [W.stack_layer_weights(l, c["d"], c["f"], c["E"], device=dev) for l in range(c["layers"])]
-    h0 = W.stack_h0(c["T"], c["d"], seed=rank_seed(rank), device=dev)
-    return layers, h0
-
-
-def run_ours_stack(args, world, rank, local):
-    """stack32: a step is one pass of h0 through all layers of the stack."""
+def run_ours_stack(args):
+    """stack32: a step is one pass of h0 through all layers of the stack, each
+    layer a stamped pre-norm block (per-layer stage spans from the same run)."""
     import sparse_mixture_experts_55_b300 as moe
     from sparse_mixture_experts_55_b300 import build as _build
-    if rank == 0:
-        _build.build()
-    barrier(world)
-    dev = torch.device("cuda", local)
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     c = CONFIGS[args.config]
     T, d, f, E, K, L = c["T"], c["d"], c["f"], c["E"], c["K"], c["layers"]
-    layers, h0 = stack_inputs(c, rank, dev)
+    layers = [W.stack_layer_weights(l, d, f, E, device=dev) for l in range(L)]
+    h0 = W.stack_h0(T, d, device=dev)
     ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
     h = torch.empty_like(h0)
     stream = torch.cuda.current_stream(dev)
     steps, warmup = args.steps, max(args.warmup, 3)
+    stamps = moe.new_stamps(steps * L, dev)
 
-    def step(hbuf):
+    def step(hbuf, i=None):
         hbuf.copy_(h0)
         for l in range(L):
-            moe.moe_block_forward(hbuf, *layers[l], K, workspace=ws, stream=stream)
+            if i is None:
+                moe.moe_block_forward(hbuf, *layers[l], K, workspace=ws, stream=stream)
+            else:
+                moe.moe_block_forward_stamped(hbuf, *layers[l], K, stamps[i * L + l], workspace=ws, stream=stream)
 
     for _ in range(warmup):
         step(h)
@@ -586,32 +595,16 @@ def run_ours_stack(args, world, rank, local):
     if moe.moe_read_status(ws) != 0:
         raise RuntimeError(f"device status {moe.moe_read_status(ws)}")
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with ClockSampler(0) as clk:
         start.record(stream)
-        for _ in range(steps):
-            step(h)
+        for i in range(steps):
+            step(h, i)
         end.record(stream)
         torch.cuda.synchronize(dev)
-    barrier(world)
-    ms = max_over_ranks(start.elapsed_time(end) / steps, world, dev)
-
-    # stage pass: the same blocks as RMSNorm + moe_forward_timed (accumulate), one step
-    xn = torch.empty_like(h0)
-    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(L)]
-    norm_ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(L)]
-    h.copy_(h0)
-    torch.cuda.synchronize(dev)
-    for l in range(L):
-        norm_ev[l][0].record(stream)
-        moe.moe_rmsnorm(h, out=xn, stream=stream)
-        norm_ev[l][1].record(stream)
-        moe.moe_forward_timed(xn, *layers[l], K, evs[l], y=h, workspace=ws, flags=moe.MOE_ACCUMULATE, stream=stream)
-    torch.cuda.synchronize(dev)
-    stage_ms = {"rmsnorm": statistics.mean(norm_ev[l][0].elapsed_time(norm_ev[l][1]) for l in range(L))}
-    for j, name in enumerate(("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")):
-        stage_ms[name] = statistics.mean(evs[l][j].elapsed_time(evs[l][j + 1]) for l in range(L))
+    ms = start.elapsed_time(end) / steps
+    clocks = clk.summary()
+    stage_ms, layer_span_ms, _ = stage_stats(moe, stamps, steps * L)
 
     # end to end with host buffers: h0 in, the whole stack, h out
     e2e_steps = max(2, min(steps, 5))
@@ -627,69 +620,70 @@ def run_ours_stack(args, world, rank, local):
 
     step_host()
     torch.cuda.synchronize(dev)
-    barrier(world)
     t0 = time.perf_counter()
     for _ in range(e2e_steps):
         step_host()
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, dev)
+    e2e_ms = 1e3 * (time.perf_counter() - t0) / e2e_steps
 
     peaks, peak_src = load_peaks()
     flops_layer, gu_flops, _, _ = algorithmic(c, E)
     flops = L * (flops_layer + 4 * T * d)          # + RMSNorm (square, sum, scale, round) per layer
+    peak, kind, why = tensor_peak(peaks, clocks)
     gu_ms = stage_ms["gate_up_gemm"]
     achieved = gu_flops / (gu_ms / 1e3) / 1e12
-    roof = {"kernel": "gate_up_gemm", "bound": "tensor", "achieved": achieved,
-            "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-            "frac": achieved / peaks["bf16_tflops_sustained"], "frac_of_burst": achieved / peaks["bf16_tflops"],
-            "traffic": None, "algorithmic_flops_per_launch": gu_flops,
-            "launches_averaged": L,
-            "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peak_src}; kernel timed inside a long step)"}
+    roof = {"kernel": "gate_up_gemm", "bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+            "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
+            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
+            "traffic": None, "algorithmic_flops_per_launch": gu_flops, "launches_averaged": steps * L,
+            "kernel_ms": gu_ms, "share_of_step": gu_ms * L / ms,
+            "peak_kind": kind, "peak_source": f"MEASURED_PEAKS.json bf16_tflops{'' if kind == 'burst' else '_sustained'} "
+                                              f"({peak_src}): {why}"}
     line = {
-        "metric": METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "metric": METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1, "steps": steps,
         "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic: seeded random-init Mixtral-shaped weights per layer, h0 ~ N(0,1)",
-        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": "one GPU",
                    "l2": "inputs larger than L2: %.1f GB of expert weights streamed per step" % (
                        L * E * 3 * d * f * 2 / 1e9)},
-        "tflops": flops / (ms / 1e3) / 1e12 * world,
-        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops_sustained"],
+        "tflops": flops / (ms / 1e3) / 1e12,
+        "tflops_frac_of_peak": flops / (ms / 1e3) / 1e12 / peak,
         "tflops_frac_of_burst_peak": flops / (ms / 1e3) / 1e12 / peaks["bf16_tflops"],
         "stages_ms_per_layer": {k: round(v, 4) for k, v in stage_ms.items()},
+        "layer_span_ms": layer_span_ms,
         "roofline": roof,
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h0_host.numel() * h0_host.element_size(),
                 "d2h_bytes_per_step": h_host.numel() * h_host.element_size()},
         # per layer: RMSNorm, then the layer's kernels
         "gpu_launches": (1 + moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16)) * L * steps,
-        "stage_timing": "separate pass of one step with RMSNorm and library-recorded stage events per layer",
-        "clocks": clk.summary(),
+        "stage_timing": "global-timer stamps written by every kernel inside the timed region "
+                        "(moe_block_forward_stamped), averaged over the steps and layers",
+        "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         n_tok = min(T, max(1, args.cpu_tokens // 4))
         dt = oracle_block_rate(h0[:n_tok], layers[0], K)
         line["cpu_baseline"] = {"value": n_tok / (L * dt), "unit": "tokens/s", "cores": blas_threads(),
                                 "kind": "oracle",
                                 "sample": f"{n_tok} tokens through layer 0 of the stack, float64 oracle block "
                                           f"({dt:.1f} s), scaled to {L} layers; banks upcast once, untimed"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
 
 
 # ---------------------------------------------------------------------------
-def run_ours_cache(args, world, rank, local):
+def run_ours_cache(args):
     """Decode steps through moe_forward_cached over a seeded locality trace."""
     import sparse_mixture_experts_55_b300 as moe
     from sparse_mixture_experts_55_b300 import build as _build
-    if rank == 0:
-        _build.build()
-    barrier(world)
-    dev = torch.device("cuda", local)
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     c = CONFIGS[args.config]
     T, d, f, E, K, C = c["T"], c["d"], c["f"], c["E"], c["K"], c["cache_slots"]
     Wg, W1, W3, W2 = W.mixtral_weights(d, f, E, seed=W.BASE_SEED, device=dev)
     steps, warmup = args.steps, max(args.warmup, 3)
-    xs, _ = W.decode_trace(warmup + steps, Wg, T=T, keep=c["keep"], seed=rank_seed(rank), device=dev)
+    xs, _ = W.decode_trace(warmup + steps, Wg, T=T, keep=c["keep"], seed=W.BASE_SEED, device=dev)
     cache = moe.ExpertCache(W1, W3, W2, C, dev)
     ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
     y = torch.empty(T, d, dtype=torch.bfloat16, device=dev)
@@ -714,9 +708,8 @@ def run_ours_cache(args, world, rank, local):
     torch.cuda.synchronize(dev)
     st = cache.state
     h0, m0, b0 = st.hits, st.misses, st.bytes_loaded
-    barrier(world)
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with ClockSampler(local) as clk:
+    with ClockSampler(0) as clk:
         t0 = time.perf_counter()
         start.record(stream)
         for i in range(warmup, warmup + steps):
@@ -724,8 +717,7 @@ def run_ours_cache(args, world, rank, local):
         end.record(stream)
         torch.cuda.synchronize(dev)
         wall_ms = 1e3 * (time.perf_counter() - t0) / steps
-    barrier(world)
-    ms = max_over_ranks(start.elapsed_time(end) / steps, world, dev)
+    ms = start.elapsed_time(end) / steps
     if moe.moe_read_status(ws) != 0:
         raise RuntimeError("device status set during timed run")
     hits, misses, loaded = st.hits - h0, st.misses - m0, st.bytes_loaded - b0
@@ -751,15 +743,15 @@ def run_ours_cache(args, world, rank, local):
         cache.forward(xd, Wg, K, y=y, workspace=ws, stream=stream)
         y_h[i].copy_(y, non_blocking=True)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / steps, world, dev)
+    e2e_ms = 1e3 * (time.perf_counter() - t0) / steps
 
     achieved = loaded / (ms * steps / 1e3) / 1e9
     line = {
-        "metric": CACHE_METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": CACHE_METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
         "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic: seeded random-init Mixtral-shaped weights, Markov-chain locality trace of steered tokens",
-        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": "one GPU",
                    "l2": "expert matrices of 117 MB each, larger than L2"},
         "cache": {"slots": C, "experts": E, "hits": hits, "misses": misses,
                   "hit_rate": hits / max(1, hits + misses), "bytes_loaded_per_step": loaded / steps,
@@ -768,12 +760,12 @@ def run_ours_cache(args, world, rank, local):
         "roofline": {"kernel": "host-to-device expert copies", "bound": "h2d", "achieved": achieved,
                      "peak": link_gbs, "unit": "GB/s", "frac": achieved / link_gbs, "traffic": None,
                      "peak_source": "pinned host-to-device copy of one 117 MB expert matrix, timed in this run"},
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": T * d * 2, "d2h_bytes_per_step": T * d * 2},
         "gpu_launches": moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16) * steps,
         "clocks": clk.summary(),
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         import numpy as np
         import oracle
         n_tok = 8
@@ -786,26 +778,24 @@ def run_ours_cache(args, world, rank, local):
         line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": f"first {n_tok} trace tokens one at a time, float64 oracle with every "
                                           f"expert in host memory ({dt:.1f} s; weights upcast once, untimed)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
 
 
 BWD_STAGES = ("prep", "dgrad_h", "wgrad_w2", "dgrad_x", "wgrad_w13", "dx", "dwg")
 
 
-def run_ours_train(args, world, rank, local):
+def run_ours_train(args):
     """Training step: moe_forward_train then moe_backward (fp32 gradients) on
     the prefill batch with a fixed seeded output gradient."""
     import sparse_mixture_experts_55_b300 as moe
     from sparse_mixture_experts_55_b300 import build as _build
-    if rank == 0:
-        _build.build()
-    barrier(world)
-    dev = torch.device("cuda", local)
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     c = CONFIGS[args.config]
     T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
-    inp, _ = make_inputs(args.config, rank, dev)
-    dy = W.randn((T, d), 1.0, rank_seed(rank) + 77, dev, torch.bfloat16)
+    inp, _ = make_inputs(args.config, dev)
+    dy = W.randn((T, d), 1.0, W.BASE_SEED + 77, dev, torch.bfloat16)
     stream = torch.cuda.current_stream(dev)
     steps, warmup = args.steps, max(args.warmup, 3)
     ws = moe.TrainWorkspace(T, d, f, E, K, torch.bfloat16, dev)
@@ -825,23 +815,23 @@ def run_ours_train(args, world, rank, local):
     if moe.moe_read_status(ws) != 0:
         raise RuntimeError(f"device status {moe.moe_read_status(ws)}")
     start, mid, end = (torch.cuda.Event(enable_timing=True) for _ in range(3))
-    barrier(world)
     torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
+    with ClockSampler(0) as clk:
         start.record(stream)
         for _ in range(steps):
             step(inp.x, grads, dy)
         end.record(stream)
         torch.cuda.synchronize(dev)
-    barrier(world)
-    ms = max_over_ranks(start.elapsed_time(end) / steps, world, dev)
+    ms = start.elapsed_time(end) / steps
+    clocks = clk.summary()
     if moe.moe_read_status(ws) != 0:
         raise RuntimeError("device status set during timed run")
 
     # per-stage durations: forward as one region, backward stages from the
-    # library's stage events (separate pass of the same steps)
+    # library's stage events (separate pass of the same steps, scaled below to
+    # the headline step so that they add up to it)
     nst = len(BWD_STAGES) + 1
-    fwd_ms, st_ms = [], {k: [] for k in BWD_STAGES}
+    fwd_ms, st_ms, pass_ms = [], {k: [] for k in BWD_STAGES}, []
     for _ in range(steps):
         evs = [torch.cuda.Event(enable_timing=True) for _ in range(nst)]
         mid.record(stream)
@@ -856,9 +846,12 @@ def run_ours_train(args, world, rank, local):
         moe._lib.check("moe_backward_timed", rc)
         torch.cuda.synchronize(dev)
         fwd_ms.append(mid.elapsed_time(evs[0]))
+        pass_ms.append(mid.elapsed_time(evs[-1]))
         for j, k in enumerate(BWD_STAGES):
             st_ms[k].append(evs[j].elapsed_time(evs[j + 1]))
-    stage_ms = {"forward_train": statistics.mean(fwd_ms), **{k: statistics.mean(v) for k, v in st_ms.items()}}
+    stage_pass = {"forward_train": statistics.mean(fwd_ms), **{k: statistics.mean(v) for k, v in st_ms.items()}}
+    scale = ms / statistics.mean(pass_ms)
+    stage_ms = {k: v * scale for k, v in stage_pass.items()}
 
     # end to end with host buffers: x and dy copied in from pinned memory,
     # dx copied out, every step (the weight gradients stay on the device for
@@ -870,14 +863,13 @@ def run_ours_train(args, world, rank, local):
     for i in range(e2e_steps + 2):
         if i == 2:
             torch.cuda.synchronize(dev)
-            barrier(world)
             t0 = time.perf_counter()
         xd.copy_(x_h, non_blocking=True)
         dyd.copy_(dy_h, non_blocking=True)
         step(xd, grads, dyd)
         dx_h.copy_(grads.dx, non_blocking=True)
         torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, dev)
+    e2e_ms = 1e3 * (time.perf_counter() - t0) / e2e_steps
 
     peaks, peak_src = load_peaks()
     unit = 2.0 * T * K * d * f  # one expert-GEMM pass over the routed rows
@@ -885,34 +877,37 @@ def run_ours_train(args, world, rank, local):
     prods = {"dgrad_h": unit, "wgrad_w2": unit, "dgrad_x": 2 * unit, "wgrad_w13": 2 * unit}
     top = max(prods, key=lambda k: stage_ms[k])  # the longest product
     achieved = prods[top] / (stage_ms[top] / 1e3) / 1e12
-    tensor_peak = peaks["bf16_tflops_sustained"]
-    roof = {"kernel": f"bwd_gemm_kernel ({top})", "bound": "tensor", "achieved": achieved, "peak": tensor_peak,
-            "unit": "TFLOP/s", "frac": achieved / tensor_peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
+    peak, kind, why = tensor_peak(peaks, clocks)
+    roof = {"kernel": f"bwd_gemm_kernel ({top})", "bound": "tensor", "achieved": achieved, "peak": peak,
+            "unit": "TFLOP/s", "frac": achieved / peak, "frac_of_burst": achieved / peaks["bf16_tflops"],
+            "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
             "traffic": traffic_from_profiles(ROOT / "sparse_mixture_experts_55_b300" / "csrc" / "gemm_bwd.cu",
                                              f"{args.config}_{top}_traffic_bytes_per_launch", "bwd_gemm_traffic.md"),
-            "algorithmic_flops_per_launch": prods[top],
-            "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained ({peak_src}; kernel timed inside a long run "
-                           f"of steps)"}
+            "algorithmic_flops_per_launch": prods[top], "kernel_ms": stage_ms[top],
+            "peak_kind": kind, "peak_source": f"MEASURED_PEAKS.json bf16_tflops{'' if kind == 'burst' else '_sustained'} "
+                                              f"({peak_src}): {why}"}
     line = {
-        "metric": TRAIN_METRIC, "value": world * T / (ms / 1e3), "unit": "tokens/s", "n_gpus": world,
+        "metric": TRAIN_METRIC, "value": T / (ms / 1e3), "unit": "tokens/s", "n_gpus": 1,
         "steps": steps, "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16 (fp32 accumulate, fp32 gradients)",
         "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens, N(0,1) dy",
-        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": "one GPU",
                    "l2": "inputs larger than L2: %.2f GB of expert weights and %.2f GB of fp32 weight gradients "
                          "per step" % (3 * E * d * f * 2 / 1e9, 3 * E * d * f * 4 / 1e9)},
-        "tflops": flops / (ms / 1e3) / 1e12 * world,
-        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
+        "tflops": flops / (ms / 1e3) / 1e12,
+        "tflops_frac_of_peak": flops / (ms / 1e3) / 1e12 / peak,
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "stages_ms_separate_pass": {k: round(v, 4) for k, v in stage_pass.items()},
         "roofline": roof,
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
                 "d2h_bytes_per_step": dx_h.numel() * dx_h.element_size()},
         "gpu_launches": (moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16) + 8) * steps,
-        "stage_timing": "separate pass of the same steps with library-recorded backward stage events",
-        "clocks": clk.summary(),
+        "stage_timing": "shares from a separate pass of the same steps with library-recorded backward stage "
+                        "events, scaled to the headline step",
+        "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         import numpy as np
         import oracle
         n_tok = max(1, min(T, args.cpu_tokens // 4))
@@ -926,86 +921,121 @@ def run_ours_train(args, world, rank, local):
         line["cpu_baseline"] = {"value": n_tok / dt, "unit": "tokens/s", "cores": blas_threads(), "kind": "oracle",
                                 "sample": f"first {n_tok} tokens, float64 oracle forward + backward ({dt:.1f} s; "
                                           f"weights upcast once, untimed)"}
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+    print(json.dumps(line), flush=True)
 
 
-def run_ours(args, world, rank, local):
+# ---------------------------------------------------------------------------
+class LayerRunner:
+    """The forward of one configuration (bf16 or e4m3 weights) through the C
+    ABI, plain or stamped, with its own workspace."""
+
+    def __init__(self, moe, c, x, weights, q8, dev, stream):
+        T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
+        self.moe, self.x, self.w, self.q8, self.K, self.stream = moe, x, weights, q8, K, stream
+        self.ws = moe.Workspace(T, d, f, E, K, torch.float8_e4m3fn if q8 else torch.bfloat16, dev)
+        self.y = torch.empty_like(x)
+
+    def __call__(self, stamps=None):
+        m, Wg = self.moe, self.w[0]
+        if self.q8 is not None:
+            if stamps is None:
+                m.moe_forward_fp8(self.x, Wg, *self.q8, self.K, y=self.y, workspace=self.ws, stream=self.stream)
+            else:
+                m.moe_forward_fp8_stamped(self.x, Wg, *self.q8, self.K, stamps, y=self.y, workspace=self.ws,
+                                          stream=self.stream)
+        elif stamps is None:
+            m.moe_forward(self.x, *self.w, self.K, y=self.y, workspace=self.ws, stream=self.stream)
+        else:
+            m.moe_forward_stamped(self.x, *self.w, self.K, stamps, y=self.y, workspace=self.ws, stream=self.stream)
+
+
+def timed_region(moe, run, steps: int, dev, stream, stamped: bool):
+    """K back-to-back forwards between two events (kernels chained by
+    programmatic dependent launch), NVML clocks sampled meanwhile; with
+    stamped, every forward writes its stage stamps into its own row."""
+    stamps = moe.new_stamps(steps, dev) if stamped else None
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(dev.index or 0) as clk:
+        start.record(stream)
+        for i in range(steps):
+            run(stamps[i] if stamped else None)
+        end.record(stream)
+        torch.cuda.synchronize(dev)
+    if moe.moe_read_status(run.ws) != 0:
+        raise RuntimeError("device status set during timed run")
+    return start.elapsed_time(end) / steps, clk.summary(), stamps
+
+
+def decode_record(moe, weights, q8, dev, stream, steps: int, warmup: int, peaks, fp8: bool):
+    """The decode half of the metric: for each decode batch size of the sweep,
+    the stamped layer over `steps` forwards of that batch through the prefill
+    weights: ms per step, algorithmic bytes (touched experts' weights once)
+    per second against the measured HBM copy bandwidth, and the same for each
+    expert GEMM from its in-run kernel span."""
+    out = {}
+    for T in (1, 8, 32, 128):
+        c = dict(CONFIGS[f"decode{T}"], fp8=fp8)
+        inp = W.decode(T, seed=W.BASE_SEED, device=dev, weights=weights)
+        counts = moe.moe_route(inp.x, inp.Wg, c["K"])[3]
+        n_touched = int(((counts[1:] - counts[:-1]) > 0).sum())
+        run = LayerRunner(moe, c, inp.x, weights, q8, dev, stream)
+        for _ in range(warmup):
+            run()
+        ms, clocks, stamps = timed_region(moe, run, steps, dev, stream, stamped=True)
+        stages, span, gaps = stage_stats(moe, stamps, steps)
+        _, _, bytes_step, gu_bytes = algorithmic(c, n_touched)
+        dn_bytes = down_bytes(c, n_touched)
+        gbs = bytes_step / (ms / 1e3) / 1e9
+        gu_gbs = gu_bytes / (stages["gate_up_gemm"] / 1e3) / 1e9
+        dn_gbs = dn_bytes / (stages["down_gemm"] / 1e3) / 1e9
+        out[f"T={T}"] = {
+            "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "touched_experts": n_touched,
+            "algorithmic_bytes_per_step": bytes_step, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
+            "gate_up_gemm": {"ms": stages["gate_up_gemm"], "bytes": gu_bytes, "gbs": gu_gbs,
+                             "frac_of_hbm": gu_gbs / peaks["hbm_gbs"]},
+            "down_gemm": {"ms": stages["down_gemm"], "bytes": dn_bytes, "gbs": dn_gbs,
+                          "frac_of_hbm": dn_gbs / peaks["hbm_gbs"]},
+            "stages_ms": {k: round(v, 4) for k, v in stages.items()},
+            "launch_gaps_ms": gaps, "clocks": clocks}
+        del run
+    return out
+
+
+def run_ours(args):
     import sparse_mixture_experts_55_b300 as moe
     from sparse_mixture_experts_55_b300 import build as _build
-    if rank == 0:
-        _build.build()
-    barrier(world)
-    dev = torch.device("cuda", local)
+    _build.build()
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     c = CONFIGS[args.config]
     T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
-    inp, weights = make_inputs(args.config, rank, dev)
+    inp, weights = make_inputs(args.config, dev)
     fp8 = bool(c.get("fp8"))
-    y = torch.empty_like(inp.x)
     stream = torch.cuda.current_stream(dev)
     steps, warmup = args.steps, max(args.warmup, 3)
-    if fp8:
-        # e4m3 expert weights: quantised once before timing (weight preparation)
-        q8 = [t for W_ in (inp.W1, inp.W3, inp.W2) for t in moe.quantize_weights_fp8(W_)]
-        ws = moe.Workspace(T, d, f, E, K, torch.float8_e4m3fn, dev)
-
-        def fwd(out):
-            moe.moe_forward_fp8(inp.x, inp.Wg, *q8, K, y=out, workspace=ws, stream=stream)
-
-        def fwd_timed(evs, out):
-            moe.moe_forward_fp8_timed(inp.x, inp.Wg, *q8, K, evs, y=out, workspace=ws, stream=stream)
-    else:
-        q8 = None
-        ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, dev)
-
-        def fwd(out):
-            moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, y=out, workspace=ws, stream=stream)
-
-        def fwd_timed(evs, out):
-            moe.moe_forward_timed(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, evs, y=out, workspace=ws, stream=stream)
+    # e4m3 expert weights: quantised once before timing (weight preparation)
+    q8 = [t for W_ in (inp.W1, inp.W3, inp.W2) for t in moe.quantize_weights_fp8(W_)] if fp8 else None
+    run = LayerRunner(moe, c, inp.x, weights, q8, dev, stream)
 
     # touched experts of this routing (algorithmic bytes at decode sizes)
     route_idx, _, _, offs, _ = moe.moe_route(inp.x, inp.Wg, K)
-    counts = (offs[1:] - offs[:-1]).cpu()
-    n_touched = int((counts > 0).sum())
-
-    def new_events(n):
-        return [[torch.cuda.Event(enable_timing=True) for _ in range(7)] for _ in range(n)]
+    n_touched = int(((offs[1:] - offs[:-1]) > 0).sum())
 
     for _ in range(warmup):
-        fwd(y)
+        run()
     torch.cuda.synchronize(dev)
-    if moe.moe_read_status(ws) != 0:
-        raise RuntimeError(f"device status {moe.moe_read_status(ws)}")
+    if moe.moe_read_status(run.ws) != 0:
+        raise RuntimeError(f"device status {moe.moe_read_status(run.ws)}")
 
-    # headline: K back-to-back forwards (kernels chained by programmatic
-    # dependent launch), two events around the whole region
-    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        start.record(stream)
-        for i in range(steps):
-            fwd(y)
-        end.record(stream)
-        torch.cuda.synchronize(dev)
-    barrier(world)
-    ms_local = start.elapsed_time(end) / steps
-    ms = max_over_ranks(ms_local, world, dev)
-    if moe.moe_read_status(ws) != 0:
-        raise RuntimeError("device status set during timed run")
-
-    # per-stage durations: the same forwards with events recorded by the
-    # library at the stage boundaries (the events serialise the kernels, so
-    # these sum to slightly more than the headline step time)
-    evs = new_events(steps)
-    torch.cuda.synchronize(dev)
-    for i in range(steps):
-        fwd_timed(evs[i], y)
-    torch.cuda.synchronize(dev)
-    stage_ms = {}
-    for j, name in enumerate(("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")):
-        stage_ms[name] = statistics.mean(evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(steps))
+    # headline: K back-to-back stamped forwards; every kernel writes its
+    # begin/end global-timer stamps, so the per-kernel spans come from this
+    # very region and add up to its step time (less launch gaps)
+    ms, clocks, stamps = timed_region(moe, run, steps, dev, stream, stamped=True)
+    stage_ms, step_span_ms, gaps_ms = stage_stats(moe, stamps, steps)
+    y_out = run.y.clone()
+    # the same steps through plain moe_forward (no stamps), for comparison
+    ms_plain, clocks_plain, _ = timed_region(moe, run, steps, dev, stream, stamped=False)
 
     # end to end through the C ABI with host buffers: every step copies its
     # batch in from pinned host memory and its result out; the copies of
@@ -1013,105 +1043,111 @@ def run_ours(args, world, rank, local):
     e2e_steps = max(3, min(steps, 50))
     x_hosts = [inp.x.cpu().pin_memory() for _ in range(2)]
     y_hosts = [torch.empty_like(x_hosts[0]).pin_memory() for _ in range(2)]
-    pipe = moe.HostPipeline(inp.Wg, inp.W1, inp.W3, inp.W2, K, T, dev, workspace=ws, fp8_weights=q8)
+    pipe = moe.HostPipeline(inp.Wg, inp.W1, inp.W3, inp.W2, K, T, dev, workspace=run.ws, fp8_weights=q8)
     for i in range(3):
         pipe.submit(x_hosts[i & 1], y_hosts[i & 1])
     pipe.synchronize()
-    barrier(world)
     t0 = time.perf_counter()
     for i in range(e2e_steps):
         pipe.submit(x_hosts[i & 1], y_hosts[i & 1])
     pipe.synchronize()
-    e2e_ms = max_over_ranks(1e3 * (time.perf_counter() - t0) / e2e_steps, world, dev)
+    e2e_ms = 1e3 * (time.perf_counter() - t0) / e2e_steps
     x_host, y_host = x_hosts[0], y_hosts[0]
 
     peaks, peak_src = load_peaks()
     flops, gu_flops, bytes_step, gu_bytes = algorithmic(c, n_touched)
-    tokens_per_s = world * T / (ms / 1e3)
+    tokens_per_s = T / (ms / 1e3)
     gu_ms = stage_ms["gate_up_gemm"]
     hbm_bound = args.config.startswith("decode")
     # e4m3 contractions take the bf16 measured peaks times the nominal fp8/bf16 ratio (4.5 / 2.25)
-    tensor_ratio = 2.0 if fp8 else 1.0
-    tensor_peak = peaks["bf16_tflops_sustained"] * tensor_ratio
-    tensor_peak_burst = peaks["bf16_tflops"] * tensor_ratio
+    ratio = 2.0 if fp8 else 1.0
     peak_note = " x 2 (nominal e4m3/bf16 dense ratio)" if fp8 else ""
     kernel_file = ROOT / "sparse_mixture_experts_55_b300" / "csrc" / "gemm_tc.cu"
+    traffic = traffic_from_profiles(kernel_file, f"{args.config}_traffic_bytes_per_launch")
     if hbm_bound:
         achieved = gu_bytes / (gu_ms / 1e3) / 1e9
         roof = {"kernel": "gate_up_gemm", "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"],
-                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"],
-                "traffic": traffic_from_profiles(kernel_file, f"{args.config}_traffic_bytes_per_launch"),
-                "algorithmic_bytes_per_launch": gu_bytes, "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
+                "unit": "GB/s", "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                "algorithmic_bytes_per_launch": gu_bytes, "kernel_ms": gu_ms, "share_of_step": gu_ms / ms,
+                "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_src})"}
     else:
+        peak, kind, why = tensor_peak(peaks, clocks, ratio)
         achieved = gu_flops / (gu_ms / 1e3) / 1e12
-        roof = {"kernel": "gate_up_gemm", "bound": "tensor", "achieved": achieved,
-                "peak": tensor_peak, "unit": "TFLOP/s",
-                "frac": achieved / tensor_peak,
-                "frac_of_burst": achieved / tensor_peak_burst,
-                "traffic": traffic_from_profiles(kernel_file, f"{args.config}_traffic_bytes_per_launch"),
-                "algorithmic_flops_per_launch": gu_flops,
-                "peak_source": f"MEASURED_PEAKS.json bf16_tflops_sustained{peak_note} ({peak_src}; kernel timed "
-                               f"inside a long run of steps)"}
+        roof = {"kernel": "gate_up_gemm", "bound": "tensor", "achieved": achieved, "peak": peak,
+                "unit": "TFLOP/s", "frac": achieved / peak,
+                "frac_of_burst": achieved / (peaks["bf16_tflops"] * ratio),
+                "frac_of_sustained": achieved / (peaks["bf16_tflops_sustained"] * ratio),
+                "traffic": traffic, "algorithmic_flops_per_launch": gu_flops,
+                "kernel_ms": gu_ms, "share_of_step": gu_ms / ms, "peak_kind": kind,
+                "peak_source": f"MEASURED_PEAKS.json bf16_tflops{'' if kind == 'burst' else '_sustained'}"
+                               f"{peak_note} ({peak_src}): {why}"}
+        dn_ms = stage_ms["down_gemm"]
+        dn_flops = T * K * 2 * d * f
+        roof["down_gemm"] = {"kernel_ms": dn_ms, "achieved": dn_flops / (dn_ms / 1e3) / 1e12,
+                             "frac": dn_flops / (dn_ms / 1e3) / 1e12 / peak, "algorithmic_flops_per_launch": dn_flops}
     line = {
-        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": world, "steps": steps,
+        "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
         "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "e4m3 experts, bf16 tokens" if fp8 else "bf16",
         "data": "synthetic: seeded random-init Mixtral-shaped weights, RMS-normalised N(0,1) tokens",
-        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": f"replicas x{world} (no collective)",
+        "config": {"workload": WORKLOAD_TEXT[args.config], **c, "parallelism": "one GPU",
                    "l2": "inputs larger than L2: %.2f GB of expert weights streamed per step" % (
                        n_touched * 3 * d * f * (1 if fp8 else 2) / 1e9), "touched_experts": n_touched},
-        "tflops": flops / (ms / 1e3) / 1e12 * world,
-        "tflops_frac_of_sustained_peak": flops / (ms / 1e3) / 1e12 / tensor_peak,
+        "tflops": flops / (ms / 1e3) / 1e12,
         "hbm_gbs_algorithmic": bytes_step / (ms / 1e3) / 1e9,
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "step_span_ms": step_span_ms, "launch_gaps_ms": gaps_ms,
         "roofline": roof,
-        "e2e": {"value": world * T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
+        "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_host.numel() * x_host.element_size(),
                 "d2h_bytes_per_step": y_host.numel() * y_host.element_size()},
         "gpu_launches": moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_FP8_E4M3 if fp8 else moe.MOE_BF16)
         * steps,
-        "stage_timing": "separate pass of the same K forwards with library-recorded stage events",
-        "clocks": clk.summary(),
+        "timed_call": ("moe_forward_fp8_stamped" if fp8 else "moe_forward_stamped") +
+                      ": the plain call's kernels, each CTA also writing two global-timer stamps",
+        "stage_timing": "global-timer stamps written by every kernel inside the timed region, averaged over the steps",
+        "plain": {"ms_per_step": ms_plain, "tokens_per_s": T / (ms_plain / 1e3), "clocks": clocks_plain,
+                  "call": "moe_forward_fp8" if fp8 else "moe_forward", "region": "the next K steps, unstamped"},
+        "clocks": clocks,
     }
-    if rank == 0 and world == 1 and not args.no_cpu_baseline and not fp8:
+    if not hbm_bound:
+        line["tflops_frac_of_peak"] = line["tflops"] / roof["peak"]
+    if args.config in ("prefill", "prefill_fp8") and not args.no_decode:
+        line["decode"] = decode_record(moe, weights, q8, dev, stream, max(steps, 20), warmup, peaks, fp8)
+    if not args.no_cpu_baseline and not fp8:
         n_tok = min(T, args.cpu_tokens)
         rate, dt, threads, y_ref = cpu_oracle_rate(inp, n_tok)
         line["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": threads, "kind": "oracle",
                                 "sample": f"first {n_tok} tokens of the batch, float64 oracle ({dt:.1f} s; "
                                           f"weights upcast once, untimed)"}
-        line["parity"] = oracle_check(inp, route_idx.cpu().numpy(), y[:n_tok].float().cpu().numpy(), y_ref)
-    if rank == 0:
-        print(json.dumps(line), flush=True)
+        line["parity"] = oracle_check(inp, route_idx.cpu().numpy(), y_out[:n_tok].float().cpu().numpy(), y_ref)
+    print(json.dumps(line), flush=True)
 
 
 def main():
     ap = argparse.ArgumentParser()
-    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--gpus", type=int, default=1, help="1 (the only supported value)")
     ap.add_argument("--steps", type=int, default=None, help="default: 100 (10 for stack32)")
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--config", default="prefill", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-decode", action="store_true", help="omit the decode sweep of the prefill line")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 10 if args.config == "stack32" else 100
-    world, rank, local = setup_dist()
-    try:
-        if args.impl == "reference":
-            run_reference(args, world, rank)
-        elif args.config == "stack32":
-            run_ours_stack(args, world, rank, local)
-        elif CONFIGS[args.config].get("train"):
-            run_ours_train(args, world, rank, local)
-        elif "cache_slots" in CONFIGS[args.config]:
-            run_ours_cache(args, world, rank, local)
-        else:
-            run_ours(args, world, rank, local)
-    finally:
-        if world > 1:
-            import torch.distributed as dist
-            dist.destroy_process_group()
+    rank = launch_rank(args)
+    if args.impl == "reference":
+        run_reference(args, rank)
+    elif args.config == "stack32":
+        run_ours_stack(args)
+    elif CONFIGS[args.config].get("train"):
+        run_ours_train(args)
+    elif "cache_slots" in CONFIGS[args.config]:
+        run_ours_cache(args)
+    else:
+        run_ours(args)
 
 
 if __name__ == "__main__":

@@ -144,22 +144,36 @@ MOE_API int moe_forward(const void *x, const void *Wg, const void *W1, const voi
                 void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
 
 /*
- * moe_forward with per-stage timing: the same work and the same results, and
- * in addition records caller-created CUDA events on `stream` at the stage
- * boundaries, for kernel durations measured inside a timed run.
- *   events: HOST array of MOE_NUM_STAGE_EVENTS cudaEvent_t handles (as void*),
- *           none NULL, created by the caller (with timing enabled for
- *           cudaEventElapsedTime).  events[0] is recorded before the router
- *           and events[i] after stage i: 1 router, 2 grouping, 3 row gather,
- *           4 gate/up expert GEMM (+SwiGLU), 5 down expert GEMM (x gate),
- *           6 two-slot combine.  With T = 0 no event is recorded.
- * Returns MOE_ERR_INVALID_ARG if events or one of its entries is NULL.
+ * moe_forward with per-stage device timestamps, for kernel durations measured
+ * inside a timed run without separating the kernels: the same kernels, work
+ * and results as moe_forward.  Each kernel also reads the GPU's global
+ * nanosecond timer: every CTA of the kernel of stage s lowers stamps[s] to the
+ * time it starts its work (after waiting for its inputs) and raises
+ * stamps[MOE_NUM_STAGES + s] to the time it finishes, so for a stage that ran,
+ * stamps[MOE_NUM_STAGES + s] - stamps[s] is its kernel's span in ns.
+ *   stamps: DEVICE array of 2 * MOE_NUM_STAGES unsigned 64-bit integers,
+ *           8-byte aligned, owned by the caller.  The call first resets it on
+ *           the stream (begin times to all ones, end times to zero), so a
+ *           stage that did not run reads (UINT64_MAX, 0).
+ *   Stages: MOE_STAGE_ROUTE router; MOE_STAGE_GROUP grouping; MOE_STAGE_GATHER
+ *           row gather (e4m3: gather and quantise); MOE_STAGE_GATE_UP gate/up
+ *           expert GEMM with SwiGLU; MOE_STAGE_QUANT_H quantisation of H
+ *           (e4m3 only); MOE_STAGE_DOWN down expert GEMM (x gate; and, when
+ *           unsplit, the combine); MOE_STAGE_COMBINE combine kernel (split
+ *           down projections and fp32); MOE_STAGE_NORM RMSNorm
+ *           (moe_block_forward_stamped only).
+ * Returns MOE_ERR_INVALID_ARG if stamps is NULL or misaligned; otherwise as
+ * moe_forward.  Calls sharing one stamps array must be ordered on the GPU.
  */
-#define MOE_NUM_STAGE_EVENTS 7
-MOE_API int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
+#define MOE_NUM_STAGES 8
+enum {
+  MOE_STAGE_ROUTE = 0, MOE_STAGE_GROUP = 1, MOE_STAGE_GATHER = 2, MOE_STAGE_GATE_UP = 3,
+  MOE_STAGE_QUANT_H = 4, MOE_STAGE_DOWN = 5, MOE_STAGE_COMBINE = 6, MOE_STAGE_NORM = 7
+};
+MOE_API int moe_forward_stamped(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2,
                       void *y, int T, int d, int f, int E, int K, int dtype,
                       void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
-                      void *const *events);
+                      unsigned long long *stamps);
 
 /*
  * One pre-norm MoE half-block of the attention-free stack, in place:
@@ -181,6 +195,13 @@ MOE_API int moe_forward_timed(const void *x, const void *Wg, const void *W1, con
 MOE_API int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2,
                       int T, int d, int f, int E, int K, int dtype, float eps,
                       void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
+
+/* moe_block_forward with the stage timestamps of moe_forward_stamped (the
+ * RMSNorm kernel as MOE_STAGE_NORM). */
+MOE_API int moe_block_forward_stamped(void *h, const void *Wg, const void *W1, const void *W3, const void *W2,
+                      int T, int d, int f, int E, int K, int dtype, float eps,
+                      void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                      unsigned long long *stamps);
 
 /*
  * e4m3 expert weights.  The pages name FP8 only as deployment work
@@ -220,12 +241,11 @@ MOE_API int moe_forward_fp8(const void *x, const void *Wg, const void *W1q, cons
                     const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
                     int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream);
 
-/* moe_forward_fp8 with the stage events of moe_forward_timed (stage 4, the
- * gate/up GEMM, includes the quantisation of H). */
-MOE_API int moe_forward_fp8_timed(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
-                          const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f,
-                          int E, int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
-                          void *const *events);
+/* moe_forward_fp8 with the stage timestamps of moe_forward_stamped. */
+MOE_API int moe_forward_fp8_stamped(const void *x, const void *Wg, const void *W1q, const float *s1,
+                          const void *W3q, const float *s3, const void *W2q, const float *s2, void *y, int T,
+                          int d, int f, int E, int K, void *workspace, size_t ws_bytes, unsigned flags,
+                          moe_stream_t stream, unsigned long long *stamps);
 
 /*
  * Training: a forward pass that keeps what the backward pass needs, and the
@@ -379,20 +399,33 @@ MOE_API int moe_route(const void *x, const void *Wg, int T, int d, int E, int K,
  * their hot path.  The pages have no counterpart; this is a convenience of
  * the library.
  *
- * Same arguments, outputs and results as moe_route, minus the workspace.  The
- * scratch is a fixed array of 1 MiB compiled into the library: every GPU
- * that loads libmoe.so reserves it until the process exits, and all calls on
- * a GPU share it, so calls that overlap on the GPU (different streams or
- * host threads) race and must be serialised by the caller.  The first call on
- * each device looks up the array's device address (cudaGetSymbolAddress, with
- * that device current); make that first call before any stream capture.
- * Limits: T <= MOE_ROUTE_NOALLOC_MAX_T, K <= 2, E <= 32; a larger T returns
- * MOE_ERR_UNSUPPORTED without launching.  Allocates nothing.
+ * Same arguments, outputs and results as moe_route, minus the workspace, plus
+ * flags (0 or MOE_DEBUG_CHECKS: non-finite router logits are then recorded as
+ * MOE_ERR_NONFINITE).  The scratch is a fixed array of 1 MiB compiled into the
+ * library: every GPU that loads libmoe.so reserves it until the process
+ * exits, and all calls on a GPU share it, so calls that overlap on the GPU
+ * (different streams or host threads) race and must be serialised by the
+ * caller.  The first call on each device (and in each new context of it, e.g.
+ * after cudaDeviceReset) looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Limits: T <= MOE_ROUTE_NOALLOC_MAX_T, K <= 2,
+ * E <= 32; a larger T returns MOE_ERR_UNSUPPORTED without launching.
+ * Allocates nothing.  Device-side errors go to a status word in the array,
+ * which the next call clears; read it with moe_route_noalloc_status.
  */
 #define MOE_ROUTE_NOALLOC_MAX_T 16384
 MOE_API int moe_route_noalloc(const void *x, const void *Wg, int T, int d, int E, int K, int dtype,
                       int32_t *idx, float *gate, int32_t *perm_tok, int32_t *offsets, int32_t *pos,
-                      moe_stream_t stream);
+                      unsigned flags, moe_stream_t stream);
+
+/*
+ * The device status word of the last moe_route_noalloc call on the current
+ * device (MOE_OK if it recorded no error): synchronises `stream` (the stream
+ * of that call), then copies the word out of the library's scratch array.
+ * MOE_ERR_CUDA if the synchronisation or the copy failed.  Allocates nothing.
+ * The pages have no counterpart.
+ */
+MOE_API int moe_route_noalloc_status(moe_stream_t stream);
 
 /*
  * RMSNorm with unit gain, out = x / sqrt(mean(x^2) + eps) per row, fp32 math

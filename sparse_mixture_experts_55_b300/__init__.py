@@ -22,8 +22,8 @@ from ._lib import (MOE_ACCUMULATE, MOE_BF16, MOE_DEBUG_CHECKS, MOE_DEBUG_FORCE_T
                    MOE_FP8_E4M3, MOE_GEMM_MULTICAST_PAIRS, MOE_GEMM_PAIR_MMA, MOE_GEMM_QUAD, MoEError,
                    status_string)
 
-__all__ = ["moe_forward", "moe_forward_timed", "moe_block_forward", "HostPipeline", "quantize_weights_fp8",
-           "moe_forward_fp8", "moe_forward_fp8_timed", "TrainWorkspace", "moe_forward_train", "moe_backward",
+__all__ = ["moe_forward", "moe_forward_stamped", "moe_block_forward", "moe_block_forward_stamped", "HostPipeline",
+           "quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_stamped", "new_stamps", "stage_spans", "TrainWorkspace", "moe_forward_train", "moe_backward",
            "LayerGrads", "ExpertCache", "moe_forward_host", "moe_route", "moe_rmsnorm", "moe_read_status", "moe_workspace_bytes",
            "Workspace", "MoEError", "MOE_ACCUMULATE", "MOE_DEBUG_CHECKS", "MOE_BF16", "MOE_F32",
            "status_string", "library_path"]
@@ -127,32 +127,65 @@ def moe_block_forward(h, Wg, W1, W3, W2, K: int = 2, eps: float = 1e-5, workspac
     return h
 
 
-def moe_forward_timed(x, Wg, W1, W3, W2, K: int, events, y=None, workspace: Workspace | None = None,
-                      flags: int = 0, stream=None):
-    """moe_forward that also records the seven torch.cuda.Event objects in
-    ``events`` at the stage boundaries (before the router, then after router,
-    grouping, gather, gate/up GEMM, down GEMM and combine)."""
-    if len(events) != _lib.MOE_NUM_STAGE_EVENTS:
-        raise ValueError(f"need {_lib.MOE_NUM_STAGE_EVENTS} events")
+def new_stamps(n: int = 1, device=None) -> torch.Tensor:
+    """Device buffer for n stamped calls: int64 [n, 2 * MOE_NUM_STAGES] (the
+    library treats each row as unsigned 64-bit begin/end times)."""
+    return torch.zeros((n, 2 * _lib.MOE_NUM_STAGES), dtype=torch.int64, device=device or "cuda")
+
+
+def _stamps_arg(stamps: torch.Tensor, device):
+    _need(stamps, "stamps", torch.int64, device)
+    if stamps.numel() != 2 * _lib.MOE_NUM_STAGES:
+        raise ValueError(f"stamps must hold {2 * _lib.MOE_NUM_STAGES} entries")
+    return ctypes.c_void_p(stamps.data_ptr())
+
+
+def stage_spans(stamps) -> list:
+    """Host decoding of stamped calls: for each row of an int64 [n, 16]
+    tensor (or one row), a dict stage name -> (begin_ns, end_ns) for the
+    stages that ran (end >= begin), in the unsigned global-timer scale."""
+    import numpy as np
+    a = np.asarray(stamps.cpu() if isinstance(stamps, torch.Tensor) else stamps).astype(np.int64).view(np.uint64)
+    a = a.reshape(-1, 2 * _lib.MOE_NUM_STAGES)
+    n = _lib.MOE_NUM_STAGES
+    out = []
+    for row in a:
+        out.append({name: (int(row[i]), int(row[n + i])) for i, name in enumerate(_lib.STAGES)
+                    if row[n + i] != 0 and row[i] != np.iinfo(np.uint64).max and row[n + i] >= row[i]})
+    return out
+
+
+def moe_forward_stamped(x, Wg, W1, W3, W2, K: int, stamps, y=None, workspace: Workspace | None = None,
+                        flags: int = 0, stream=None):
+    """moe_forward whose kernels also write their begin/end global-timer
+    times into ``stamps`` (one row of new_stamps; decode with stage_spans)."""
     dev = x.device
-    s = stream if stream is not None else torch.cuda.current_stream(dev)
-    handles = []
-    for ev in events:
-        if ev.cuda_event == 0:      # torch creates the CUDA event on first record
-            ev.record(s)
-        handles.append(ev.cuda_event)
-    arr = (ctypes.c_void_p * len(handles))(*handles)
     T, d = x.shape
     E, _, f = W1.shape
     if y is None:
         y = torch.empty_like(x)
     if workspace is None:
         workspace = Workspace(T, d, f, E, K, x.dtype, dev)
-    rc = _lib.load().moe_forward_timed(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(y), T, d, f, E, K,
-                                       _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
-                                       ctypes.c_void_p(s.cuda_stream), arr)
-    _lib.check("moe_forward_timed", rc)
+    rc = _lib.load().moe_forward_stamped(_ptr(x), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), _ptr(y), T, d, f, E, K,
+                                         _dtype_code(x), workspace.ptr(), workspace.nbytes, flags,
+                                         _stream_ptr(stream, dev), _stamps_arg(stamps, dev))
+    _lib.check("moe_forward_stamped", rc)
     return y
+
+
+def moe_block_forward_stamped(h, Wg, W1, W3, W2, K: int, stamps, eps: float = 1e-5,
+                              workspace: Workspace | None = None, flags: int = 0, stream=None):
+    """moe_block_forward with stage timestamps (see moe_forward_stamped)."""
+    dev = h.device
+    T, d = h.shape
+    E, _, f = W1.shape
+    if workspace is None:
+        workspace = Workspace(T, d, f, E, K, h.dtype, dev)
+    rc = _lib.load().moe_block_forward_stamped(_ptr(h), _ptr(Wg), _ptr(W1), _ptr(W3), _ptr(W2), T, d, f, E, K,
+                                               _dtype_code(h), float(eps), workspace.ptr(), workspace.nbytes, flags,
+                                               _stream_ptr(stream, dev), _stamps_arg(stamps, dev))
+    _lib.check("moe_block_forward_stamped", rc)
+    return h
 
 
 def moe_forward_host(x_host, y_host, Wg, W1, W3, W2, K: int = 2, x_dev=None, y_dev=None,
@@ -219,23 +252,17 @@ def moe_forward_fp8(x, Wg, W1q, s1, W3q, s3, W2q, s2, K: int = 2, y=None, worksp
     return y
 
 
-def moe_forward_fp8_timed(x, Wg, W1q, s1, W3q, s3, W2q, s2, K: int, events, y=None,
-                          workspace: Workspace | None = None, flags: int = 0, stream=None):
-    """moe_forward_fp8 recording the seven stage events (see moe_forward_timed)."""
+def moe_forward_fp8_stamped(x, Wg, W1q, s1, W3q, s3, W2q, s2, K: int, stamps, y=None,
+                            workspace: Workspace | None = None, flags: int = 0, stream=None):
+    """moe_forward_fp8 with stage timestamps (see moe_forward_stamped)."""
     T, d, f, E, y = _fp8_args(x, Wg, W1q, s1, W3q, s3, W2q, s2, y)
-    s = stream if stream is not None else torch.cuda.current_stream(x.device)
-    handles = []
-    for ev in events:
-        if ev.cuda_event == 0:
-            ev.record(s)
-        handles.append(ev.cuda_event)
-    arr = (ctypes.c_void_p * len(handles))(*handles)
     if workspace is None:
         workspace = Workspace(T, d, f, E, K, torch.float8_e4m3fn, x.device)
-    rc = _lib.load().moe_forward_fp8_timed(_ptr(x), _ptr(Wg), _ptr(W1q), _ptr(s1), _ptr(W3q), _ptr(s3), _ptr(W2q),
-                                           _ptr(s2), _ptr(y), T, d, f, E, K, workspace.ptr(), workspace.nbytes,
-                                           flags, ctypes.c_void_p(s.cuda_stream), arr)
-    _lib.check("moe_forward_fp8_timed", rc)
+    rc = _lib.load().moe_forward_fp8_stamped(_ptr(x), _ptr(Wg), _ptr(W1q), _ptr(s1), _ptr(W3q), _ptr(s3),
+                                             _ptr(W2q), _ptr(s2), _ptr(y), T, d, f, E, K, workspace.ptr(),
+                                             workspace.nbytes, flags, _stream_ptr(stream, x.device),
+                                             _stamps_arg(stamps, x.device))
+    _lib.check("moe_forward_fp8_stamped", rc)
     return y
 
 

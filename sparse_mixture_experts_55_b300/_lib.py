@@ -26,8 +26,9 @@ MOE_F32 = 1
 MOE_FP8_E4M3 = 2
 
 MOE_ACCUMULATE = 0x1
-MOE_NUM_STAGE_EVENTS = 7
-STAGES = ("route", "group", "gather", "gate_up_gemm", "down_gemm", "combine")
+# stage slots of a stamps array (moe_forward_stamped), in order
+MOE_NUM_STAGES = 8
+STAGES = ("route", "group", "gather", "gate_up_gemm", "quant_h", "down_gemm", "combine", "rmsnorm")
 MOE_DEBUG_CHECKS = 0x2
 MOE_DEBUG_FORCE_TIMEOUT = 0x4
 MOE_GEMM_PAIR_MMA = 0x8
@@ -52,13 +53,15 @@ SIGNATURES = {
     "moe_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_forward_launches": (_i, [_i, _i, _i, _i, _i, _i]),
     "moe_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
-    "moe_forward_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp, _vp]),
+    "moe_forward_stamped": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp, _vp]),
     "moe_block_forward": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _sz, _u,
                                 _vp]),
+    "moe_block_forward_stamped": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _sz,
+                                        _u, _vp, _vp]),
     "moe_quantize_weights_fp8": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
     "moe_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
-    "moe_forward_fp8_timed": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp,
-                                   _vp]),
+    "moe_forward_fp8_stamped": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u,
+                                     _vp, _vp]),
     "moe_train_workspace_bytes": (_sz, [_i, _i, _i, _i, _i, _i]),
     "moe_forward_train": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
     "moe_backward": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz, _u,
@@ -70,7 +73,8 @@ SIGNATURES = {
     "moe_forward_cached": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _cp, _vp, _i, _i, _i, _i, _i, _i, _vp, _sz,
                                 _u, _vp]),
     "moe_route": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
-    "moe_route_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "moe_route_noalloc": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _u, _vp]),
+    "moe_route_noalloc_status": (_i, [_vp]),
     "moe_rmsnorm": (_i, [_vp, _vp, _i, _i, ctypes.c_float, _i, _vp]),
     "moe_read_status": (_i, [_vp, _vp]),
     "moe_status_string": (ctypes.c_char_p, [_i]),

@@ -44,10 +44,9 @@ def up_to_date() -> bool:
 def build(force: bool = False, verbose: bool = False) -> pathlib.Path:
     if not force and up_to_date():
         return LIB
-    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17", "--use_fast_math=false",
+    cmd = [nvcc(), *ARCH, "-O3", "-lineinfo", "-std=c++17",
            "-Xcompiler", "-fPIC,-fvisibility=hidden", "-shared", "-cudart", "static",
            "-I", str(INCLUDE), "-o", str(LIB) + ".tmp", *map(str, sources())]
-    cmd = [c for c in cmd if c != "--use_fast_math=false"]
     if verbose:
         cmd.insert(1, "-Xptxas=-v")
         print(" ".join(cmd), flush=True)

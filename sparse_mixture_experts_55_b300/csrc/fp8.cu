@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "stamps.cuh"
 
 namespace moe {
 namespace {
@@ -141,10 +142,11 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
                                                            const int32_t *__restrict__ perm_tok,
                                                            const int32_t *__restrict__ poffsets, int E,
                                                            uint8_t *__restrict__ xq, float *__restrict__ xs,
-                                                           int *status) {
+                                                           int *status, unsigned long long *stamps) {
   __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
+  stamp_begin(stamps, ST_GATHER);
   const Team<BLOCK_TEAM> tm;
   const int rows = poffsets[E];
   const int nchunk = d / 8;  // 8 bf16 in, 8 codes out
@@ -167,6 +169,7 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
     for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(__ldg(src + c), s);
     if (tm.rank == 0) xs[r] = s;
   }
+  stamp_end(stamps, ST_GATHER);
 }
 
 // Hq[r, :] = e4m3(H[r, :] / hs[r]) for every real grouped row, with hs[r] =
@@ -179,10 +182,12 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__res
                                                       const float *__restrict__ habs, int n_tiles,
                                                       const int32_t *__restrict__ offsets,
                                                       const int32_t *__restrict__ poffsets, int E,
-                                                      uint8_t *__restrict__ hq, float *__restrict__ hs) {
+                                                      uint8_t *__restrict__ hq, float *__restrict__ hs,
+                                                      unsigned long long *stamps) {
   __shared__ float red[8];
   pdl_wait();
   pdl_trigger();
+  stamp_begin(stamps, ST_QUANT_H);
   const Team<BLOCK_TEAM> tm;
   const int rows = poffsets[E];
   const int nchunk = f / 8;
@@ -199,6 +204,7 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__res
     for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], s);
     if (tm.rank == 0) hs[r] = s;
   }
+  stamp_end(stamps, ST_QUANT_H);
 }
 
 }  // namespace
@@ -228,7 +234,7 @@ cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const
                        0, s, true,
                        static_cast<const __nv_bfloat16 *>(x), T, d, static_cast<const int32_t *>(P.perm_tok),
                        static_cast<const int32_t *>(P.poffsets), E, static_cast<uint8_t *>(P.xperm), P.xscale,
-                       P.status);
+                       P.status, P.stamps);
 }
 
 cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
@@ -239,7 +245,7 @@ cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int 
   return launch_kernel(block_team ? quant_h_kernel<true> : quant_h_kernel<false>, dim3(blocks), dim3(256), 0, s, true,
                        static_cast<const __nv_bfloat16 *>(P.hbuf), f, static_cast<const float *>(P.habs), n_tiles,
                        static_cast<const int32_t *>(P.offsets), static_cast<const int32_t *>(P.poffsets), E,
-                       static_cast<uint8_t *>(P.hq), P.hscale);
+                       static_cast<uint8_t *>(P.hq), P.hscale, P.stamps);
 }
 
 }  // namespace moe

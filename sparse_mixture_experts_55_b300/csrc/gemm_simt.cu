@@ -9,6 +9,7 @@
 #include <cuda_runtime.h>
 
 #include "internal.h"
+#include "stamps.cuh"
 
 namespace moe {
 namespace {
@@ -20,12 +21,14 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float *__restrict__ 
                                                       const float *__restrict__ B1, int k_total, int n_out,
                                                       const int32_t *__restrict__ poffsets,
                                                       const int32_t *__restrict__ offsets, int E,
-                                                      const float *__restrict__ perm_gate, float *__restrict__ out) {
+                                                      const float *__restrict__ perm_gate, float *__restrict__ out,
+                                                      unsigned long long *stamps) {
   __shared__ float As[TK][TM];
   __shared__ float Bs0[TK][TN];
   __shared__ float Bs1[GATE_UP ? TK : 1][GATE_UP ? TN : 1];
   const int row0 = blockIdx.y * TM;
-  if (row0 >= poffsets[E]) return;
+  if (row0 >= poffsets[E]) return;  // whole block
+  stamp_begin(stamps, GATE_UP ? ST_GATE_UP : ST_DOWN);
   int e = 0;
   while (row0 >= poffsets[e + 1]) ++e;
   const int n0 = blockIdx.x * TN;
@@ -86,22 +89,22 @@ __global__ void __launch_bounds__(256) ffn_f32_kernel(const float *__restrict__ 
       out[static_cast<size_t>(r_out) * n_out + n] = v;
     }
   }
+  stamp_end(stamps, GATE_UP ? ST_GATE_UP : ST_DOWN);
 }
 
 }  // namespace
 
 cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,
-                                  const WsLayout &L, const Ptrs &P, cudaStream_t s, void *const *mid_event) {
+                                  const WsLayout &L, const Ptrs &P, cudaStream_t s) {
   const dim3 g1((f + TN - 1) / TN, L.R / TM);
   ffn_f32_kernel<true><<<g1, 256, 0, s>>>(static_cast<const float *>(P.xperm), static_cast<const float *>(W1),
                                           static_cast<const float *>(W3), d, f, P.poffsets, P.offsets, E, P.perm_gate,
-                                          static_cast<float *>(P.hbuf));
+                                          static_cast<float *>(P.hbuf), P.stamps);
   cudaError_t err = cudaGetLastError();
-  if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
   const dim3 g2((d + TN - 1) / TN, L.R / TM);
   ffn_f32_kernel<false><<<g2, 256, 0, s>>>(static_cast<const float *>(P.hbuf), static_cast<const float *>(W2),
-                                           nullptr, f, d, P.poffsets, P.offsets, E, P.perm_gate, P.obuf);
+                                           nullptr, f, d, P.poffsets, P.offsets, E, P.perm_gate, P.obuf, P.stamps);
   return cudaGetLastError();
 }
 

@@ -67,6 +67,7 @@
 
 #include "internal.h"
 #include "ptx.cuh"
+#include "stamps.cuh"
 #include "tc_common.cuh"
 
 namespace moe {
@@ -150,6 +151,7 @@ struct GemmArgs {
   const int32_t *perm_tok;  // [R] token of each padded grouped row
   int *tok_cnt;             // [T, num_n_tiles], zero at launch
   int T, K;
+  unsigned long long *stamps;  // profiling calls: stage begin/end times (stamps.cuh), else null
 };
 
 struct Ctrl {
@@ -317,6 +319,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // dependent launch); its outputs are read only after this wait.
   ptx::grid_dependency_wait();
   ptx::allow_dependent_launch();
+  constexpr int kStage = MODE == MODE_GATE_UP ? ST_GATE_UP : ST_DOWN;
+  stamp_begin(args.stamps, kStage);
   if (threadIdx.x == 0) {
     // Unit table from the padded segment offsets written by the grouping kernel.
     int acc = 0;
@@ -935,6 +939,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (PAIR) ptx::tmem_dealloc_pair(tmem, TMEM_COLS);  // with the peer CTA's warp 1
     else ptx::tmem_dealloc(tmem, TMEM_COLS);
   }
+  if (args.stamps != nullptr && threadIdx.x == 0) atomicMax(args.stamps + kNumStages + kStage, stamp_now());
 }
 
 // ---------------------------------------------------------------- host side
@@ -1067,7 +1072,7 @@ void set_fused_combine(GemmArgs &g, const WsLayout &L, const Ptrs &P, void *y, u
 
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, void *y, unsigned flags, int num_sms,
-                                     cudaStream_t s, void *const *mid_event, const int *slot_of, int n_slots) {
+                                     cudaStream_t s, const int *slot_of, int n_slots) {
   Grids grids;
   cudaError_t err = device_state(num_sms, &grids);
   if (err != cudaSuccess) return err;
@@ -1102,8 +1107,8 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.status = P.status;
   g1.use_slots = slot_of ? 1 : 0;
   for (int e = 0; e < E && slot_of; ++e) g1.wslot[e] = slot_of[e];
+  g1.stamps = P.stamps;
   err = launch_form<MODE_GATE_UP, false>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
-  if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -1119,13 +1124,12 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
-  return launch_form<MODE_DOWN, false>(form, grids, s, mid_event == nullptr, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
+  return launch_form<MODE_DOWN, false>(form, grids, s, true, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 
 cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
                                     const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
-                                    const Ptrs &P, void *y, unsigned flags, int num_sms, cudaStream_t s,
-                                    void *const *mid_event) {
+                                    const Ptrs &P, void *y, unsigned flags, int num_sms, cudaStream_t s) {
   Grids grids;
   cudaError_t err = device_state(num_sms, &grids);
   if (err != cudaSuccess) return err;
@@ -1160,10 +1164,10 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g1.col_scale1 = s3;
   g1.habs = P.habs;
   g1.status = P.status;
+  g1.stamps = P.stamps;
   err = launch_form<MODE_GATE_UP, true>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
-  // H rows to e4m3 with their own scales, inside the gate/up stage
+  // H rows to e4m3 with their own scales
   if (err == cudaSuccess) err = launch_quant_h(f, E, L.R, g1.num_n_tiles, P, num_sms, s);
-  if (err == cudaSuccess && mid_event) err = cudaEventRecord(static_cast<cudaEvent_t>(*mid_event), s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;
@@ -1182,7 +1186,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g2.col_scale0 = s2;
   g2.col_scale1 = nullptr;
   g2.habs = nullptr;
-  return launch_form<MODE_DOWN, true>(form, grids, s, mid_event == nullptr, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
+  return launch_form<MODE_DOWN, true>(form, grids, s, true, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 
 }  // namespace moe

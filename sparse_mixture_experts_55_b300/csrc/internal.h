@@ -24,6 +24,14 @@ constexpr int kMaxE = 32;
 constexpr int kMaxK = 2;
 // Status-word slots at the start of the workspace.
 constexpr int kStatusInts = 8;
+// Stages of a forward pass, as indexed in a stamps array (stamps.cuh).
+enum Stage {
+  ST_ROUTE = MOE_STAGE_ROUTE, ST_GROUP = MOE_STAGE_GROUP, ST_GATHER = MOE_STAGE_GATHER,
+  ST_GATE_UP = MOE_STAGE_GATE_UP, ST_QUANT_H = MOE_STAGE_QUANT_H, ST_DOWN = MOE_STAGE_DOWN,
+  ST_COMBINE = MOE_STAGE_COMBINE, ST_NORM = MOE_STAGE_NORM
+};
+constexpr int kNumStages = MOE_NUM_STAGES;
+static_assert(kNumStages == 8, "one stamp pair per stage");
 
 // Launch `kernel` on stream s; with pdl the launch may begin while the
 // previous kernel in the stream finishes (programmatic dependent launch): the
@@ -111,8 +119,17 @@ struct Ptrs {
   float *dxc;       // [T*K, d] dL/dX per unpadded grouped row
   float *dl;        // [T, E] dL/dlogits
   float *dwg_part;  // [dwg_chunks, d, E] partial sums of dL/dWg
+  // profiling calls only: [2 * kNumStages] begin/end times of each stage
+  // (stamps.cuh); null otherwise
+  unsigned long long *stamps;
 };
 Ptrs carve(void *ws, const WsLayout &L);
+
+// Streaming multiprocessors of the current device (148 if it cannot be read).
+int sm_count_or_default();
+// MOE_OK on an sm_103a device, MOE_ERR_UNSUPPORTED on another part,
+// MOE_ERR_CUDA if the device cannot be queried.
+int check_device();
 
 // -------- routing.cu
 cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
@@ -124,10 +141,10 @@ cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsig
                            int num_sms, cudaStream_t s);
 cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate,
                                 int32_t *perm_tok, int32_t *offsets, int32_t *pos, cudaStream_t s);
-cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s);
+cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s,
+                           unsigned long long *stamps = nullptr);
 
 // -------- gemm_tc.cu (bf16 tensor-core path)
-// mid_event (optional): recorded between the gate/up and the down kernel.
 // slot_of (host array of E entries, or null): expert e's matrices are slot
 // slot_of[e] of banks holding n_slots matrices each (the expert cache);
 // without it, slot e of banks of E.
@@ -135,8 +152,7 @@ cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, in
 // (then no combine kernel runs).
 cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void *W2, int d, int f, int E,
                                      const WsLayout &L, const Ptrs &P, void *y, unsigned flags, int num_sms,
-                                     cudaStream_t s, void *const *mid_event, const int *slot_of = nullptr,
-                                     int n_slots = 0);
+                                     cudaStream_t s, const int *slot_of = nullptr, int n_slots = 0);
 
 // -------- fp8.cu (e4m3 expert weights)
 cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, cudaStream_t s);
@@ -146,8 +162,7 @@ cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int 
 // gemm_tc.cu, e4m3 operands: gate/up GEMM, H quantisation, down GEMM
 cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
                                     const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
-                                    const Ptrs &P, void *y, unsigned flags, int num_sms, cudaStream_t s,
-                                    void *const *mid_event);
+                                    const Ptrs &P, void *y, unsigned flags, int num_sms, cudaStream_t s);
 
 // -------- gemm_simt.cu (exact fp32 path)
 // -------- backward.cu / gemm_bwd.cu (bf16, d and f multiples of 64)
@@ -162,6 +177,6 @@ cudaError_t launch_bwd_input(const void *x, const void *Wg, void *dx, void *dWg,
                              void *const *events);
 
 cudaError_t launch_expert_ffn_f32(const void *W1, const void *W3, const void *W2, int d, int f, int E,
-                                  const WsLayout &L, const Ptrs &P, cudaStream_t s, void *const *mid_event);
+                                  const WsLayout &L, const Ptrs &P, cudaStream_t s);
 
 }  // namespace moe

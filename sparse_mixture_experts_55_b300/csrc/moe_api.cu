@@ -86,6 +86,22 @@ int check_shape(int T, int d, int f, int E, int K, int dtype) {
   return MOE_OK;
 }
 
+
+// Profiling calls: reset a stamps array on the stream (begin times to all
+// ones, end times to zero) so that the stages' atomic min / max start clean.
+cudaError_t reset_stamps(unsigned long long *stamps, cudaStream_t s) {
+  if (stamps == nullptr) return cudaSuccess;
+  cudaError_t err = cudaMemsetAsync(stamps, 0xff, kNumStages * sizeof(unsigned long long), s);
+  if (err == cudaSuccess) err = cudaMemsetAsync(stamps + kNumStages, 0, kNumStages * sizeof(unsigned long long), s);
+  return err;
+}
+
+bool stamps_ok(const unsigned long long *stamps) {
+  return stamps != nullptr && (reinterpret_cast<uintptr_t>(stamps) & 7u) == 0;
+}
+
+}  // namespace
+
 int sm_count_or_default() {
   DevInfo di;
   return device_info(di) ? di.sms : kDefaultSms;
@@ -98,8 +114,6 @@ int check_device() {
   if (di.major != 10 || di.minor != 3) return MOE_ERR_UNSUPPORTED;
   return MOE_OK;
 }
-
-}  // namespace
 
 SplitPlan plan_splits(long long TK, int E, int n_tiles, int kb, int clusters, double part_ratio) {
   SplitPlan best{1, kb};
@@ -258,6 +272,7 @@ Ptrs carve(void *ws, const WsLayout &L) {
   P.dxc = L.train ? reinterpret_cast<float *>(b + L.dxc) : nullptr;
   P.dl = L.train ? reinterpret_cast<float *>(b + L.dl) : nullptr;
   P.dwg_part = L.train ? reinterpret_cast<float *>(b + L.dwg_part) : nullptr;
+  P.stamps = nullptr;
   return P;
 }
 
@@ -284,7 +299,8 @@ static int check_train_shape(int T, int d, int f, int E, int K, int dtype) {
 
 static int forward_impl(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
                         int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
-                        unsigned flags, moe_stream_t stream, void *const *events, bool train = false) {
+                        unsigned flags, moe_stream_t stream, unsigned long long *stamps, bool train = false,
+                        bool stamps_reset = true) {
   if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;  // e4m3 weights go through moe_forward_fp8
   int st = train ? check_train_shape(T, d, f, E, K, dtype) : check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
@@ -305,30 +321,22 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   st = check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const Ptrs P = carve(workspace, L);
+  Ptrs P = carve(workspace, L);
+  P.stamps = stamps;
   // status word and split-tile counters start at zero
   if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (stamps_reset && reset_stamps(stamps, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  // events (optional): one before the router and one after each of the six stages
-  auto mark = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
-  };
-  cudaError_t err = mark(0);
-  if (err == cudaSuccess) err = launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s);
-  if (err == cudaSuccess) err = mark(1);
+  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s);
   if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
-  if (err == cudaSuccess) err = mark(2);
   if (err == cudaSuccess) err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
-  if (err == cudaSuccess) err = mark(3);
   if (err == cudaSuccess) {
     if (dtype == MOE_BF16)
-      err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, y, flags, sms, s, events ? events + 4 : nullptr);
+      err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, y, flags, sms, s);
     else
-      err = launch_expert_ffn_f32(W1, W3, W2, d, f, E, L, P, s, events ? events + 4 : nullptr);
+      err = launch_expert_ffn_f32(W1, W3, W2, d, f, E, L, P, s);
   }
-  if (err == cudaSuccess) err = mark(5);
   if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
-  if (err == cudaSuccess) err = mark(6);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -338,9 +346,9 @@ int moe_forward(const void *x, const void *Wg, const void *W1, const void *W3, c
   return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, nullptr);
 }
 
-int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d, int f,
-                      int E, int K, int dtype, float eps, void *workspace, size_t ws_bytes, unsigned flags,
-                      moe_stream_t stream) {
+static int block_forward_impl(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d,
+                              int f, int E, int K, int dtype, float eps, void *workspace, size_t ws_bytes,
+                              unsigned flags, moe_stream_t stream, unsigned long long *stamps) {
   if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
@@ -355,20 +363,34 @@ int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, c
   st = check_device();
   if (st != MOE_OK) return st;
   const Ptrs P = carve(workspace, L);
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // x_n = RMSNorm(h) into the workspace, then h += MoE(x_n)
-  if (launch_rmsnorm(h, P.xnorm, T, d, eps, dtype, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
-    return MOE_ERR_CUDA;
+  if (reset_stamps(stamps, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_rmsnorm(h, P.xnorm, T, d, eps, dtype, s, stamps) != cudaSuccess) return MOE_ERR_CUDA;
   return forward_impl(P.xnorm, Wg, W1, W3, W2, h, T, d, f, E, K, dtype, workspace, ws_bytes, flags | MOE_ACCUMULATE,
-                      stream, nullptr);
+                      stream, stamps, false, /*stamps_reset=*/false);
 }
 
-int moe_forward_timed(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
-                      int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
-                      unsigned flags, moe_stream_t stream, void *const *events) {
-  if (!events) return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
-    if (!events[i]) return MOE_ERR_INVALID_ARG;
-  return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, events);
+int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d, int f,
+                      int E, int K, int dtype, float eps, void *workspace, size_t ws_bytes, unsigned flags,
+                      moe_stream_t stream) {
+  return block_forward_impl(h, Wg, W1, W3, W2, T, d, f, E, K, dtype, eps, workspace, ws_bytes, flags, stream,
+                            nullptr);
+}
+
+int moe_block_forward_stamped(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d,
+                              int f, int E, int K, int dtype, float eps, void *workspace, size_t ws_bytes,
+                              unsigned flags, moe_stream_t stream, unsigned long long *stamps) {
+  if (!stamps_ok(stamps)) return MOE_ERR_INVALID_ARG;
+  return block_forward_impl(h, Wg, W1, W3, W2, T, d, f, E, K, dtype, eps, workspace, ws_bytes, flags, stream,
+                            stamps);
+}
+
+int moe_forward_stamped(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
+                        int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
+                        unsigned flags, moe_stream_t stream, unsigned long long *stamps) {
+  if (!stamps_ok(stamps)) return MOE_ERR_INVALID_ARG;
+  return forward_impl(x, Wg, W1, W3, W2, y, T, d, f, E, K, dtype, workspace, ws_bytes, flags, stream, stamps);
 }
 
 int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const void *W3_host, const void *W2_host,
@@ -419,8 +441,7 @@ int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const
   cache->bytes_loaded += static_cast<long long>(n_loads) * 3 * static_cast<long long>(mat);
   cudaError_t err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
   if (err == cudaSuccess)
-    err = launch_expert_gemms_bf16(W1_dev, W3_dev, W2_dev, d, f, E, L, P, y, flags, sms, s, nullptr, cache->slot_of,
-                                   cache->C);
+    err = launch_expert_gemms_bf16(W1_dev, W3_dev, W2_dev, d, f, E, L, P, y, flags, sms, s, cache->slot_of, cache->C);
   if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -527,7 +548,7 @@ int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float
 static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
                             const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
                             int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
-                            void *const *events) {
+                            unsigned long long *stamps) {
   constexpr int dtype = MOE_FP8_E4M3;
   int st = check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
@@ -548,25 +569,16 @@ static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, cons
   st = check_device();
   if (st != MOE_OK) return st;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const Ptrs P = carve(workspace, L);
+  Ptrs P = carve(workspace, L);
+  P.stamps = stamps;
   if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-  auto mark = [&](int i) -> cudaError_t {
-    return events ? cudaEventRecord(static_cast<cudaEvent_t>(events[i]), s) : cudaSuccess;
-  };
+  if (reset_stamps(stamps, s) != cudaSuccess) return MOE_ERR_CUDA;
   // routing on the bf16 tokens, as moe_forward; the gather quantises rows
-  cudaError_t err = mark(0);
-  if (err == cudaSuccess) err = launch_route(x, Wg, T, d, E, K, MOE_BF16, flags, L, P, s);
-  if (err == cudaSuccess) err = mark(1);
+  cudaError_t err = launch_route(x, Wg, T, d, E, K, MOE_BF16, flags, L, P, s);
   if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
-  if (err == cudaSuccess) err = mark(2);
   if (err == cudaSuccess) err = launch_gather_quant(x, T, d, E, L.R, P, sms, s);
-  if (err == cudaSuccess) err = mark(3);
-  if (err == cudaSuccess)
-    err = launch_expert_gemms_fp8(W1q, s1, W3q, s3, W2q, s2, d, f, E, L, P, y, flags, sms, s,
-                                  events ? events + 4 : nullptr);
-  if (err == cudaSuccess) err = mark(5);
+  if (err == cudaSuccess) err = launch_expert_gemms_fp8(W1q, s1, W3q, s3, W2q, s2, d, f, E, L, P, y, flags, sms, s);
   if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, MOE_BF16, flags, P, sms, s);
-  if (err == cudaSuccess) err = mark(6);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -577,15 +589,13 @@ int moe_forward_fp8(const void *x, const void *Wg, const void *W1q, const float 
                           nullptr);
 }
 
-int moe_forward_fp8_timed(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
-                          const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
-                          int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
-                          void *const *events) {
-  if (!events) return MOE_ERR_INVALID_ARG;
-  for (int i = 0; i < MOE_NUM_STAGE_EVENTS; ++i)
-    if (!events[i]) return MOE_ERR_INVALID_ARG;
+int moe_forward_fp8_stamped(const void *x, const void *Wg, const void *W1q, const float *s1, const void *W3q,
+                            const float *s3, const void *W2q, const float *s2, void *y, int T, int d, int f, int E,
+                            int K, void *workspace, size_t ws_bytes, unsigned flags, moe_stream_t stream,
+                            unsigned long long *stamps) {
+  if (!stamps_ok(stamps)) return MOE_ERR_INVALID_ARG;
   return forward_fp8_impl(x, Wg, W1q, s1, W3q, s3, W2q, s2, y, T, d, f, E, K, workspace, ws_bytes, flags, stream,
-                          events);
+                          stamps);
 }
 
 int moe_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, int32_t *idx, float *gate,

@@ -16,6 +16,7 @@
 #include <cstdint>
 
 #include "internal.h"
+#include "stamps.cuh"
 
 namespace moe {
 namespace {
@@ -201,7 +202,7 @@ template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
                  unsigned flags, int32_t *__restrict__ idx, float *__restrict__ gate,
-                 int32_t *__restrict__ blockcounts, int *status) {
+                 int32_t *__restrict__ blockcounts, int *status, unsigned long long *stamps) {
   constexpr int NV = Vec<Tin>::N;
   constexpr int NW = kRouteThreads / 32;
   constexpr int G = kRouteGroup;  // tokens per reduction group
@@ -216,6 +217,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   if (tid < kMaxE) s_cnt[tid] = 0;
   pdl_wait();
   pdl_trigger();
+  stamp_begin(stamps, ST_ROUTE);
 
   const bool own = tid < nchunks;
   float w[kCached ? NV : 1][kCached ? EP : 1];
@@ -260,6 +262,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   }
   __syncthreads();
   if (tid < E) blockcounts[blockIdx.x * E + tid] = s_cnt[tid];
+  stamp_end(stamps, ST_ROUTE);
 }
 
 // Stable grouping.  Block b ranks the (token, slot) entries of tokens
@@ -272,7 +275,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 __global__ void __launch_bounds__(kGroupTokens *kMaxK)
     group_kernel(int T, int E, int K, int nb_route, int tpb, unsigned flags, const int32_t *__restrict__ idx,
                  const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
-                 int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status) {
+                 int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status,
+                 unsigned long long *stamps) {
   constexpr int NT = kGroupTokens * kMaxK;
   constexpr int NW = NT / 32;
   __shared__ int s_base[kMaxE], s_tot[kMaxE], s_off[kMaxE + 1], s_poff[kMaxE + 1];
@@ -284,6 +288,7 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
   __syncthreads();
   pdl_wait();
   pdl_trigger();
+  stamp_begin(stamps, ST_GROUP);
   // entries ahead of this chunk: whole router blocks from their histograms,
   // plus the part of the router block it starts in, counted from idx
   const int tok0 = b * kGroupTokens;
@@ -343,6 +348,7 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
     }
   }
   (void)flags;
+  stamp_end(stamps, ST_GROUP);
 }
 
 // X_perm[r, :] = x[perm_tok[r], :] for every grouped row; pad rows are zeroed.
@@ -350,9 +356,11 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
 __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x, int T, int vec_per_row,
                                                      const int32_t *__restrict__ perm_tok,
                                                      const int32_t *__restrict__ poffsets, int E,
-                                                     uint4 *__restrict__ xperm, int *status) {
+                                                     uint4 *__restrict__ xperm, int *status,
+                                                     unsigned long long *stamps) {
   pdl_wait();
   pdl_trigger();
+  stamp_begin(stamps, ST_GATHER);
   const int rows = poffsets[E];
   const int lane = threadIdx.x & 31;
   const int gw = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -380,6 +388,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x
       for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
     }
   }
+  stamp_end(stamps, ST_GATHER);
 }
 
 __device__ __forceinline__ void store4(float *p, float4 v) { *reinterpret_cast<float4 *>(p) = v; }
@@ -406,9 +415,10 @@ template <typename Tout>
 __global__ void __launch_bounds__(256) combine_kernel(Tout *__restrict__ y, int T, int d, int K, int S,
                                                       long long split_stride, const float *__restrict__ obuf,
                                                       const int32_t *__restrict__ pos, int rows_bound,
-                                                      unsigned flags, int *status) {
+                                                      unsigned flags, int *status, unsigned long long *stamps) {
   pdl_wait();
   pdl_trigger();
+  stamp_begin(stamps, ST_COMBINE);
   const int q = d >> 2;
   const long long total = static_cast<long long>(T) * q;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -441,6 +451,7 @@ __global__ void __launch_bounds__(256) combine_kernel(Tout *__restrict__ y, int 
     }
     store4(dst, acc);
   }
+  stamp_end(stamps, ST_COMBINE);
 }
 
 // Unpadded copies of the routing results for moe_route.
@@ -464,8 +475,10 @@ __global__ void route_export_kernel(int T, int E, int K, const int32_t *__restri
 
 // out = x / sqrt(mean(x^2) + eps) per row; one block per row, fp32 sums.
 template <typename T>
-__global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T *__restrict__ out, int d, float eps) {
+__global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T *__restrict__ out, int d, float eps,
+                                                      unsigned long long *stamps) {
   __shared__ float s_red[8];
+  stamp_begin(stamps, ST_NORM);
   const T *row = x + static_cast<size_t>(blockIdx.x) * d;
   T *orow = out + static_cast<size_t>(blockIdx.x) * d;
   float ss = 0.f;
@@ -486,6 +499,7 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T
     if constexpr (sizeof(T) == 2) orow[j] = __float2bfloat16_rn(v);
     else orow[j] = v;
   }
+  stamp_end(stamps, ST_NORM);
 }
 
 }  // namespace
@@ -501,23 +515,24 @@ cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int
     auto *ww = static_cast<const __nv_bfloat16 *>(Wg);
     if (E <= 8)
       return launch_kernel(route_kernel<__nv_bfloat16, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags,
-                           P.idx, P.gate, P.blockcounts, P.status);
+                           P.idx, P.gate, P.blockcounts, P.status, P.stamps);
     return launch_kernel(route_kernel<__nv_bfloat16, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags,
-                         P.idx, P.gate, P.blockcounts, P.status);
+                         P.idx, P.gate, P.blockcounts, P.status, P.stamps);
   }
   auto *xx = static_cast<const float *>(x);
   auto *ww = static_cast<const float *>(Wg);
   if (E <= 8)
     return launch_kernel(route_kernel<float, 8>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags, P.idx,
-                         P.gate, P.blockcounts, P.status);
+                         P.gate, P.blockcounts, P.status, P.stamps);
   return launch_kernel(route_kernel<float, 32>, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags, P.idx,
-                       P.gate, P.blockcounts, P.status);
+                       P.gate, P.blockcounts, P.status, P.stamps);
 }
 
 cudaError_t launch_group(int T, int E, int K, const WsLayout &L, unsigned flags, const Ptrs &P, cudaStream_t s) {
   const dim3 grid((T + kGroupTokens - 1) / kGroupTokens), block(kGroupTokens * kMaxK);
   return launch_kernel(group_kernel, grid, block, 0, s, true, T, E, K, L.n_route_blocks, L.route_tpb, flags, P.idx,
-                       P.gate, P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status);
+                       P.gate, P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status,
+                       P.stamps);
 }
 
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
@@ -529,7 +544,7 @@ cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, 
   if (blocks < 1) blocks = 1;
   return launch_kernel(gather_kernel, dim3(blocks), dim3(256), 0, s, true, static_cast<const uint4 *>(x), T,
                        vec_per_row, static_cast<const int32_t *>(P.perm_tok), static_cast<const int32_t *>(P.poffsets),
-                       E, static_cast<uint4 *>(P.xperm), P.status);
+                       E, static_cast<uint4 *>(P.xperm), P.status, P.stamps);
 }
 
 cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsigned flags, const Ptrs &P,
@@ -543,10 +558,10 @@ cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsig
   if (dtype == MOE_BF16)
     return launch_kernel(combine_kernel<__nv_bfloat16>, grid, block, 0, s, true, static_cast<__nv_bfloat16 *>(y), T,
                          d, K, S, split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos),
-                         T * K, flags, P.status);
+                         T * K, flags, P.status, P.stamps);
   return launch_kernel(combine_kernel<float>, grid, block, 0, s, true, static_cast<float *>(y), T, d, K, S,
                        split_stride, static_cast<const float *>(P.obuf), static_cast<const int32_t *>(P.pos), T * K,
-                       flags, P.status);
+                       flags, P.status, P.stamps);
 }
 
 cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate, int32_t *perm_tok,
@@ -560,13 +575,14 @@ cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx
                        static_cast<const int32_t *>(P.poffsets), idx, gate, perm_tok, offsets, pos);
 }
 
-cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s) {
+cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s,
+                           unsigned long long *stamps) {
   if (T == 0) return cudaSuccess;
   if (dtype == MOE_BF16)
     rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                     static_cast<__nv_bfloat16 *>(out), d, eps);
+                                                     static_cast<__nv_bfloat16 *>(out), d, eps, stamps);
   else
-    rmsnorm_kernel<float><<<T, 256, 0, s>>>(static_cast<const float *>(x), static_cast<float *>(out), d, eps);
+    rmsnorm_kernel<float><<<T, 256, 0, s>>>(static_cast<const float *>(x), static_cast<float *>(out), d, eps, stamps);
   return cudaGetLastError();
 }
 

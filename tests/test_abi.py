@@ -28,12 +28,13 @@ def lib():
 
 def test_header_declares_the_boundary():
     names = _header_functions()
-    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_timed", "moe_block_forward", "moe_route",
-                            "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_timed",
+    assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_stamped", "moe_block_forward",
+                            "moe_block_forward_stamped", "moe_route",
+                            "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_stamped",
                             "moe_train_workspace_bytes", "moe_forward_train", "moe_backward", "moe_backward_timed",
                             "moe_expert_cache_init", "moe_expert_cache_plan", "moe_forward_cached",
                             "moe_forward_launches",
-                            "moe_route_noalloc", "moe_rmsnorm",
+                            "moe_route_noalloc", "moe_route_noalloc_status", "moe_rmsnorm",
                             "moe_read_status", "moe_status_string", "moe_version"])
 
 

