@@ -929,24 +929,25 @@ class LayerRunner:
     """The forward of one configuration (bf16 or e4m3 weights) through the C
     ABI, plain or stamped, with its own workspace."""
 
-    def __init__(self, moe, c, x, weights, q8, dev, stream):
+    def __init__(self, moe, c, x, weights, q8, dev, stream, flags=0):
         T, d, f, E, K = c["T"], c["d"], c["f"], c["E"], c["K"]
         self.moe, self.x, self.w, self.q8, self.K, self.stream = moe, x, weights, q8, K, stream
+        self.flags = flags
         self.ws = moe.Workspace(T, d, f, E, K, torch.float8_e4m3fn if q8 else torch.bfloat16, dev)
         self.y = torch.empty_like(x)
 
     def __call__(self, stamps=None):
         m, Wg = self.moe, self.w[0]
+        kw = dict(y=self.y, workspace=self.ws, flags=self.flags, stream=self.stream)
         if self.q8 is not None:
             if stamps is None:
-                m.moe_forward_fp8(self.x, Wg, *self.q8, self.K, y=self.y, workspace=self.ws, stream=self.stream)
+                m.moe_forward_fp8(self.x, Wg, *self.q8, self.K, **kw)
             else:
-                m.moe_forward_fp8_stamped(self.x, Wg, *self.q8, self.K, stamps, y=self.y, workspace=self.ws,
-                                          stream=self.stream)
+                m.moe_forward_fp8_stamped(self.x, Wg, *self.q8, self.K, stamps, **kw)
         elif stamps is None:
-            m.moe_forward(self.x, *self.w, self.K, y=self.y, workspace=self.ws, stream=self.stream)
+            m.moe_forward(self.x, *self.w, self.K, **kw)
         else:
-            m.moe_forward_stamped(self.x, *self.w, self.K, stamps, y=self.y, workspace=self.ws, stream=self.stream)
+            m.moe_forward_stamped(self.x, *self.w, self.K, stamps, **kw)
 
 
 def timed_region(moe, run, steps: int, dev, stream, stamped: bool):
@@ -972,7 +973,9 @@ def decode_record(moe, weights, q8, dev, stream, steps: int, warmup: int, peaks,
     the stamped layer over `steps` forwards of that batch through the prefill
     weights: ms per step, algorithmic bytes (touched experts' weights once)
     per second against the measured HBM copy bandwidth, and the same for each
-    expert GEMM from its in-run kernel span."""
+    expert GEMM from its in-run kernel span (which starts when the kernel
+    issues its first weight copies, possibly before the previous kernel has
+    finished; negative launch gaps are that overlap)."""
     out = {}
     for T in (1, 8, 32, 128):
         c = dict(CONFIGS[f"decode{T}"], fp8=fp8)
@@ -1016,11 +1019,20 @@ def run_ours(args):
     steps, warmup = args.steps, max(args.warmup, 3)
     # e4m3 expert weights: quantised once before timing (weight preparation)
     q8 = [t for W_ in (inp.W1, inp.W3, inp.W2) for t in moe.quantize_weights_fp8(W_)] if fp8 else None
-    run = LayerRunner(moe, c, inp.x, weights, q8, dev, stream)
+    form_flags = {"auto": 0, "pair": moe.MOE_GEMM_PAIR_MMA, "mc2": moe.MOE_GEMM_MULTICAST_PAIRS,
+                  "quad": moe.MOE_GEMM_QUAD}[args.gemm_form]
+    run = LayerRunner(moe, c, inp.x, weights, q8, dev, stream, form_flags)
 
     # touched experts of this routing (algorithmic bytes at decode sizes)
     route_idx, _, _, offs, _ = moe.moe_route(inp.x, inp.Wg, K)
     n_touched = int(((offs[1:] - offs[:-1]) > 0).sum())
+
+    # the decode half of the metric first (light on power), then a pause, so
+    # that neither set of numbers is taken in the other's power-management tail
+    decode = None
+    if args.config in ("prefill", "prefill_fp8") and not args.no_decode:
+        decode = decode_record(moe, weights, q8, dev, stream, max(steps, 100), warmup, load_peaks()[0], fp8)
+        time.sleep(1.0)
 
     for _ in range(warmup):
         run()
@@ -1110,10 +1122,12 @@ def run_ours(args):
                   "call": "moe_forward_fp8" if fp8 else "moe_forward", "region": "the next K steps, unstamped"},
         "clocks": clocks,
     }
+    if args.gemm_form != "auto":
+        line["config"]["gemm_form"] = args.gemm_form
     if not hbm_bound:
         line["tflops_frac_of_peak"] = line["tflops"] / roof["peak"]
-    if args.config in ("prefill", "prefill_fp8") and not args.no_decode:
-        line["decode"] = decode_record(moe, weights, q8, dev, stream, max(steps, 20), warmup, peaks, fp8)
+    if decode is not None:
+        line["decode"] = decode
     if not args.no_cpu_baseline and not fp8:
         n_tok = min(T, args.cpu_tokens)
         rate, dt, threads, y_ref = cpu_oracle_rate(inp, n_tok)
@@ -1134,6 +1148,8 @@ def main():
     ap.add_argument("--cpu-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-decode", action="store_true", help="omit the decode sweep of the prefill line")
+    ap.add_argument("--gemm-form", default="auto", choices=["auto", "pair", "mc2", "quad"],
+                    help="expert-GEMM form (the library's MOE_GEMM_* flags; results are identical)")
     args = ap.parse_args()
     if args.steps is None:
         args.steps = 10 if args.config == "stack32" else 100

@@ -110,10 +110,12 @@ MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype)
 
 /*
  * Number of kernels one moe_forward (dtype MOE_BF16 or MOE_F32) or
- * moe_forward_fp8 (dtype MOE_FP8_E4M3) call with these sizes enqueues: 5 when
- * the down GEMM's epilogue forms y (bf16 and e4m3 calls whose down projection
- * is not split over its contraction), 6 otherwise, one more for e4m3 (the H
- * quantiser); 0 for T = 0 or invalid sizes.  Host only.
+ * moe_forward_fp8 (dtype MOE_FP8_E4M3) call with these sizes enqueues: the
+ * router and the grouping (one launch for T <= 256, two above), the row
+ * gather, the two expert GEMMs, one more for e4m3 (the H quantiser), and a
+ * combine kernel unless the down GEMM's epilogue forms y (bf16 and e4m3 calls
+ * whose down projection is not split over its contraction); 0 for T = 0 or
+ * invalid sizes.  Host only.
  */
 MOE_API int moe_forward_launches(int T, int d, int f, int E, int K, int dtype);
 
@@ -152,9 +154,10 @@ MOE_API int moe_forward(const void *x, const void *Wg, const void *W1, const voi
  * stamps[MOE_NUM_STAGES + s] to the time it finishes, so for a stage that ran,
  * stamps[MOE_NUM_STAGES + s] - stamps[s] is its kernel's span in ns.
  *   stamps: DEVICE array of 2 * MOE_NUM_STAGES unsigned 64-bit integers,
- *           8-byte aligned, owned by the caller.  The call first resets it on
- *           the stream (begin times to all ones, end times to zero), so a
- *           stage that did not run reads (UINT64_MAX, 0).
+ *           8-byte aligned, owned by the caller, who initialises it before
+ *           the call (begin times to all ones, end times to zero; the call
+ *           itself enqueues nothing extra), so a stage that did not run
+ *           reads (UINT64_MAX, 0).
  *   Stages: MOE_STAGE_ROUTE router; MOE_STAGE_GROUP grouping; MOE_STAGE_GATHER
  *           row gather (e4m3: gather and quantise); MOE_STAGE_GATE_UP gate/up
  *           expert GEMM with SwiGLU; MOE_STAGE_QUANT_H quantisation of H

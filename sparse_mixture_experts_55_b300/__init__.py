@@ -128,9 +128,12 @@ def moe_block_forward(h, Wg, W1, W3, W2, K: int = 2, eps: float = 1e-5, workspac
 
 
 def new_stamps(n: int = 1, device=None) -> torch.Tensor:
-    """Device buffer for n stamped calls: int64 [n, 2 * MOE_NUM_STAGES] (the
-    library treats each row as unsigned 64-bit begin/end times)."""
-    return torch.zeros((n, 2 * _lib.MOE_NUM_STAGES), dtype=torch.int64, device=device or "cuda")
+    """Device buffer for n stamped calls, initialised as the calls expect:
+    int64 [n, 2 * MOE_NUM_STAGES], begin slots -1 (all ones as unsigned) and
+    end slots 0 (the library treats each row as unsigned 64-bit times)."""
+    st = torch.zeros((n, 2 * _lib.MOE_NUM_STAGES), dtype=torch.int64, device=device or "cuda")
+    st[:, :_lib.MOE_NUM_STAGES] = -1
+    return st
 
 
 def _stamps_arg(stamps: torch.Tensor, device):

@@ -281,9 +281,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint16_t kAll = FormInfo<FORM>::ALL;  // every CTA of the cluster
   using RG = Ring<PAIR>;
   constexpr int STAGES = RG::STAGES;
-  // a k-block is one 128-byte row of A and of B in shared memory: 64 bf16 or
-  // 128 e4m3 elements of the contraction
-  constexpr int KB_ELEMS = FP8 ? 128 : BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;
@@ -315,12 +312,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   }
   // Barriers must be initialised in both CTAs before either signals the other.
   ptx::cluster_sync_all();
-  // Everything above overlaps the previous kernel's tail (programmatic
-  // dependent launch); its outputs are read only after this wait.
-  ptx::grid_dependency_wait();
-  ptx::allow_dependent_launch();
   constexpr int kStage = MODE == MODE_GATE_UP ? ST_GATE_UP : ST_DOWN;
   stamp_begin(args.stamps, kStage);
+  // Everything up to grid_dependency_wait overlaps the previous kernel's tail
+  // (programmatic dependent launch).  The routing arrays read here (segment
+  // offsets) are older: this grid is launched only once every CTA of the
+  // previous kernel has passed its own wait, so the kernel that wrote them
+  // has completed.
   if (threadIdx.x == 0) {
     // Unit table from the padded segment offsets written by the grouping kernel.
     int acc = 0;
@@ -353,6 +351,116 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // Both CTAs of a cluster read the same table, so they leave together.
   if (cluster >= total) return;
 
+  // Producer bookkeeping: stages ever filled, the phase parity of each one's
+  // latest fill, and the ring position after the last fill.
+  uint32_t issued = 0, last_par = 0;
+  int p_stage = 0;
+  uint32_t p_phase = 0;
+  // a k-block is one 128-byte row of A and of B in shared memory: 64 bf16 or
+  // 128 e4m3 elements of the contraction
+  constexpr int KB_ELEMS = FP8 ? 128 : BK;
+  uint64_t pol_a = 0, pol_b = 0;
+  // Stage `st` of k-block k0 of tile t: arm its barrier for all the bytes
+  // that complete it, and issue this CTA's weight (B) and activation (A) copies.
+  auto stage_bar = [&](int st) -> uint64_t * { return &c.full[st]; };
+  auto arm = [&](int st) {
+    // pair MMA: both CTAs' copies complete on the first CTA's barrier, which
+    // expects the bytes of both
+    if (!PAIR || leader) ptx::mbar_arrive_expect_tx(stage_bar(st), RG::STAGE_TX);
+  };
+  auto load_b = [&](int st, const Tile &t, int k0) {
+    uint8_t *b_dst = sB + st * RG::B_BYTES;
+    const int wz = c.wslot[t.e];  // the bank slot holding expert e's weights
+    if (PAIR) {
+      // CTA r holds half r of the 256 B columns (gate/up: W1 for CTA 0, W3 for CTA 1)
+      const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[st]), 0);
+      const CUtensorMap *mb = (MODE == MODE_GATE_UP && rank == 1) ? &tmB1 : &tmB0;
+      const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + rank * (BN / 2);
+      if (FP8) {
+        // e4m3 banks are K-contiguous ([E, N, K]): one 128 x 128 box, 16 KiB
+        ptx::tma_load_3d_pair(b_dst, mb, bar, k0, nb, wz, pol_b);
+      } else {
+        ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, wz, pol_b);
+        ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, wz, pol_b);
+      }
+      return;
+    }
+    uint64_t *bar = stage_bar(st);
+    // B: half h (128 of the 256 columns) of the tile; gate/up half 0 is W1,
+    // half 1 is W3; delivered to the CTAs of the cluster that compute with it
+    auto load_b_half = [&](int h, uint16_t mask) {
+      const CUtensorMap *mb = (MODE == MODE_GATE_UP && h == 1) ? &tmB1 : &tmB0;
+      const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + h * (BN / 2);
+      uint8_t *dst = b_dst + h * (2 * B_CHUNK);
+      if (FP8) {
+        if (mask) ptx::tma_load_3d_mc(dst, mb, bar, k0, nb, wz, mask, pol_b);
+        else ptx::tma_load_3d(dst, mb, bar, k0, nb, wz, pol_b);
+      } else {
+        if (mask) {
+          ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, wz, mask, pol_b);
+          ptx::tma_load_3d_mc(dst + B_CHUNK, mb, bar, nb + 64, k0, wz, mask, pol_b);
+        } else {
+          ptx::tma_load_3d(dst, mb, bar, nb, k0, wz, pol_b);
+          ptx::tma_load_3d(dst + B_CHUNK, mb, bar, nb + 64, k0, wz, pol_b);
+        }
+      }
+    };
+    if (t.npair) {
+      load_b_half(0, 0);  // own n-tile, whole
+      load_b_half(1, 0);
+    } else if (QUAD) {
+      // row i of the 2x2 tiles loads half i of its column's B tile, for both CTAs of that column
+      load_b_half(rank >> 1, uint16_t((1u << (rank & 1)) | (1u << (2 + (rank & 1)))));
+    } else {
+      load_b_half(rank, kBothCtas);  // M-pair: half r, for both CTAs
+    }
+  };
+  auto load_a = [&](int st, const Tile &t, int k0) {
+    uint8_t *a_dst = sA + st * A_BYTES;
+    const int row0 = c.poff[t.e] + t.mt * BM;
+    if (PAIR) {
+      const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[st]), 0);
+      ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, row0, pol_a);
+    } else if (!t.npair && !QUAD) {
+      ptx::tma_load_2d(a_dst, &tmA, stage_bar(st), k0, row0, pol_a);  // M-pair: own A tile
+    } else {
+      // shared A tile: halves (N-pair; 2x2 tiles: the two CTAs of a row)
+      // or quarters (the odd m-tile of the 2x2 form: all four CTAs)
+      const bool quarter = QUAD && t.npair;
+      const int part = quarter ? rank : (QUAD ? (rank & 1) : rank);
+      const int prow = quarter ? 32 : 64;
+      const uint16_t amask = quarter ? uint16_t(0xF) : (QUAD ? uint16_t(0x3 << (rank & 2)) : kBothCtas);
+      ptx::tma_load_2d_mc(a_dst + part * prow * 128, quarter ? &tmA_quarter : &tmA_half, stage_bar(st), k0,
+                          row0 + part * prow, amask, pol_a);
+    }
+  };
+  // The weights do not depend on the previous kernel: the first stages of
+  // this CTA's first unit get their weight copies before the wait, so the
+  // weight stream starts while the previous kernel finishes; their
+  // activation copies follow the wait.
+  int pre_kb = 0;
+  Tile t_first{};
+  int kb_first = 0;
+  if (warp == 0 && lane == 0) {
+    pol_a = ptx::policy_evict_last();
+    pol_b = ptx::policy_evict_normal();
+    ptx::prefetch_tmap(&tmB0);
+    if (MODE == MODE_GATE_UP) ptx::prefetch_tmap(&tmB1);
+    t_first = decode_unit<FORM>(cluster, c, NT, S, rank);
+    kb_first = t_first.s * args.kb_per_split;
+    const int kb_end = min(args.num_kb, kb_first + args.kb_per_split);
+    pre_kb = min(STAGES, kb_end - kb_first);
+    for (int i = 0; i < pre_kb; ++i) {
+      arm(i);
+      load_b(i, t_first, (kb_first + i) * KB_ELEMS);
+    }
+    issued = (1u << pre_kb) - 1u;
+    p_stage = pre_kb % STAGES;
+    p_phase = pre_kb == STAGES ? 1u : 0u;
+  }
+  ptx::grid_dependency_wait();
+  ptx::allow_dependent_launch();
+
   if (warp == 1) {
     if (PAIR) {
       ptx::tmem_alloc_pair(&c.tmem_base, TMEM_COLS);  // with the peer CTA's warp 1
@@ -366,98 +474,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::prefetch_tmap(&tmA);
     if (!PAIR) ptx::prefetch_tmap(&tmA_half);
     if (QUAD) ptx::prefetch_tmap(&tmA_quarter);
-    ptx::prefetch_tmap(&tmB0);
-    if (MODE == MODE_GATE_UP) ptx::prefetch_tmap(&tmB1);
+    // the activations of the stages whose weights went out before the wait
+    for (int i = 0; i < pre_kb; ++i) load_a(i, t_first, (kb_first + i) * KB_ELEMS);
   }
   ptx::tc_fence_before();
   __syncthreads();
   ptx::tc_fence_after();
   const uint32_t tmem = c.tmem_base;
-  // Producer bookkeeping: stages ever filled, the phase parity of each one's
-  // latest fill, and the ring position after the last fill.
-  uint32_t issued = 0, last_par = 0;
-  int p_stage = 0;
-  uint32_t p_phase = 0;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      const uint64_t pol_a = ptx::policy_evict_last();
-      const uint64_t pol_b = ptx::policy_evict_normal();
       bool ok = true;
       for (int u = cluster; ok && u < total; u += nclusters) {
         const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
-        const int row0 = c.poff[t.e] + t.mt * BM;
         const int kb0 = t.s * args.kb_per_split;
         const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = u == cluster ? kb0 + pre_kb : kb0; kb < kb1; ++kb) {
           if (!wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, true)) { ok = false; break; }
-          uint8_t *a_dst = sA + p_stage * A_BYTES;
-          uint8_t *b_dst = sB + p_stage * RG::B_BYTES;
           const int k0 = kb * KB_ELEMS;
-          if (PAIR) {
-            // both CTAs' copies complete on the first CTA's barrier, which
-            // expects the bytes of both; CTA r holds half r of the 256 B
-            // columns (gate/up: W1 for CTA 0, W3 for CTA 1)
-            if (leader) ptx::mbar_arrive_expect_tx(&c.full[p_stage], RG::STAGE_TX);
-            const uint32_t bar = ptx::mapa_shared(ptx::smem_u32(&c.full[p_stage]), 0);
-            ptx::tma_load_2d_pair(a_dst, &tmA, bar, k0, row0, pol_a);
-            const CUtensorMap *mb = (MODE == MODE_GATE_UP && rank == 1) ? &tmB1 : &tmB0;
-            const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + rank * (BN / 2);
-            if (FP8) {
-              // e4m3 banks are K-contiguous ([E, N, K]): one 128 x 128 box, 16 KiB
-              ptx::tma_load_3d_pair(b_dst, mb, bar, k0, nb, c.wslot[t.e], pol_b);
-            } else {
-              ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, c.wslot[t.e], pol_b);
-              ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, c.wslot[t.e], pol_b);
-            }
-          } else {
-            // multicast forms: this CTA's share of the A and B tiles, each
-            // delivered to the CTAs of the cluster that compute with it
-            uint64_t *bar = &c.full[p_stage];
-            ptx::mbar_arrive_expect_tx(bar, RG::STAGE_TX);  // own and multicast-in copies fill the stage
-            if (!t.npair && !QUAD) {
-              ptx::tma_load_2d(a_dst, &tmA, bar, k0, row0, pol_a);  // M-pair: own A tile
-            } else {
-              // shared A tile: halves (N-pair; 2x2 tiles: the two CTAs of a row)
-              // or quarters (the odd m-tile of the 2x2 form: all four CTAs)
-              const bool quarter = QUAD && t.npair;
-              const int part = quarter ? rank : (QUAD ? (rank & 1) : rank);
-              const int prow = quarter ? 32 : 64;
-              const uint16_t amask = quarter ? uint16_t(0xF) : (QUAD ? uint16_t(0x3 << (rank & 2)) : kBothCtas);
-              ptx::tma_load_2d_mc(a_dst + part * prow * 128, quarter ? &tmA_quarter : &tmA_half, bar, k0,
-                                  row0 + part * prow, amask, pol_a);
-            }
-            // B: half h (128 of the 256 columns) of the tile; gate/up half 0 is
-            // W1, half 1 is W3
-            auto load_b_half = [&](int h, uint16_t mask) {
-              const CUtensorMap *mb = (MODE == MODE_GATE_UP && h == 1) ? &tmB1 : &tmB0;
-              const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + h * (BN / 2);
-              uint8_t *dst = b_dst + h * (2 * B_CHUNK);
-              const int wz = c.wslot[t.e];  // the bank slot holding expert e's weights
-              if (FP8) {
-                if (mask) ptx::tma_load_3d_mc(dst, mb, bar, k0, nb, wz, mask, pol_b);
-                else ptx::tma_load_3d(dst, mb, bar, k0, nb, wz, pol_b);
-              } else {
-                if (mask) {
-                  ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, wz, mask, pol_b);
-                  ptx::tma_load_3d_mc(dst + B_CHUNK, mb, bar, nb + 64, k0, wz, mask, pol_b);
-                } else {
-                  ptx::tma_load_3d(dst, mb, bar, nb, k0, wz, pol_b);
-                  ptx::tma_load_3d(dst + B_CHUNK, mb, bar, nb + 64, k0, wz, pol_b);
-                }
-              }
-            };
-            if (t.npair) {
-              load_b_half(0, 0);  // own n-tile, whole
-              load_b_half(1, 0);
-            } else if (QUAD) {
-              // row i of the 2x2 tiles loads half i of its column's B tile, for both CTAs of that column
-              load_b_half(rank >> 1, uint16_t((1u << (rank & 1)) | (1u << (2 + (rank & 1)))));
-            } else {
-              load_b_half(rank, kBothCtas);  // M-pair: half r, for both CTAs
-            }
-          }
+          arm(p_stage);
+          load_b(p_stage, t, k0);
+          load_a(p_stage, t, k0);
           issued |= 1u << p_stage;
           last_par = (last_par & ~(1u << p_stage)) | (p_phase << p_stage);
           if (++p_stage == STAGES) { p_stage = 0; p_phase ^= 1u; }

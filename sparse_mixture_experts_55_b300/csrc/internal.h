@@ -20,6 +20,9 @@ constexpr int kRouteThreads = 512;
 constexpr int kRouteGroup = 4;
 // Tokens whose (token, slot) entries one grouping block ranks.
 constexpr int kGroupTokens = 256;
+// Batches up to this many tokens are routed and grouped by one block, which
+// also clears the call's status words and counters (no memset before it).
+constexpr int kSingleRouteT = 8;
 constexpr int kMaxE = 32;
 constexpr int kMaxK = 2;
 // Status-word slots at the start of the workspace.
@@ -73,6 +76,7 @@ struct WsLayout {
   bool train;         // training layout (bf16): saved pre-activations and backward buffers
   int route_tpb;      // tokens per router block
   int n_route_blocks;
+  bool route_single;  // T <= kSingleRouteT: one block routes, groups and clears the status and counters
 };
 
 // Split of one grouped GEMM's contraction into S ranges of kb_per_split
@@ -135,8 +139,17 @@ int check_device();
 cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
                          const WsLayout &L, const Ptrs &P, cudaStream_t s);
 cudaError_t launch_group(int T, int E, int K, const WsLayout &L, unsigned flags, const Ptrs &P, cudaStream_t s);
+// Router then grouping.  L.route_single: one block, launched with programmatic
+// dependent launch, that first waits for the previous work in the stream and
+// clears the status words and counters itself (the caller enqueues no memset).
+// Otherwise the status block must be zero at launch: one fused launch when
+// T <= kGroupTokens (P.status[1] serves as its ticket counter), else the two
+// kernels above.
+cudaError_t launch_route_group(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
+                               const WsLayout &L, const Ptrs &P, cudaStream_t s);
+// zero_pads: also zero the rows of padding (training forward)
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
-                          cudaStream_t s);
+                          cudaStream_t s, bool zero_pads);
 cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsigned flags, const Ptrs &P,
                            int num_sms, cudaStream_t s);
 cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx, float *gate,

@@ -87,15 +87,6 @@ int check_shape(int T, int d, int f, int E, int K, int dtype) {
 }
 
 
-// Profiling calls: reset a stamps array on the stream (begin times to all
-// ones, end times to zero) so that the stages' atomic min / max start clean.
-cudaError_t reset_stamps(unsigned long long *stamps, cudaStream_t s) {
-  if (stamps == nullptr) return cudaSuccess;
-  cudaError_t err = cudaMemsetAsync(stamps, 0xff, kNumStages * sizeof(unsigned long long), s);
-  if (err == cudaSuccess) err = cudaMemsetAsync(stamps + kNumStages, 0, kNumStages * sizeof(unsigned long long), s);
-  return err;
-}
-
 bool stamps_ok(const unsigned long long *stamps) {
   return stamps != nullptr && (reinterpret_cast<uintptr_t>(stamps) & 7u) == 0;
 }
@@ -153,6 +144,8 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bo
     // about one wave of router blocks: ceil(T / SMs) tokens each, in groups of kRouteGroup
     const int per = (T + num_sms - 1) / (num_sms > 0 ? num_sms : 1);
     L.route_tpb = ((per > 0 ? per : 1) + kRouteGroup - 1) / kRouteGroup * kRouteGroup;
+    L.route_single = T <= kSingleRouteT;
+    if (L.route_single) L.route_tpb = T > 0 ? (T + kRouteGroup - 1) / kRouteGroup * kRouteGroup : kRouteGroup;
     L.n_route_blocks = (T + L.route_tpb - 1) / L.route_tpb;
   }
   const long long TKl = static_cast<long long>(T) * K;
@@ -299,8 +292,7 @@ static int check_train_shape(int T, int d, int f, int E, int K, int dtype) {
 
 static int forward_impl(const void *x, const void *Wg, const void *W1, const void *W3, const void *W2, void *y,
                         int T, int d, int f, int E, int K, int dtype, void *workspace, size_t ws_bytes,
-                        unsigned flags, moe_stream_t stream, unsigned long long *stamps, bool train = false,
-                        bool stamps_reset = true) {
+                        unsigned flags, moe_stream_t stream, unsigned long long *stamps, bool train = false) {
   if (dtype == MOE_FP8_E4M3) return MOE_ERR_UNSUPPORTED;  // e4m3 weights go through moe_forward_fp8
   int st = train ? check_train_shape(T, d, f, E, K, dtype) : check_shape(T, d, f, E, K, dtype);
   if (st != MOE_OK) return st;
@@ -323,13 +315,12 @@ static int forward_impl(const void *x, const void *Wg, const void *W1, const voi
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Ptrs P = carve(workspace, L);
   P.stamps = stamps;
-  // status word and split-tile counters start at zero
-  if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (stamps_reset && reset_stamps(stamps, s) != cudaSuccess) return MOE_ERR_CUDA;
+  // status word and split-tile counters start at zero (small batches: the
+  // routing kernel clears them)
+  if (!L.route_single && cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
 
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
-  if (err == cudaSuccess) err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
+  cudaError_t err = launch_route_group(x, Wg, T, d, E, K, dtype, flags, L, P, s);
+  if (err == cudaSuccess) err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s, /*zero_pads=*/L.train);
   if (err == cudaSuccess) {
     if (dtype == MOE_BF16)
       err = launch_expert_gemms_bf16(W1, W3, W2, d, f, E, L, P, y, flags, sms, s);
@@ -365,10 +356,9 @@ static int block_forward_impl(void *h, const void *Wg, const void *W1, const voi
   const Ptrs P = carve(workspace, L);
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   // x_n = RMSNorm(h) into the workspace, then h += MoE(x_n)
-  if (reset_stamps(stamps, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (launch_rmsnorm(h, P.xnorm, T, d, eps, dtype, s, stamps) != cudaSuccess) return MOE_ERR_CUDA;
   return forward_impl(P.xnorm, Wg, W1, W3, W2, h, T, d, f, E, K, dtype, workspace, ws_bytes, flags | MOE_ACCUMULATE,
-                      stream, stamps, false, /*stamps_reset=*/false);
+                      stream, stamps);
 }
 
 int moe_block_forward(void *h, const void *Wg, const void *W1, const void *W3, const void *W2, int T, int d, int f,
@@ -417,8 +407,7 @@ int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Ptrs P = carve(workspace, L);
   if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (launch_group(T, E, K, L, flags, P, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_route_group(x, Wg, T, d, E, K, dtype, flags, L, P, s) != cudaSuccess) return MOE_ERR_CUDA;
   // the experts this batch needs: wait for the grouping's segment offsets
   int32_t offs[kMaxE + 1];
   if (cudaMemcpyAsync(offs, P.offsets, (E + 1) * sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
@@ -439,7 +428,7 @@ int moe_forward_cached(const void *x, const void *Wg, const void *W1_host, const
           cudaSuccess)
         return MOE_ERR_CUDA;
   cache->bytes_loaded += static_cast<long long>(n_loads) * 3 * static_cast<long long>(mat);
-  cudaError_t err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s);
+  cudaError_t err = launch_gather(x, T, d, E, dtype, L.R, P, sms, s, /*zero_pads=*/false);
   if (err == cudaSuccess)
     err = launch_expert_gemms_bf16(W1_dev, W3_dev, W2_dev, d, f, E, L, P, y, flags, sms, s, cache->slot_of, cache->C);
   if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, dtype, flags, P, sms, s);
@@ -450,9 +439,10 @@ int moe_forward_launches(int T, int d, int f, int E, int K, int dtype) {
   if (check_shape(T, d, f, E, K, dtype) != MOE_OK) return 0;
   if (T == 0) return 0;
   const WsLayout L = ws_layout(T, d, f, E, K, dtype, sm_count_or_default());
-  // route, group, gather (e4m3: gather + quantise), the two expert GEMMs (e4m3:
-  // plus the H quantiser), and the combine unless the down GEMM forms y
-  return 5 + (dtype == MOE_FP8_E4M3 ? 1 : 0) + (L.fuse_combine ? 0 : 1);
+  // route and group (one fused launch up to kGroupTokens tokens), gather
+  // (e4m3: gather + quantise), the two expert GEMMs (e4m3: plus the H
+  // quantiser), and the combine unless the down GEMM forms y
+  return (T <= kGroupTokens ? 1 : 2) + 3 + (dtype == MOE_FP8_E4M3 ? 1 : 0) + (L.fuse_combine ? 0 : 1);
 }
 
 size_t moe_train_workspace_bytes(int T, int d, int f, int E, int K, int dtype) {
@@ -571,11 +561,9 @@ static int forward_fp8_impl(const void *x, const void *Wg, const void *W1q, cons
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   Ptrs P = carve(workspace, L);
   P.stamps = stamps;
-  if (cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (reset_stamps(stamps, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (!L.route_single && cudaMemsetAsync(P.status, 0, L.zero_bytes, s) != cudaSuccess) return MOE_ERR_CUDA;
   // routing on the bf16 tokens, as moe_forward; the gather quantises rows
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, MOE_BF16, flags, L, P, s);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
+  cudaError_t err = launch_route_group(x, Wg, T, d, E, K, MOE_BF16, flags, L, P, s);
   if (err == cudaSuccess) err = launch_gather_quant(x, T, d, E, L.R, P, sms, s);
   if (err == cudaSuccess) err = launch_expert_gemms_fp8(W1q, s1, W3q, s3, W2q, s2, d, f, E, L, P, y, flags, sms, s);
   if (err == cudaSuccess && !L.fuse_combine) err = launch_combine(y, T, d, K, L.S, MOE_BF16, flags, P, sms, s);
@@ -623,8 +611,7 @@ int moe_route(const void *x, const void *Wg, int T, int d, int E, int K, int dty
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   const Ptrs P = carve(workspace, L);
   if (cudaMemsetAsync(P.status, 0, kStatusInts * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, 0, L, P, s);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L, 0, P, s);
+  cudaError_t err = launch_route_group(x, Wg, T, d, E, K, dtype, 0, L, P, s);
   if (err == cudaSuccess) err = launch_route_export(T, E, K, P, idx, gate, perm_tok, offsets, pos, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -121,11 +121,11 @@ extern "C" int moe_route_noalloc(const void *x, const void *Wg, int T, int d, in
                                /*routing_only=*/true);
   if (L.xperm > kNoAllocBytes) return MOE_ERR_UNSUPPORTED;
   const Ptrs P = carve(scratch, L);
-  // The status word must start at zero; every other scratch word the kernels
-  // read is written earlier in the same call.
+  // The status words (the status and the fused router's ticket) must start
+  // at zero; every other scratch word the kernels read is written earlier in
+  // the same call.
   if (cudaMemsetAsync(P.status, 0, kStatusInts * sizeof(int), s) != cudaSuccess) return MOE_ERR_CUDA;
-  cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s);
-  if (err == cudaSuccess) err = launch_group(T, E, K, L, flags, P, s);
+  cudaError_t err = launch_route_group(x, Wg, T, d, E, K, dtype, flags, L, P, s);
   if (err == cudaSuccess) err = launch_route_export(T, E, K, P, idx, gate, perm_tok, offsets, pos, s);
   return err == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

@@ -199,10 +199,10 @@ __device__ __forceinline__ void select_and_store(const float (&l)[EP], int t, in
 // warp reduce-scatters its partial logits and the warp sums are added in a
 // fixed order, so the logits are deterministic.
 template <typename Tin, int EP>
-__global__ void __launch_bounds__(kRouteThreads, 1)
-    route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
-                 unsigned flags, int32_t *__restrict__ idx, float *__restrict__ gate,
-                 int32_t *__restrict__ blockcounts, int *status, unsigned long long *stamps) {
+__device__ __forceinline__ void route_body(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d,
+                                           int E, int K, int tpb, unsigned flags, int32_t *__restrict__ idx,
+                                           float *__restrict__ gate, int32_t *__restrict__ blockcounts, int *status,
+                                           unsigned long long *stamps) {
   constexpr int NV = Vec<Tin>::N;
   constexpr int NW = kRouteThreads / 32;
   constexpr int G = kRouteGroup;  // tokens per reduction group
@@ -265,42 +265,49 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   stamp_end(stamps, ST_ROUTE);
 }
 
-// Stable grouping.  Block b ranks the (token, slot) entries of tokens
+template <typename Tin, int EP>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
+                 unsigned flags, int32_t *__restrict__ idx, float *__restrict__ gate,
+                 int32_t *__restrict__ blockcounts, int *status, unsigned long long *stamps) {
+  route_body<Tin, EP>(x, Wg, T, d, E, K, tpb, flags, idx, gate, blockcounts, status, stamps);
+}
+
+// Stable grouping.  Block b (of nb) ranks the (token, slot) entries of tokens
 // [b*kGroupTokens, (b+1)*kGroupTokens) in flat t*K + k order: rank = entries of
 // that expert in earlier router blocks + in earlier warps of this block + in
 // earlier lanes of this warp.  Each expert's segment in the padded grouped
 // buffers (X_perm, H) starts at a multiple of kSegPad; pad rows get token -1
 // and gate 0.  pos[t, k] is the entry's row in the unpadded grouped order
-// (offsets[e] + rank), which indexes the compact expert-output buffer.
-__global__ void __launch_bounds__(kGroupTokens *kMaxK)
-    group_kernel(int T, int E, int K, int nb_route, int tpb, unsigned flags, const int32_t *__restrict__ idx,
-                 const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
-                 int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status,
-                 unsigned long long *stamps) {
+// (offsets[e] + rank), which indexes the compact expert-output buffer.  The
+// router's outputs are read through L2 (ld.cg): in the fused router the block
+// that runs this has not written most of them itself.
+__device__ __forceinline__ void group_body(int b, int nb, int T, int E, int K, int nb_route, int tpb,
+                                           const int32_t *__restrict__ idx, const float *__restrict__ gate,
+                                           const int32_t *__restrict__ blockcounts, int32_t *offsets,
+                                           int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate,
+                                           int *status) {
   constexpr int NT = kGroupTokens * kMaxK;
   constexpr int NW = NT / 32;
   __shared__ int s_base[kMaxE], s_tot[kMaxE], s_off[kMaxE + 1], s_poff[kMaxE + 1];
   __shared__ int s_wcnt[NW][kMaxE];
-  const int tid = threadIdx.x, b = blockIdx.x;
+  const int tid = threadIdx.x;
   const int warp = tid >> 5, lane = tid & 31;
   if (tid < kMaxE) { s_base[tid] = 0; s_tot[tid] = 0; }
   for (int i = tid; i < NW * kMaxE; i += NT) (&s_wcnt[0][0])[i] = 0;
   __syncthreads();
-  pdl_wait();
-  pdl_trigger();
-  stamp_begin(stamps, ST_GROUP);
   // entries ahead of this chunk: whole router blocks from their histograms,
   // plus the part of the router block it starts in, counted from idx
   const int tok0 = b * kGroupTokens;
   const int rb_full = tok0 / tpb;
   for (int i = tid; i < nb_route * E; i += NT) {
     const int rb = i / E, e = i - rb * E;
-    const int c = blockcounts[i];
+    const int c = __ldcg(blockcounts + i);
     atomicAdd(&s_tot[e], c);
     if (rb < rb_full) atomicAdd(&s_base[e], c);
   }
   for (int i = rb_full * tpb * K + tid; i < tok0 * K; i += NT) {
-    const int e = idx[i];
+    const int e = __ldcg(idx + i);
     if (e >= 0 && e < E) atomicAdd(&s_base[e], 1);
   }
   __syncthreads();
@@ -321,7 +328,7 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
   const int flat0 = b * kGroupTokens * K;
   const int n_entries = min(kGroupTokens, T - b * kGroupTokens) * K;
   bool active = tid < n_entries;
-  int e = active ? idx[flat0 + tid] : -1;
+  int e = active ? __ldcg(idx + flat0 + tid) : -1;
   if (active && (e < 0 || e >= E)) {
     set_status(status, MOE_ERR_DEVICE_BOUNDS);
     active = false;
@@ -336,10 +343,9 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
     for (int w = 0; w < warp; ++w) r += s_wcnt[w][e];
     const int rp = s_poff[e] + r;
     perm_tok[rp] = (flat0 + tid) / K;
-    perm_gate[rp] = gate[flat0 + tid];
+    perm_gate[rp] = __ldcg(gate + flat0 + tid);
     pos[flat0 + tid] = s_off[e] + r;  // unpadded grouped row
   }
-  const int nb = gridDim.x;
   for (int ee = b; ee < E; ee += nb) {
     const int start = s_poff[ee] + s_tot[ee], end = s_poff[ee + 1];
     for (int r = start + tid; r < end; r += NT) {
@@ -347,16 +353,81 @@ __global__ void __launch_bounds__(kGroupTokens *kMaxK)
       perm_gate[r] = 0.f;
     }
   }
+}
+
+__global__ void __launch_bounds__(kGroupTokens *kMaxK)
+    group_kernel(int T, int E, int K, int nb_route, int tpb, unsigned flags, const int32_t *__restrict__ idx,
+                 const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
+                 int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status,
+                 unsigned long long *stamps) {
+  pdl_wait();
+  pdl_trigger();
+  stamp_begin(stamps, ST_GROUP);
+  group_body(blockIdx.x, gridDim.x, T, E, K, nb_route, tpb, idx, gate, blockcounts, offsets, poffsets, pos,
+             perm_tok, perm_gate, status);
   (void)flags;
   stamp_end(stamps, ST_GROUP);
 }
 
-// X_perm[r, :] = x[perm_tok[r], :] for every grouped row; pad rows are zeroed.
-// One warp per row, 16-byte vectors.
+// Router and grouping in one launch, for batches that one grouping block
+// covers (T <= kGroupTokens): every block routes its tokens as route_kernel
+// does (same arithmetic, same results), then the block that finishes last --
+// the one whose arrival on the ticket counter (zero at launch) completes the
+// count -- groups all the tokens.
+template <typename Tin, int EP>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_group_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
+                       unsigned flags, int32_t *idx, float *gate, int32_t *blockcounts, int32_t *offsets,
+                       int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status,
+                       int *ticket, unsigned long long *stamps) {
+  route_body<Tin, EP>(x, Wg, T, d, E, K, tpb, flags, idx, gate, blockcounts, status, stamps);
+  __shared__ int s_last;
+  __syncthreads();  // this block's routing stores precede its arrival
+  if (threadIdx.x == 0) {
+    __threadfence();
+    s_last = atomicAdd(ticket, 1) == static_cast<int>(gridDim.x) - 1 ? 1 : 0;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();  // the other blocks' routing stores are visible to this one
+  stamp_begin(stamps, ST_GROUP);
+  group_body(0, 1, T, E, K, gridDim.x, tpb, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate,
+             status);
+  stamp_end(stamps, ST_GROUP);
+}
+
+// Router and grouping of a small batch (T <= kSingleRouteT) in one block,
+// launched with programmatic dependent launch: the block first waits for the
+// previous work in the stream to finish, then clears the call's status words
+// and split / slot counters (n_zero ints from `status`, which that work may
+// have been using), then routes every token as route_kernel does (same
+// arithmetic) and groups them.
+template <typename Tin, int EP>
+__global__ void __launch_bounds__(kRouteThreads, 1)
+    route_single_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
+                        unsigned flags, int32_t *idx, float *gate, int32_t *blockcounts, int32_t *offsets,
+                        int32_t *poffsets, int32_t *pos, int32_t *perm_tok, float *perm_gate, int *status, int n_zero,
+                        unsigned long long *stamps) {
+  pdl_wait();
+  for (int i = threadIdx.x; i < n_zero; i += blockDim.x) status[i] = 0;
+  __syncthreads();
+  route_body<Tin, EP>(x, Wg, T, d, E, K, tpb, flags, idx, gate, blockcounts, status, stamps);
+  __syncthreads();
+  __threadfence_block();
+  stamp_begin(stamps, ST_GROUP);
+  group_body(0, 1, T, E, K, 1, tpb, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, status);
+  stamp_end(stamps, ST_GROUP);
+}
+
+// X_perm[r, :] = x[perm_tok[r], :] for every grouped row; pad rows are zeroed
+// when zero_pads (the training forward: the weight gradients contract over
+// whole segments) and left as they are otherwise (every product row depends
+// on its own input row only, and the rows of padding are never stored to the
+// layer's output).  One warp per row, 16-byte vectors.
 __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x, int T, int vec_per_row,
                                                      const int32_t *__restrict__ perm_tok,
                                                      const int32_t *__restrict__ poffsets, int E,
-                                                     uint4 *__restrict__ xperm, int *status,
+                                                     uint4 *__restrict__ xperm, int zero_pads, int *status,
                                                      unsigned long long *stamps) {
   pdl_wait();
   pdl_trigger();
@@ -384,7 +455,7 @@ __global__ void __launch_bounds__(256) gather_kernel(const uint4 *__restrict__ x
         for (int i = 0; i < 8; ++i) dst[v + 32 * i] = a[i];
       }
       for (; v < vec_per_row; v += 32) dst[v] = __ldg(src + v);
-    } else {
+    } else if (zero_pads) {
       for (int v = lane; v < vec_per_row; v += 32) dst[v] = make_uint4(0, 0, 0, 0);
     }
   }
@@ -528,6 +599,50 @@ cudaError_t launch_route(const void *x, const void *Wg, int T, int d, int E, int
                        P.gate, P.blockcounts, P.status, P.stamps);
 }
 
+cudaError_t launch_route_group(const void *x, const void *Wg, int T, int d, int E, int K, int dtype, unsigned flags,
+                               const WsLayout &L, const Ptrs &P, cudaStream_t s) {
+  if (L.route_single) {
+    const int n_zero = static_cast<int>(L.zero_bytes / sizeof(int));
+    const int tpb = L.route_tpb;
+    if (dtype == MOE_BF16) {
+      auto *xx = static_cast<const __nv_bfloat16 *>(x);
+      auto *ww = static_cast<const __nv_bfloat16 *>(Wg);
+      auto kern = E <= 8 ? route_single_kernel<__nv_bfloat16, 8> : route_single_kernel<__nv_bfloat16, 32>;
+      return launch_kernel(kern, dim3(1), dim3(kRouteThreads), 0, s, true, xx, ww, T, d, E, K, tpb, flags, P.idx,
+                           P.gate, P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status,
+                           n_zero, P.stamps);
+    }
+    auto *xx = static_cast<const float *>(x);
+    auto *ww = static_cast<const float *>(Wg);
+    auto kern = E <= 8 ? route_single_kernel<float, 8> : route_single_kernel<float, 32>;
+    return launch_kernel(kern, dim3(1), dim3(kRouteThreads), 0, s, true, xx, ww, T, d, E, K, tpb, flags, P.idx, P.gate,
+                         P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status, n_zero,
+                         P.stamps);
+  }
+  if (T > kGroupTokens) {
+    const cudaError_t err = launch_route(x, Wg, T, d, E, K, dtype, flags, L, P, s);
+    return err == cudaSuccess ? launch_group(T, E, K, L, flags, P, s) : err;
+  }
+  // one launch: the router blocks, then the grouping in the block that finishes last
+  const dim3 grid(L.n_route_blocks), block(kRouteThreads);
+  static_assert(kRouteThreads == kGroupTokens * kMaxK, "the fused kernel's blocks run both bodies");
+  const int tpb = L.route_tpb;
+  int *ticket = P.status + 1;  // zero at launch, like the rest of the status words
+  if (dtype == MOE_BF16) {
+    auto *xx = static_cast<const __nv_bfloat16 *>(x);
+    auto *ww = static_cast<const __nv_bfloat16 *>(Wg);
+    auto kern = E <= 8 ? route_group_kernel<__nv_bfloat16, 8> : route_group_kernel<__nv_bfloat16, 32>;
+    return launch_kernel(kern, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags, P.idx, P.gate,
+                         P.blockcounts, P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status, ticket,
+                         P.stamps);
+  }
+  auto *xx = static_cast<const float *>(x);
+  auto *ww = static_cast<const float *>(Wg);
+  auto kern = E <= 8 ? route_group_kernel<float, 8> : route_group_kernel<float, 32>;
+  return launch_kernel(kern, grid, block, 0, s, false, xx, ww, T, d, E, K, tpb, flags, P.idx, P.gate, P.blockcounts,
+                       P.offsets, P.poffsets, P.pos, P.perm_tok, P.perm_gate, P.status, ticket, P.stamps);
+}
+
 cudaError_t launch_group(int T, int E, int K, const WsLayout &L, unsigned flags, const Ptrs &P, cudaStream_t s) {
   const dim3 grid((T + kGroupTokens - 1) / kGroupTokens), block(kGroupTokens * kMaxK);
   return launch_kernel(group_kernel, grid, block, 0, s, true, T, E, K, L.n_route_blocks, L.route_tpb, flags, P.idx,
@@ -536,7 +651,7 @@ cudaError_t launch_group(int T, int E, int K, const WsLayout &L, unsigned flags,
 }
 
 cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, const Ptrs &P, int num_sms,
-                          cudaStream_t s) {
+                          cudaStream_t s, bool zero_pads) {
   const int elem = dtype == MOE_BF16 ? 2 : 4;
   const int vec_per_row = d * elem / 16;
   int blocks = (R + 7) / 8;  // 8 warps (rows) per block
@@ -544,7 +659,7 @@ cudaError_t launch_gather(const void *x, int T, int d, int E, int dtype, int R, 
   if (blocks < 1) blocks = 1;
   return launch_kernel(gather_kernel, dim3(blocks), dim3(256), 0, s, true, static_cast<const uint4 *>(x), T,
                        vec_per_row, static_cast<const int32_t *>(P.perm_tok), static_cast<const int32_t *>(P.poffsets),
-                       E, static_cast<uint4 *>(P.xperm), P.status, P.stamps);
+                       E, static_cast<uint4 *>(P.xperm), zero_pads ? 1 : 0, P.status, P.stamps);
 }
 
 cudaError_t launch_combine(void *y, int T, int d, int K, int S, int dtype, unsigned flags, const Ptrs &P,

@@ -249,10 +249,13 @@ def test_forward_launch_counts(lib):
     # prefill: the down projection is not split, so its epilogue forms y
     assert lib.moe_forward_launches(4096, 4096, 14336, 8, 2, _lib.MOE_BF16) == 5
     assert lib.moe_forward_launches(4096, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 6
-    # one token: split down projection, separate combine
-    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_BF16) == 6
-    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 7
+    # one token: router and grouping fused, split down projection, separate combine
+    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_BF16) == 5
+    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 6
+    # 256 tokens still fuse the router and the grouping, 257 do not
+    assert lib.moe_forward_launches(256, 64, 128, 8, 2, _lib.MOE_F32) == 5
+    assert lib.moe_forward_launches(257, 64, 128, 8, 2, _lib.MOE_F32) == 6
     # fp32: two SIMT FFN kernels and the combine
-    assert lib.moe_forward_launches(64, 64, 128, 8, 2, _lib.MOE_F32) == 6
+    assert lib.moe_forward_launches(64, 64, 128, 8, 2, _lib.MOE_F32) == 5
     assert lib.moe_forward_launches(0, 64, 128, 8, 2, _lib.MOE_BF16) == 0
     assert lib.moe_forward_launches(16, 63, 128, 8, 2, _lib.MOE_BF16) == 0

@@ -2,16 +2,19 @@
 locality trace the cached layer equals moe_forward bit for bit at every step
 (the same kernels, reading expert e from its slot), and the cache's decisions
 (loads, hits, misses, maps) equal the oracle LRU policy's on the needed sets
-the GPU routing produced.  A step that needs more experts than there are
-slots is refused without changing the state."""
+the GPU routing produced; the cached layer's output is also compared with the
+float64 oracle directly at every step.  A step that needs more experts than
+there are slots is refused without changing the state."""
 from __future__ import annotations
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 import workloads as W
 from oracle.cache_oracle import LRUCache
+from tests import parity
 
 pytestmark = pytest.mark.gpu
 
@@ -38,6 +41,8 @@ def test_cached_forward_equals_forward_and_policy_matches_oracle(moe, cuda_devic
         y_ref = moe.moe_forward(x, Wg, W1, W3, W2, K)
         torch.cuda.synchronize()
         assert torch.equal(y, y_ref), i
+        y64 = oracle.moe_layer(x.cpu(), Wg.cpu(), W1.cpu(), W3.cpu(), W2.cpu(), K).y
+        assert parity.rel_linf(y.float().cpu().numpy(), y64) <= parity.TOL["bf16"], i
         idx, *_ = moe.moe_route(x, Wg, K)
         ref.plan(sorted(set(idx.flatten().tolist())))
         st = cache.state
@@ -70,6 +75,9 @@ def test_cached_forward_at_full_size(moe, cuda_device):
     for i in range(xs.shape[0]):
         y = cache.forward(xs[i], Wg, K)
         assert torch.equal(y, moe.moe_forward(xs[i], Wg, W1, W3, W2, K)), i
+        if i < 2:  # the oracle on the token directly (two steps keep the host work bounded)
+            y64 = oracle.moe_layer_tokens(xs[i].cpu(), Wg.cpu(), W1, W3, W2, K, [0]).y
+            assert parity.rel_linf(y.float().cpu().numpy(), y64) <= parity.TOL["bf16"], i
         idx, *_ = moe.moe_route(xs[i], Wg, K)
         ref.plan(sorted(set(idx.flatten().tolist())))
         assert list(cache.state.slot_of)[:E] == ref.slot_of, i
