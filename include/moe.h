@@ -223,20 +223,28 @@ MOE_API int moe_block_forward_stamped(void *h, const void *Wg, const void *W1, c
  * The expert GEMMs multiply e4m3 codes on the tensor cores (fp32
  * accumulation) and apply the row and column scales in their epilogues.
  *
- * moe_quantize_weights_fp8: W [E, K, N] bf16 -> Wq [E, N, K] e4m3 codes (one
- * byte each) and scales [E, N] fp32, all device memory owned by the caller;
- * K, N >= 1.  For the layer: W1 and W3 ([E, d, f]) give [E, f, d] codes and
- * [E, f] scales, W2 ([E, f, d]) gives [E, d, f] codes and [E, d] scales.
+ * moe_quantize_weights_fp8: W [E, K, N] bf16 -> codes Wq (one byte each)
+ * and scales [E, N] fp32, all device memory owned by the caller; K, N >= 1.
+ * The codes are stored in 128 x 128 tiles, so that the expert GEMMs stream
+ * each tile as one contiguous 16 KiB block: Wq is
+ * [E, Nt, Kt, 128, 128] with Nt = ceil(N / 128), Kt = ceil(K / 128), and
+ * Wq[e, n / 128, k / 128, n % 128, k % 128] = code of W[e, k, n]; codes past
+ * N or K are zero.  Its size is moe_fp8_weight_bytes(E, K, N).  For the
+ * layer: W1 and W3 ([E, d, f]) give tiles over (N, K) = (f, d) and [E, f]
+ * scales, W2 ([E, f, d]) gives tiles over (d, f) and [E, d] scales.
  */
 MOE_API int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales,
                              moe_stream_t stream);
+
+/* Bytes of the tiled e4m3 codes of an [E, K, N] bank (0 if a size is below 1). */
+MOE_API size_t moe_fp8_weight_bytes(int E, int K, int N);
 
 /*
  * The layer with e4m3 expert weights: y = sum over the K selected experts of
  * gate * SwiGLU_expert(x), as moe_forward, with the expert projections on
  * e4m3 operands (scheme above).  x [T, d], Wg [d, E] and y [T, d] are bf16;
- * W1q, W3q [E, f, d] and W2q [E, d, f] are e4m3 codes with scales s1, s3
- * [E, f] and s2 [E, d] from moe_quantize_weights_fp8.  d and f are multiples
+ * W1q, W3q (tiles over f x d) and W2q (tiles over d x f) are e4m3 codes with
+ * scales s1, s3 [E, f] and s2 [E, d] from moe_quantize_weights_fp8.  d and f are multiples
  * of 16.  workspace: at least moe_workspace_bytes(T, d, f, E, K,
  * MOE_FP8_E4M3).  flags: as moe_forward.  Other rules as moe_forward.
  */

@@ -209,12 +209,15 @@ def moe_forward_host(x_host, y_host, Wg, W1, W3, W2, K: int = 2, x_dev=None, y_d
 
 
 def quantize_weights_fp8(W, stream=None):
-    """e4m3 codes of an expert bank: W [E, K, N] bf16 -> (Wq [E, N, K]
-    float8_e4m3fn, K contiguous; scales [E, N] fp32), one scale per output
-    column (scale = max |column| / 448)."""
+    """e4m3 codes of an expert bank: W [E, K, N] bf16 -> (Wq, scales [E, N]
+    fp32), one scale per output column (scale = max |column| / 448).  Wq is
+    float8_e4m3fn [E, ceil(N/128), ceil(K/128), 128, 128]: 128 x 128 tiles,
+    Wq[e, n // 128, k // 128, n % 128, k % 128] = code of W[e, k, n], zero past
+    N or K."""
     _need(W, "W", torch.bfloat16)
     E, Kd, N = W.shape
-    Wq = torch.empty((E, N, Kd), dtype=torch.float8_e4m3fn, device=W.device)
+    Wq = torch.empty((E, (N + 127) // 128, (Kd + 127) // 128, 128, 128), dtype=torch.float8_e4m3fn,
+                     device=W.device)
     scales = torch.empty((E, N), dtype=torch.float32, device=W.device)
     rc = _lib.load().moe_quantize_weights_fp8(_ptr(W), E, Kd, N, _ptr(Wq), _ptr(scales), _stream_ptr(stream, W.device))
     _lib.check("moe_quantize_weights_fp8", rc)
@@ -230,10 +233,12 @@ def _fp8_args(x, Wg, W1q, s1, W3q, s3, W2q, s2, y):
     for t, n in ((s1, "s1"), (s3, "s3"), (s2, "s2")):
         _need(t, n, torch.float32, dev)
     T, d = x.shape
-    E, f, d1 = W1q.shape
-    if (Wg.shape != (d, E) or d1 != d or W3q.shape != (E, f, d) or W2q.shape != (E, d, f) or s1.shape != (E, f)
+    E, f = s1.shape
+    tiles = lambda n, k: (E, (n + 127) // 128, (k + 127) // 128, 128, 128)
+    if (Wg.shape != (d, E) or W1q.shape != tiles(f, d) or W3q.shape != tiles(f, d) or W2q.shape != tiles(d, f)
             or s3.shape != (E, f) or s2.shape != (E, d)):
-        raise ValueError("shape mismatch: x [T,d], Wg [d,E], W1q/W3q [E,f,d], W2q [E,d,f], s1/s3 [E,f], s2 [E,d]")
+        raise ValueError("shape mismatch: x [T,d], Wg [d,E], s1/s3 [E,f], s2 [E,d], W1q/W3q tiles over (f, d), "
+                         "W2q tiles over (d, f) (quantize_weights_fp8)")
     if y is None:
         y = torch.empty_like(x)
     else:

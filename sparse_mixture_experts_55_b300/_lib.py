@@ -59,6 +59,7 @@ SIGNATURES = {
     "moe_block_forward_stamped": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _i, ctypes.c_float, _vp, _sz,
                                         _u, _vp, _vp]),
     "moe_quantize_weights_fp8": (_i, [_vp, _i, _i, _i, _vp, _vp, _vp]),
+    "moe_fp8_weight_bytes": (_sz, [_i, _i, _i]),
     "moe_forward_fp8": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u, _vp]),
     "moe_forward_fp8_stamped": (_i, [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _sz, _u,
                                      _vp, _vp]),

@@ -15,22 +15,15 @@
 
 #include <cstdint>
 
+#include "fp8_codec.cuh"
 #include "internal.h"
 #include "stamps.cuh"
 
 namespace moe {
 namespace {
 
-constexpr float kE4M3Max = 448.0f;
-
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
-
-__device__ __forceinline__ float scale_of(float absmax) { return absmax > 0.f ? absmax / kE4M3Max : 1.0f; }
-
-__device__ __forceinline__ uint8_t to_e4m3(float v) {
-  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
-}
 
 // scales[e, n] = max_k |W[e, k, n]| / 448 (1 for an all-zero column).
 // Block: 64 columns x 4 row phases.
@@ -53,14 +46,18 @@ __global__ void __launch_bounds__(256) weight_absmax_kernel(const __nv_bfloat16 
   }
 }
 
-// Wq[e, n, k] = e4m3(W[e, k, n] / scales[e, n]); 64x64 tiles through shared
-// memory so that both the reads (along n) and the writes (along k) coalesce.
+// Wq holds e4m3(W[e, k, n] / scales[e, n]) in 128 x 128 tiles: tile (nt, kt)
+// of expert e is the contiguous 16 KiB block ((e * Nt + nt) * Kt + kt), inside
+// it row n % 128 holds the 128 codes of k = kt*128 .. kt*128 + 127 (zero past
+// N or K).  64x64 pieces through shared memory so that both the reads (along
+// n) and the writes (along k) coalesce; the grid covers whole tiles.
 __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N,
                                                            const float *__restrict__ scales, uint8_t *__restrict__ Wq) {
   __shared__ uint8_t tile[64][65];
   const int e = blockIdx.z;
   const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
   const int tx = threadIdx.x & 63, ty = threadIdx.x >> 6;
+  const int Nt = (N + kFp8Tile - 1) / kFp8Tile, Kt = (K + kFp8Tile - 1) / kFp8Tile;
   const __nv_bfloat16 *Wb = W + static_cast<size_t>(e) * K * N;
   const int n = n0 + tx;
   const float s = n < N ? scales[static_cast<size_t>(e) * N + n] : 1.0f;
@@ -71,10 +68,10 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *
     tile[tx][i] = q;  // [n][k]
   }
   __syncthreads();
-  uint8_t *Wqb = Wq + static_cast<size_t>(e) * N * K;
   for (int i = ty; i < 64; i += 4) {
     const int nn = n0 + i, k = k0 + tx;
-    if (nn < N && k < K) Wqb[static_cast<size_t>(nn) * K + k] = tile[i][tx];
+    const size_t t = (static_cast<size_t>(e) * Nt + nn / kFp8Tile) * Kt + k / kFp8Tile;
+    Wq[t * kFp8Tile * kFp8Tile + (nn % kFp8Tile) * kFp8Tile + k % kFp8Tile] = tile[i][tx];
   }
 }
 
@@ -109,19 +106,6 @@ __device__ __forceinline__ float team_max(float v, float *red) {
   float m = 0.f;
   for (int i = 0; i < nw; ++i) m = fmaxf(m, red[i]);
   return m;
-}
-
-// 8 values (16 bytes of bf16) to 8 e4m3 codes.
-__device__ __forceinline__ uint2 quant8(uint4 u, float s) {
-  const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
-  uint32_t w[2] = {0, 0};
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float2 f = __bfloat1622float2(h[i]);
-    const uint32_t q = static_cast<uint32_t>(to_e4m3(f.x / s)) | (static_cast<uint32_t>(to_e4m3(f.y / s)) << 8);
-    w[i >> 1] |= q << (16 * (i & 1));
-  }
-  return make_uint2(w[0], w[1]);
 }
 
 __device__ __forceinline__ float absmax8(uint4 u) {
@@ -215,7 +199,8 @@ cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void
   weight_absmax_kernel<<<g1, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(W), K, N, scales);
   cudaError_t err = cudaGetLastError();
   if (err != cudaSuccess) return err;
-  const dim3 g2((N + 63) / 64, (K + 63) / 64, E);
+  // every 64 x 64 piece of the whole tiles (padding included)
+  const dim3 g2(2 * ((N + kFp8Tile - 1) / kFp8Tile), 2 * ((K + kFp8Tile - 1) / kFp8Tile), E);
   weight_quant_kernel<<<g2, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(W), K, N, scales,
                                          static_cast<uint8_t *>(Wq));
   return cudaGetLastError();

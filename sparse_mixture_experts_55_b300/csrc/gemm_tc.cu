@@ -65,6 +65,7 @@
 
 #include <mutex>
 
+#include "fp8_codec.cuh"
 #include "internal.h"
 #include "ptx.cuh"
 #include "stamps.cuh"
@@ -133,6 +134,8 @@ struct GemmArgs {
   const float *col_scale0;
   const float *col_scale1;
   float *habs;
+  // e4m3 weight banks in 128 x 128 tiles: tiles per expert along N and K
+  int b_nt, b_kt;
   // training forward (bf16 gate/up without splits): also store the
   // pre-activations a = X W1 and b = X W3 as bf16 [R, 2 n_out] (a in columns
   // [0, n_out), b after), for every row of the segments including padding
@@ -363,6 +366,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   // Stage `st` of k-block k0 of tile t: arm its barrier for all the bytes
   // that complete it, and issue this CTA's weight (B) and activation (A) copies.
   auto stage_bar = [&](int st) -> uint64_t * { return &c.full[st]; };
+  // e4m3: first row of the 128 x 128 weight tile holding columns nb.. and
+  // k-elements k0.. of bank slot wz, in the tiles' 128-byte-row view
+  auto fp8_tile_row = [&](int wz, int nb, int k0) {
+    return ((wz * args.b_nt + nb / kFp8Tile) * args.b_kt + k0 / kFp8Tile) * kFp8Tile;
+  };
   auto arm = [&](int st) {
     // pair MMA: both CTAs' copies complete on the first CTA's barrier, which
     // expects the bytes of both
@@ -377,8 +385,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const CUtensorMap *mb = (MODE == MODE_GATE_UP && rank == 1) ? &tmB1 : &tmB0;
       const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + rank * (BN / 2);
       if (FP8) {
-        // e4m3 banks are K-contiguous ([E, N, K]): one 128 x 128 box, 16 KiB
-        ptx::tma_load_3d_pair(b_dst, mb, bar, k0, nb, wz, pol_b);
+        // e4m3 banks are stored in 128 x 128 tiles: one contiguous 16 KiB box
+        ptx::tma_load_2d_pair(b_dst, mb, bar, 0, fp8_tile_row(wz, nb, k0), pol_b);
       } else {
         ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, wz, pol_b);
         ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, wz, pol_b);
@@ -393,8 +401,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int nb = MODE == MODE_GATE_UP ? t.nt * (BN / 2) : t.nt * BN + h * (BN / 2);
       uint8_t *dst = b_dst + h * (2 * B_CHUNK);
       if (FP8) {
-        if (mask) ptx::tma_load_3d_mc(dst, mb, bar, k0, nb, wz, mask, pol_b);
-        else ptx::tma_load_3d(dst, mb, bar, k0, nb, wz, pol_b);
+        const int row = fp8_tile_row(wz, nb, k0);
+        if (mask) ptx::tma_load_2d_mc(dst, mb, bar, 0, row, mask, pol_b);
+        else ptx::tma_load_2d(dst, mb, bar, 0, row, pol_b);
       } else {
         if (mask) {
           ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, wz, mask, pol_b);
@@ -1172,13 +1181,18 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   cudaError_t err = device_state(num_sms, &grids);
   if (err != cudaSuccess) return err;
   const int form = pick_form(L, grids);
-  // e4m3 operands: X_perm [R, d], H [R, f] and the banks [E, N, K], all K-contiguous
+  // e4m3 operands: X_perm [R, d] and H [R, f] K-contiguous; the banks in
+  // 128 x 128 tiles, addressed as rows of 128 codes (tile t = rows 128 t ..)
+  const int nt13 = (f + kFp8Tile - 1) / kFp8Tile, kt13 = (d + kFp8Tile - 1) / kFp8Tile;
+  const int nt2 = (d + kFp8Tile - 1) / kFp8Tile, kt2 = (f + kFp8Tile - 1) / kFp8Tile;
+  const uint64_t rows13 = static_cast<uint64_t>(E) * nt13 * kt13 * kFp8Tile;
+  const uint64_t rows2 = static_cast<uint64_t>(E) * nt2 * kt2 * kFp8Tile;
   CUtensorMap tm_x, tm_xh, tm_xq, tm_w1, tm_w3, tm_h, tm_hh, tm_hq, tm_w2;
   if (!tmap_2d_u8(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d_u8(&tm_xh, P.xperm, d, L.R, BM / 2) ||
-      !tmap_2d_u8(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_3d_u8(&tm_w1, W1q, d, f, E) ||
-      !tmap_3d_u8(&tm_w3, W3q, d, f, E) || !tmap_2d_u8(&tm_h, P.hq, f, L.R, BM) ||
+      !tmap_2d_u8(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_2d_u8(&tm_w1, W1q, kFp8Tile, rows13, kFp8Tile) ||
+      !tmap_2d_u8(&tm_w3, W3q, kFp8Tile, rows13, kFp8Tile) || !tmap_2d_u8(&tm_h, P.hq, f, L.R, BM) ||
       !tmap_2d_u8(&tm_hh, P.hq, f, L.R, BM / 2) || !tmap_2d_u8(&tm_hq, P.hq, f, L.R, BM / 4) ||
-      !tmap_3d_u8(&tm_w2, W2q, f, d, E))
+      !tmap_2d_u8(&tm_w2, W2q, kFp8Tile, rows2, kFp8Tile))
     return cudaErrorInvalidValue;
 
   GemmArgs g1{};
@@ -1201,6 +1215,8 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g1.col_scale0 = s1;
   g1.col_scale1 = s3;
   g1.habs = P.habs;
+  g1.b_nt = nt13;
+  g1.b_kt = kt13;
   g1.status = P.status;
   g1.stamps = P.stamps;
   err = launch_form<MODE_GATE_UP, true>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
@@ -1224,6 +1240,8 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g2.col_scale0 = s2;
   g2.col_scale1 = nullptr;
   g2.habs = nullptr;
+  g2.b_nt = nt2;
+  g2.b_kt = kt2;
   return launch_form<MODE_DOWN, true>(form, grids, s, true, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 

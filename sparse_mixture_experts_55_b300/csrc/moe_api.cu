@@ -524,10 +524,16 @@ int moe_backward_timed(const void *x, const void *Wg, const void *W1, const void
                        flags, stream, events);
 }
 
+size_t moe_fp8_weight_bytes(int E, int K, int N) {
+  if (E < 1 || K < 1 || N < 1) return 0;
+  const size_t nt = (static_cast<size_t>(N) + 127) / 128, kt = (static_cast<size_t>(K) + 127) / 128;
+  return static_cast<size_t>(E) * nt * kt * 128 * 128;
+}
+
 int moe_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, moe_stream_t stream) {
   if (E < 1 || K < 1 || N < 1) return MOE_ERR_INVALID_ARG;
   if (!W || !Wq || !scales) return MOE_ERR_INVALID_ARG;
-  if (overlaps(W, static_cast<size_t>(E) * K * N * 2, Wq, static_cast<size_t>(E) * K * N)) return MOE_ERR_INVALID_ARG;
+  if (overlaps(W, static_cast<size_t>(E) * K * N * 2, Wq, moe_fp8_weight_bytes(E, K, N))) return MOE_ERR_INVALID_ARG;
   const int st = check_device();
   if (st != MOE_OK) return st;
   return launch_quantize_weights_fp8(W, E, K, N, Wq, scales, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess

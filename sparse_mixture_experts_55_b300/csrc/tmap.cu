@@ -67,18 +67,4 @@ bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, u
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// 3-D e4m3 bank [E, rows, cols] (cols = the contraction, contiguous), box =
-// 128 x 128 x 1, 128-byte swizzle.
-bool tmap_3d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E) {
-  auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[3] = {cols, rows, E};
-  cuuint64_t strides[2] = {cols, cols * rows};
-  cuuint32_t box[3] = {128, 128, 1};
-  cuuint32_t estr[3] = {1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void *>(ptr), dims, strides, box, estr,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 }  // namespace moe

@@ -30,7 +30,8 @@ def test_header_declares_the_boundary():
     names = _header_functions()
     assert names == sorted(["moe_workspace_bytes", "moe_forward", "moe_forward_stamped", "moe_block_forward",
                             "moe_block_forward_stamped", "moe_route",
-                            "moe_quantize_weights_fp8", "moe_forward_fp8", "moe_forward_fp8_stamped",
+                            "moe_quantize_weights_fp8", "moe_fp8_weight_bytes", "moe_forward_fp8",
+                            "moe_forward_fp8_stamped",
                             "moe_train_workspace_bytes", "moe_forward_train", "moe_backward", "moe_backward_timed",
                             "moe_expert_cache_init", "moe_expert_cache_plan", "moe_forward_cached",
                             "moe_forward_launches",
@@ -259,3 +260,10 @@ def test_forward_launch_counts(lib):
     assert lib.moe_forward_launches(64, 64, 128, 8, 2, _lib.MOE_F32) == 5
     assert lib.moe_forward_launches(0, 64, 128, 8, 2, _lib.MOE_BF16) == 0
     assert lib.moe_forward_launches(16, 63, 128, 8, 2, _lib.MOE_BF16) == 0
+
+
+def test_fp8_weight_bytes(lib):
+    # whole 128 x 128 tiles per expert, padding included
+    assert lib.moe_fp8_weight_bytes(8, 4096, 14336) == 8 * 4096 * 14336
+    assert lib.moe_fp8_weight_bytes(3, 200, 72) == 3 * 2 * 1 * 128 * 128
+    assert lib.moe_fp8_weight_bytes(0, 64, 64) == 0
