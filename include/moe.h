@@ -114,7 +114,8 @@ MOE_API size_t moe_workspace_bytes(int T, int d, int f, int E, int K, int dtype)
  * router and the grouping (one launch for T <= 256, two above), the row
  * gather, the two expert GEMMs, one more for e4m3 (the H quantiser), and a
  * combine kernel unless the down GEMM's epilogue forms y (bf16 and e4m3 calls
- * whose down projection is not split over its contraction); 0 for T = 0 or
+ * whose down projection is not split over its contraction, or with T <= 4);
+ * 0 for T = 0 or
  * invalid sizes.  Host only.
  */
 MOE_API int moe_forward_launches(int T, int d, int f, int E, int K, int dtype);

@@ -271,7 +271,12 @@ __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S,
   return t;
 }
 
-__device__ __forceinline__ float silu_f(float g) { return g / (1.0f + __expf(-g)); }
+// SiLU(g) = g / (1 + e^-g) with CUDA's fast exponential and fast division
+// intrinsics (a few ulp of fp32; the result is rounded to bf16 next).  An
+// IEEE division's longer dependent chain made this the epilogue's cost at
+// decode sizes, where one warp holds a tile's real rows.  For g below about
+// -88, e^-g is infinite and the quotient is 0, SiLU's limit.
+__device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <int MODE, int FORM, bool FP8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -618,13 +623,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tmem_wait_ld();
               if (FP8) {
                 const int cb = n0 + cc * 32;
+                // the chunk's 32 column scales of each bank: addresses clamped
+                // into range so that all sixteen loads are in flight together
+                float4 a4s[8], b4s[8];
+#pragma unroll
+                for (int j4 = 0; j4 < 8; ++j4) {
+                  const int c0 = min(cb + 4 * j4, args.n_out - 4);
+                  a4s[j4] = __ldg(reinterpret_cast<const float4 *>(cs1 + c0));
+                  b4s[j4] = __ldg(reinterpret_cast<const float4 *>(cs3 + c0));
+                }
 #pragma unroll
                 for (int j4 = 0; j4 < 8; ++j4) {
                   // n_out is a multiple of 16, so a group of four is all in or all out
-                  const int c0 = cb + 4 * j4;
-                  const bool in = c0 < args.n_out;
-                  const float4 a4 = in ? __ldg(reinterpret_cast<const float4 *>(cs1 + c0)) : make_float4(0, 0, 0, 0);
-                  const float4 b4 = in ? __ldg(reinterpret_cast<const float4 *>(cs3 + c0)) : make_float4(0, 0, 0, 0);
+                  const bool in = cb + 4 * j4 < args.n_out;
+                  const float4 a4 = in ? a4s[j4] : make_float4(0, 0, 0, 0);
+                  const float4 b4 = in ? b4s[j4] : make_float4(0, 0, 0, 0);
                   const float sa[4] = {a4.x, a4.y, a4.z, a4.w}, sb[4] = {b4.x, b4.y, b4.z, b4.w};
 #pragma unroll
                   for (int i = 0; i < 4; ++i) {
@@ -823,11 +836,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int col = n0 + cc * 32;
             if (FP8) {
               const float *cs2 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
+              // the chunk's 32 column scales, addresses clamped into range so
+              // that all eight loads are in flight together
+              float4 s4s[8];
+#pragma unroll
+              for (int j4 = 0; j4 < 8; ++j4)
+                s4s[j4] = __ldg(reinterpret_cast<const float4 *>(cs2 + min(col + 4 * j4, args.n_out - 4)));
 #pragma unroll
               for (int j4 = 0; j4 < 8; ++j4) {
-                const int c0 = col + 4 * j4;
-                const float4 s4 =
-                    c0 < args.n_out ? __ldg(reinterpret_cast<const float4 *>(cs2 + c0)) : make_float4(0, 0, 0, 0);
+                const float4 s4 = col + 4 * j4 < args.n_out ? s4s[j4] : make_float4(0, 0, 0, 0);
                 v[4 * j4] = __float_as_uint(__uint_as_float(v[4 * j4]) * s4.x);
                 v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) * s4.y);
                 v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) * s4.z);
@@ -849,9 +866,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
         if (args.y != nullptr && n0 < args.n_out) {
-          // Fused combine: the slot that completes this token's 256 columns
-          // last adds the K slot rows in slot order (the combine kernel's
-          // order, so y is the same bit for bit) and stores y.  The warp
+          // Fused combine: the writer that completes this token's 256 columns
+          // last (of its K slot rows times S splits) adds them -- per slot the
+          // splits in order, then the slots in order: the combine kernel's
+          // order, so y is the same bit for bit -- and stores y.  The warp
           // finishes its rows that arrived last together, four at a time,
           // lane l taking columns [8l, 8l + 8) of each.
           int tok = -1, last = 0;
@@ -861,7 +879,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (tok < 0 || tok >= args.T) {
               atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
             } else {
-              last = atomicAdd(args.tok_cnt + static_cast<size_t>(tok) * NT + t.nt, 1) == args.K - 1;
+              last = atomicAdd(args.tok_cnt + static_cast<size_t>(tok) * NT + t.nt, 1) == args.K * S - 1;
             }
           }
           unsigned m = __ballot_sync(0xffffffffu, last);
@@ -880,6 +898,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             float4 a[4][2], b[4][2];
             bool ok[4];
+            // split 0 of the slot outputs (this unit wrote split t.s)
+            const float *O0 = static_cast<const float *>(args.out);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
               ok[q] = false;
@@ -888,13 +908,28 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const int p1 = args.K > 1 ? args.pos[tk[q] * args.K + 1] : 0;
               ok[q] = p0 >= 0 && p0 < args.tk && p1 >= 0 && p1 < args.tk;
               if (!ok[q] || !col_in) continue;
-              const float *s0 = O + static_cast<size_t>(p0) * args.n_out + n0 + c8;
-              const float *s1 = O + static_cast<size_t>(p1) * args.n_out + n0 + c8;
+              const float *s0 = O0 + static_cast<size_t>(p0) * args.n_out + n0 + c8;
+              const float *s1 = O0 + static_cast<size_t>(p1) * args.n_out + n0 + c8;
               a[q][0] = __ldcg(reinterpret_cast<const float4 *>(s0));
               a[q][1] = __ldcg(reinterpret_cast<const float4 *>(s0 + 4));
               if (args.K > 1) {
                 b[q][0] = __ldcg(reinterpret_cast<const float4 *>(s1));
                 b[q][1] = __ldcg(reinterpret_cast<const float4 *>(s1 + 4));
+              }
+              // the other splits of each slot, added in split order
+              for (int sp = 1; sp < S; ++sp) {
+                const float *r0 = s0 + static_cast<size_t>(sp) * args.out_split_stride;
+                const float4 x0 = __ldcg(reinterpret_cast<const float4 *>(r0));
+                const float4 x1 = __ldcg(reinterpret_cast<const float4 *>(r0 + 4));
+                a[q][0].x += x0.x; a[q][0].y += x0.y; a[q][0].z += x0.z; a[q][0].w += x0.w;
+                a[q][1].x += x1.x; a[q][1].y += x1.y; a[q][1].z += x1.z; a[q][1].w += x1.w;
+                if (args.K > 1) {
+                  const float *r1 = s1 + static_cast<size_t>(sp) * args.out_split_stride;
+                  const float4 z0 = __ldcg(reinterpret_cast<const float4 *>(r1));
+                  const float4 z1 = __ldcg(reinterpret_cast<const float4 *>(r1 + 4));
+                  b[q][0].x += z0.x; b[q][0].y += z0.y; b[q][0].z += z0.z; b[q][0].w += z0.w;
+                  b[q][1].x += z1.x; b[q][1].y += z1.y; b[q][1].z += z1.z; b[q][1].w += z1.w;
+                }
               }
             }
 #pragma unroll

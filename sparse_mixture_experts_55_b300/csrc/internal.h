@@ -23,6 +23,9 @@ constexpr int kGroupTokens = 256;
 // Batches up to this many tokens are routed and grouped by one block, which
 // also clears the call's status words and counters (no memset before it).
 constexpr int kSingleRouteT = 8;
+// The down GEMM's epilogue forms y when its contraction is not split, and for
+// batches up to this many tokens when it is.
+constexpr int kFuseSplitT = 4;
 constexpr int kMaxE = 32;
 constexpr int kMaxK = 2;
 // Status-word slots at the start of the workspace.
@@ -66,7 +69,7 @@ struct WsLayout {
   size_t zero_bytes;  // bytes from `status` that every call clears (status word + split counters)
   int T, K;
   int TK;             // T*K: rows of the compact grouped buffers
-  bool fuse_combine;  // the down GEMM's epilogue also forms y (unsplit tensor-core paths)
+  bool fuse_combine;  // the down GEMM's epilogue also forms y (tensor-core paths: unsplit, or T <= kFuseSplitT)
   int R;              // padded grouped rows (upper bound): T*K + E*(kSegPad-1), rounded up to kSegPad
   int S;              // split count over the contraction of the down projection
   int kb_per_split;

@@ -194,7 +194,10 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bo
   const size_t n_cnt = L.S_gu > 1 ? (R / kSegPad) * static_cast<size_t>((f + 127) / 128) * 4 : 0;
   L.tile_cnt = take(n_cnt * sizeof(int));
   // fused combine: one slot-arrival counter per (token, 256-column tile of y)
-  L.fuse_combine = dtype != MOE_F32 && L.S == 1 && !routing_only;
+  // (a split down projection for the smallest batches too: the last of a
+  // token's K*S writers reads at most 2 * kFuseSplitT * S rows per tile, and
+  // a separate combine launch would cost more)
+  L.fuse_combine = dtype != MOE_F32 && (L.S == 1 || T <= kFuseSplitT) && !routing_only;
   L.tok_cnt = take(L.fuse_combine ? static_cast<size_t>(T) * ((d + 255) / 256) * sizeof(int) : 0);
   L.zero_bytes = o - L.status;
   L.idx = take(TK * 4);

@@ -250,9 +250,12 @@ def test_forward_launch_counts(lib):
     # prefill: the down projection is not split, so its epilogue forms y
     assert lib.moe_forward_launches(4096, 4096, 14336, 8, 2, _lib.MOE_BF16) == 5
     assert lib.moe_forward_launches(4096, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 6
-    # one token: router and grouping fused, split down projection, separate combine
-    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_BF16) == 5
-    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 6
+    # one token: router and grouping fused, split down projection whose
+    # epilogue still forms y (up to 4 tokens)
+    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_BF16) == 4
+    assert lib.moe_forward_launches(1, 4096, 14336, 8, 2, _lib.MOE_FP8_E4M3) == 5
+    # eight tokens: split down projection, separate combine
+    assert lib.moe_forward_launches(8, 4096, 14336, 8, 2, _lib.MOE_BF16) == 5
     # 256 tokens still fuse the router and the grouping, 257 do not
     assert lib.moe_forward_launches(256, 64, 128, 8, 2, _lib.MOE_F32) == 5
     assert lib.moe_forward_launches(257, 64, 128, 8, 2, _lib.MOE_F32) == 6
