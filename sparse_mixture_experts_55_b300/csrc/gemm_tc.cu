@@ -155,6 +155,12 @@ struct GemmArgs {
   int *tok_cnt;             // [T, num_n_tiles], zero at launch
   int T, K;
   unsigned long long *stamps;  // profiling calls: stage begin/end times (stamps.cuh), else null
+  // tail split (multicast pairs, unsplit contraction): scratch for the fp32
+  // first halves of the last wave's tiles, [tail_slots][2][BM][BN], and one
+  // arrival counter per (slot, CTA), zero at launch; null disables it
+  float *tail_part;
+  int *tail_flag;
+  int tail_slots;
 };
 
 struct Ctrl {
@@ -168,6 +174,8 @@ struct Ctrl {
   uint32_t tmem_base;
   int abort;
   int total_units;
+  int total_items;  // work items: units, with the last wave's units split in two halves when tail_base >= 0
+  int tail_base;
   int ustart[kMaxE + 1];
   int mtiles[kMaxE];
   int poff[kMaxE + 1];
@@ -276,6 +284,53 @@ __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S,
 // IEEE division's longer dependent chain made this the epilogue's cost at
 // decode sizes, where one warp holds a tile's real rows.  For g below about
 // -88, e^-g is infinite and the quotient is 0, SiLU's limit.
+// Work item `it` of the persistent schedule: a whole unit, or (the tail
+// split) one k-half of one of the last wave's units.  Items before tail_base
+// are units; item tail_base + j is half (j & 1) of unit tail_base + (j >> 1),
+// both halves computing the same tiles: the first half (role 1) stores its
+// fp32 sums, the second (role 2, the owner) adds them and runs the epilogue.
+struct Work {
+  Tile t;
+  int kb0, kb1, role, slot;
+};
+
+template <int FORM>
+__device__ __forceinline__ Work work_item(int it, const Ctrl &c, int NT, int S, int rank, int kb_per_split, int num_kb) {
+  Work w;
+  int unit = it;
+  w.role = 0;
+  w.slot = 0;
+  if (c.tail_base >= 0 && it >= c.tail_base) {
+    const int j = it - c.tail_base;
+    unit = c.tail_base + (j >> 1);
+    w.role = 1 + (j & 1);
+    w.slot = j >> 1;
+  }
+  w.t = decode_unit<FORM>(unit, c, NT, S, rank);
+  w.kb0 = w.t.s * kb_per_split;
+  w.kb1 = min(num_kb, w.kb0 + kb_per_split);
+  if (w.role) {
+    const int mid = w.kb0 + (w.kb1 - w.kb0) / 2;
+    if (w.role == 1) w.kb1 = mid;
+    else w.kb0 = mid;
+  }
+  return w;
+}
+
+// Bounded wait until *p reaches target (a counter other CTAs raise); records
+// MOE_ERR_DEVICE_TIMEOUT and returns false after about one second.
+__device__ __noinline__ bool wait_count(const int *p, int target, int *status) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while (*reinterpret_cast<const volatile int *>(p) < target) {
+    if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
+      atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+    __nanosleep(64);
+  }
+  return true;
+}
+
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <int MODE, int FORM, bool FP8>
@@ -352,10 +407,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     c.uoff[args.E] = args.offsets[args.E];
     c.ustart[args.E] = acc;
     c.total_units = acc;
+    // Tail split: when the last of several waves of units leaves most
+    // clusters idle, its r units run as 2r halves of their contraction.
+    int items = acc, tail_base = -1;
+    if (FORM == FORM_MC2 && S == 1 && args.tail_part != nullptr) {
+      const int waves = (acc + nclusters - 1) / nclusters;
+      const int r = acc - (waves - 1) * nclusters;
+      if (waves >= 3 && r > 0 && 2 * r <= nclusters && r <= args.tail_slots && args.num_kb >= 2) {
+        tail_base = (waves - 1) * nclusters;
+        items = tail_base + 2 * r;
+      }
+    }
+    c.total_items = items;
+    c.tail_base = tail_base;
     c.abort = 0;
   }
   __syncthreads();
-  const int total = c.total_units;
+  const int total = c.total_items;
   // Both CTAs of a cluster read the same table, so they leave together.
   if (cluster >= total) return;
 
@@ -460,10 +528,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     pol_b = ptx::policy_evict_normal();
     ptx::prefetch_tmap(&tmB0);
     if (MODE == MODE_GATE_UP) ptx::prefetch_tmap(&tmB1);
-    t_first = decode_unit<FORM>(cluster, c, NT, S, rank);
-    kb_first = t_first.s * args.kb_per_split;
-    const int kb_end = min(args.num_kb, kb_first + args.kb_per_split);
-    pre_kb = min(STAGES, kb_end - kb_first);
+    const Work w0 = work_item<FORM>(cluster, c, NT, S, rank, args.kb_per_split, args.num_kb);
+    t_first = w0.t;
+    kb_first = w0.kb0;
+    pre_kb = min(STAGES, w0.kb1 - w0.kb0);
     for (int i = 0; i < pre_kb; ++i) {
       arm(i);
       load_b(i, t_first, (kb_first + i) * KB_ELEMS);
@@ -501,10 +569,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (lane == 0) {
       bool ok = true;
       for (int u = cluster; ok && u < total; u += nclusters) {
-        const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
-        const int kb0 = t.s * args.kb_per_split;
-        const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
-        for (int kb = u == cluster ? kb0 + pre_kb : kb0; kb < kb1; ++kb) {
+        const Work w = work_item<FORM>(u, c, NT, S, rank, args.kb_per_split, args.num_kb);
+        const Tile &t = w.t;
+        for (int kb = u == cluster ? w.kb0 + pre_kb : w.kb0; kb < w.kb1; ++kb) {
           if (!wait_bounded(&c.empty[p_stage], p_phase ^ 1u, c, args.status, true)) { ok = false; break; }
           const int k0 = kb * KB_ELEMS;
           arm(p_stage);
@@ -530,9 +597,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // failure-path test: this wait expires, raising the CTA's abort flag
       if (args.force_timeout) ok = wait_bounded(&c.stall, 0, c, args.status, true);
       for (int u = cluster; ok && u < total; u += nclusters) {
-        const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
-        const int kb0 = t.s * args.kb_per_split;
-        const int kb1 = min(args.num_kb, kb0 + args.kb_per_split);
+        const Work w = work_item<FORM>(u, c, NT, S, rank, args.kb_per_split, args.num_kb);
+        const int kb0 = w.kb0, kb1 = w.kb1;
         const int acc = local & 1;
         const uint32_t apar = (local >> 1) & 1;
         if (!wait_bounded(&c.tempty[acc], apar ^ 1u, c, args.status, true)) { ok = false; break; }
@@ -582,7 +648,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tempty_at1 = ptx::mapa_shared(ptx::smem_u32(&c.tempty[1]), PAIR ? 0 : rank);
     int local = 0;
     for (int u = cluster; u < total; u += nclusters) {
-      const Tile t = decode_unit<FORM>(u, c, NT, S, rank);
+      const Work w = work_item<FORM>(u, c, NT, S, rank, args.kb_per_split, args.num_kb);
+      const Tile &t = w.t;
       const int acc = local & 1;
       const uint32_t apar = (local >> 1) & 1;
       int ok = 1;
@@ -590,6 +657,55 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __shfl_sync(0xffffffffu, ok, 0);
       if (!ok) break;
       ptx::tc_fence_after();
+      // Tail split: this thread's accumulator row in the (slot, CTA) scratch tile
+      float *tail_row = w.role ? args.tail_part + (static_cast<size_t>(w.slot) * 2 + rank) * BM * BN +
+                                     static_cast<size_t>(q * 32 + lane) * BN
+                               : nullptr;
+      if (w.role == 1) {
+        // first k-half: store the raw fp32 sums for the owner, release the
+        // accumulator, count this warp's arrival
+        const uint32_t tb = tmem + acc * ACC_COLS + (static_cast<uint32_t>(q * 32) << 16);
+#pragma unroll 1
+        for (int cc = 0; cc < BN / 32; ++cc) {
+          uint32_t v[32];
+          ptx::tmem_ld_32x32b_x32(tb + cc * 32, v);
+          ptx::tmem_wait_ld();
+#pragma unroll
+          for (int j4 = 0; j4 < 8; ++j4)
+            __stcg(reinterpret_cast<float4 *>(tail_row + cc * 32 + 4 * j4),
+                   make_float4(__uint_as_float(v[4 * j4]), __uint_as_float(v[4 * j4 + 1]),
+                               __uint_as_float(v[4 * j4 + 2]), __uint_as_float(v[4 * j4 + 3])));
+        }
+        __threadfence();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          atomicAdd(args.tail_flag + w.slot * 2 + rank, 1);
+          ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
+        }
+        ++local;
+        continue;
+      }
+      const float *part = nullptr;  // owner of a split tile: the first half's sums, added below
+      if (w.role == 2) {
+        int okp = 1;
+        if (lane == 0) okp = wait_count(args.tail_flag + w.slot * 2 + rank, 4, args.status) ? 1 : 0;
+        okp = __shfl_sync(0xffffffffu, okp, 0);
+        __threadfence();
+        if (okp) part = tail_row;
+      }
+      // acc_cols[i] += part[c0 + i]: the first half's sums, in one fixed order
+      auto add_part = [&](uint32_t(&r)[32], int c0) {
+        if (part == nullptr) return;
+#pragma unroll
+        for (int j4 = 0; j4 < 8; ++j4) {
+          const float4 x = __ldcg(reinterpret_cast<const float4 *>(part + c0 + 4 * j4));
+          r[4 * j4] = __float_as_uint(x.x + __uint_as_float(r[4 * j4]));
+          r[4 * j4 + 1] = __float_as_uint(x.y + __uint_as_float(r[4 * j4 + 1]));
+          r[4 * j4 + 2] = __float_as_uint(x.z + __uint_as_float(r[4 * j4 + 2]));
+          r[4 * j4 + 3] = __float_as_uint(x.w + __uint_as_float(r[4 * j4 + 3]));
+        }
+      };
       // This thread's accumulator row: padded grouped row `row`; the first
       // count_e rows of an expert's segment are real, the rest padding, and
       // rows past the segment (the phantom tile of pair MMA) are not stored.
@@ -621,6 +737,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               ptx::tmem_ld_32x32b_x32(tbase + cc * 32, g);
               ptx::tmem_ld_32x32b_x32(tbase + BN / 2 + cc * 32, v);
               ptx::tmem_wait_ld();
+              add_part(g, cc * 32);
+              add_part(v, BN / 2 + cc * 32);
               if (FP8) {
                 const int cb = n0 + cc * 32;
                 // the chunk's 32 column scales of each bank: addresses clamped
@@ -833,6 +951,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t v[32];
             ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
             ptx::tmem_wait_ld();
+            add_part(v, cc * 32);
             const int col = n0 + cc * 32;
             if (FP8) {
               const float *cs2 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
@@ -1138,6 +1257,19 @@ cudaError_t launch_form(int form, const Grids &g, cudaStream_t s, bool pdl, cons
   return launch_gemm<MODE, FORM_MC2, FP8>(g, s, pdl, a, ah, aq, b0, b1, args);
 }
 
+// Tail split of an unsplit GEMM in the multicast-pair form (the kernel decides
+// from the routing whether the last wave is worth splitting); `which` selects
+// the GEMM's own arrival counters (0 gate/up, 1 down).
+void set_tail_split(GemmArgs &g, const WsLayout &L, const Ptrs &P, int form, int splits, int which) {
+  g.tail_part = nullptr;
+  g.tail_flag = nullptr;
+  g.tail_slots = 0;
+  if (form != FORM_MC2 || splits != 1 || L.tail_slots < 1) return;
+  g.tail_part = P.tail_part;
+  g.tail_flag = P.tail_flag + which * L.tail_slots * 2;
+  g.tail_slots = L.tail_slots;
+}
+
 // The down GEMM's fused-combine arguments (y formed in its epilogue).
 void set_fused_combine(GemmArgs &g, const WsLayout &L, const Ptrs &P, void *y, unsigned flags) {
   if (!L.fuse_combine) return;
@@ -1190,6 +1322,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.use_slots = slot_of ? 1 : 0;
   for (int e = 0; e < E && slot_of; ++e) g1.wslot[e] = slot_of[e];
   g1.stamps = P.stamps;
+  set_tail_split(g1, L, P, form, L.S_gu, 0);
   err = launch_form<MODE_GATE_UP, false>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   if (err != cudaSuccess) return err;
 
@@ -1206,6 +1339,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.num_kb = (f + BK - 1) / BK;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
+  set_tail_split(g2, L, P, form, L.S, 1);
   return launch_form<MODE_DOWN, false>(form, grids, s, true, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 
@@ -1254,6 +1388,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g1.b_kt = kt13;
   g1.status = P.status;
   g1.stamps = P.stamps;
+  set_tail_split(g1, L, P, form, L.S_gu, 0);
   err = launch_form<MODE_GATE_UP, true>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   // H rows to e4m3 with their own scales
   if (err == cudaSuccess) err = launch_quant_h(f, E, L.R, g1.num_n_tiles, P, num_sms, s);
@@ -1277,6 +1412,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   g2.habs = nullptr;
   g2.b_nt = nt2;
   g2.b_kt = kt2;
+  set_tail_split(g2, L, P, form, L.S, 1);
   return launch_form<MODE_DOWN, true>(form, grids, s, true, tm_h, tm_hh, tm_hq, tm_w2, tm_w2, g2);
 }
 

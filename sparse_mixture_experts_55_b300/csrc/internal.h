@@ -60,10 +60,12 @@ cudaError_t launch_kernel(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_
 
 struct WsLayout {
   // byte offsets into the workspace
-  size_t status, tile_cnt, tok_cnt, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf,
+  size_t status, tile_cnt, tok_cnt, tail_flag, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, xperm, hbuf,
       obuf, gu_part, xnorm;
   size_t xscale, habs, hq, hscale;  // e4m3 variant only (0 bytes otherwise)
   size_t ab, dye, dab, dxc, dl, dwg_part;  // training only (0 bytes otherwise)
+  size_t tail_part;   // expert GEMMs' tail split: fp32 first halves (0 bytes when no GEMM is unsplit)
+  int tail_slots;     // split tiles the scratch holds (per GEMM launch)
   int dwg_chunks;     // token chunks of the router-weight gradient's partial sums
   size_t total;
   size_t zero_bytes;  // bytes from `status` that every call clears (status word + split counters)
@@ -105,6 +107,8 @@ struct Ptrs {
   int *status;
   int *tile_cnt;  // arrival counters of split gate/up tiles
   int *tok_cnt;   // [T, down n-tiles] slot arrivals of the fused combine
+  int *tail_flag; // [2][tail_slots][2] arrivals on the tail split's first halves (gate/up, down)
+  float *tail_part;  // [tail_slots][2][128][256] fp32 first halves of the tail split
   int32_t *idx;
   float *gate;
   int32_t *blockcounts, *offsets, *poffsets, *pos, *perm_tok;

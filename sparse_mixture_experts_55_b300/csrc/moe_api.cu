@@ -199,6 +199,11 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bo
   // a separate combine launch would cost more)
   L.fuse_combine = dtype != MOE_F32 && (L.S == 1 || T <= kFuseSplitT) && !routing_only;
   L.tok_cnt = take(L.fuse_combine ? static_cast<size_t>(T) * ((d + 255) / 256) * sizeof(int) : 0);
+  // tail split of an unsplit expert GEMM (gemm_tc.cu): at most one split
+  // tile per two 2-CTA clusters, i.e. num_sms / 4, each for both CTAs
+  const bool tail = dtype != MOE_F32 && !routing_only && (L.S == 1 || L.S_gu == 1) && touched > 0;
+  L.tail_slots = tail ? (num_sms > 0 ? num_sms : 1) / 4 + 1 : 0;
+  L.tail_flag = take(static_cast<size_t>(L.tail_slots) * 2 * 2 * sizeof(int));
   L.zero_bytes = o - L.status;
   L.idx = take(TK * 4);
   L.gate = take(TK * 4);
@@ -235,6 +240,7 @@ WsLayout ws_layout(int T, int d, int f, int E, int K, int dtype, int num_sms, bo
   L.dxc = take(tr * TK * d * 4);
   L.dl = take(tr * static_cast<size_t>(T) * E * 4);
   L.dwg_part = take(tr * static_cast<size_t>(L.dwg_chunks) * d * E * 4);
+  L.tail_part = take(static_cast<size_t>(L.tail_slots) * 2 * 128 * 256 * sizeof(float));
   L.total = o;
   return L;
 }
@@ -245,6 +251,8 @@ Ptrs carve(void *ws, const WsLayout &L) {
   P.status = reinterpret_cast<int *>(b + L.status);
   P.tile_cnt = reinterpret_cast<int *>(b + L.tile_cnt);
   P.tok_cnt = reinterpret_cast<int *>(b + L.tok_cnt);
+  P.tail_flag = reinterpret_cast<int *>(b + L.tail_flag);
+  P.tail_part = reinterpret_cast<float *>(b + L.tail_part);
   P.idx = reinterpret_cast<int32_t *>(b + L.idx);
   P.gate = reinterpret_cast<float *>(b + L.gate);
   P.blockcounts = reinterpret_cast<int32_t *>(b + L.blockcounts);

@@ -55,9 +55,12 @@ def test_status_strings_and_version(lib):
 def test_workspace_bytes(lib):
     mix = lib.moe_workspace_bytes(4096, 4096, 14336, 8, 2, _lib.MOE_BF16)
     # grouped rows: 8192 tokens*slots + 8 * 127 pad rows, rounded to 128 -> 9216;
-    # padded X_perm and H, compact fp32 expert outputs, the block's normalised input
+    # padded X_perm and H, compact fp32 expert outputs, the block's normalised
+    # input, and the expert GEMMs' tail-split scratch (one 2 x 128 x 256 fp32
+    # pair of tiles per four SMs and one more)
     R, TK = 9216, 8192
-    lower = R * 4096 * 2 + R * 14336 * 2 + TK * 4096 * 4 + 4096 * 4096 * 2
+    tail = (148 // 4 + 1) * 2 * 128 * 256 * 4
+    lower = R * 4096 * 2 + R * 14336 * 2 + TK * 4096 * 4 + 4096 * 4096 * 2 + tail
     assert lower <= mix <= lower + 2 * 1024 * 1024
     assert lib.moe_workspace_bytes(0, 64, 128, 8, 2, _lib.MOE_F32) > 0
     # invalid shapes -> 0
