@@ -344,6 +344,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   constexpr uint16_t kAll = FormInfo<FORM>::ALL;  // every CTA of the cluster
   using RG = Ring<PAIR>;
   constexpr int STAGES = RG::STAGES;
+  // a k-block is one 128-byte row of A and of B in shared memory: 64 bf16 or
+  // 128 e4m3 elements of the contraction
+  constexpr int KB_ELEMS = FP8 ? 128 : BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t *base = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t *sA = base;
@@ -407,10 +410,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     c.uoff[args.E] = args.offsets[args.E];
     c.ustart[args.E] = acc;
     c.total_units = acc;
-    // Tail split: when the last of several waves of units leaves most
-    // clusters idle, its r units run as 2r halves of their contraction.
+    // Tail split: when the last of several waves of long units (a
+    // contraction of 8192 or more elements, the down projection's) leaves
+    // most clusters idle, its r units run as 2r halves of their contraction.
+    // (Units of 4096 elements, the gate/up projection's, gain nothing: the
+    // owner's wait for the partial costs about what the halving saves.)
     int items = acc, tail_base = -1;
-    if (FORM == FORM_MC2 && S == 1 && args.tail_part != nullptr) {
+    if (FORM == FORM_MC2 && S == 1 && args.tail_part != nullptr && args.num_kb * KB_ELEMS >= 8192) {
       const int waves = (acc + nclusters - 1) / nclusters;
       const int r = acc - (waves - 1) * nclusters;
       if (waves >= 3 && r > 0 && 2 * r <= nclusters && r <= args.tail_slots && args.num_kb >= 2) {
@@ -432,9 +438,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint32_t issued = 0, last_par = 0;
   int p_stage = 0;
   uint32_t p_phase = 0;
-  // a k-block is one 128-byte row of A and of B in shared memory: 64 bf16 or
-  // 128 e4m3 elements of the contraction
-  constexpr int KB_ELEMS = FP8 ? 128 : BK;
   uint64_t pol_a = 0, pol_b = 0;
   // Stage `st` of k-block k0 of tile t: arm its barrier for all the bytes
   // that complete it, and issue this CTA's weight (B) and activation (A) copies.

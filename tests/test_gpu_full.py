@@ -65,6 +65,28 @@ def test_prefill_full(moe, mixtral, cuda_device):
     _run_and_check(moe, inp, sample=48)
 
 
+def test_prefill_tail_split_against_unsplit_form(moe, mixtral, cuda_device):
+    """At the prefill size the down projection's last wave is split over its
+    contraction in the default multicast-pair form (the tail split), not in
+    the CTA-pair form: the two agree within the parity bar, differing by the
+    one extra fp32 rounding of the split tiles' sums, and the split form is
+    bitwise deterministic."""
+    inp = W.prefill(device=cuda_device, weights=mixtral)
+    T, d, f, E, K = inp.shape
+    ws = moe.Workspace(T, d, f, E, K, torch.bfloat16, cuda_device)
+    y = moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, workspace=ws,
+                        flags=moe.MOE_GEMM_MULTICAST_PAIRS)
+    y2 = moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, workspace=ws,
+                         flags=moe.MOE_GEMM_MULTICAST_PAIRS)
+    yp = moe.moe_forward(inp.x, inp.Wg, inp.W1, inp.W3, inp.W2, K, workspace=ws, flags=moe.MOE_GEMM_PAIR_MMA)
+    assert moe.moe_read_status(ws) == 0
+    assert torch.equal(y, y2)
+    err = parity.rel_linf(_np(y.float()), _np(yp.float()))
+    print(f"\nprefill multicast pairs (tail split) vs CTA pairs: rel {err:.2e}, "
+          f"bitwise equal {torch.equal(y, yp)}")
+    assert err <= parity.TOL["bf16"]
+
+
 @pytest.mark.parametrize("T", [1, 8, 32, 128])
 def test_decode_full(moe, mixtral, cuda_device, T):
     inp = W.decode(T, device=cuda_device, weights=mixtral)
