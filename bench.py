@@ -11,6 +11,8 @@ The run uses one GPU from one process; multi-process launches are refused.
                forwards
   stages_ms    each kernel's span inside that same region, from the
                global-timer stamps every kernel writes (moe_forward_stamped)
+  stages_exclusive_ms  the part of each span after the previous kernels
+               ended (spans overlap under programmatic dependent launch)
   roofline     the gate/up expert GEMM (the dominant kernel): algorithmic
                FLOPs (or bytes at decode sizes) per launch over its in-run
                span, against MEASURED_PEAKS.json (burst or sustained peak as
@@ -364,6 +366,23 @@ def stage_stats(moe, stamps, steps: int):
     out = {n: statistics.mean((s[n][1] - s[n][0]) / 1e6 for s in spans if n in s) for n in names}
     step = statistics.mean((max(e for _, e in s.values()) - min(b for b, _ in s.values())) / 1e6 for s in spans)
     return out, step, step - sum(out.values())
+
+
+def exclusive_stage_ms(moe, stamps) -> dict:
+    """Per-stage mean exclusive span (ms): a kernel's end minus the later of
+    its own start and the latest end among the kernels that started before
+    it.  With programmatic dependent launch a kernel starts (and issues its
+    weight copies) while the previous one drains, so the raw spans overlap;
+    the exclusive spans are what each kernel adds to the step and sum to the
+    step span less the launch gaps."""
+    acc: dict = {}
+    for s in moe.stage_spans(stamps):
+        done = None
+        for name, (b, e) in sorted(s.items(), key=lambda kv: kv[1][0]):
+            lo = b if done is None else max(b, done)
+            acc.setdefault(name, []).append(max(0, e - lo) / 1e6)
+            done = e if done is None else max(done, e)
+    return {n: statistics.mean(v) for n, v in acc.items()}
 
 
 def make_inputs(cfg_name: str, dev, weights=None):
@@ -987,6 +1006,7 @@ def decode_record(moe, weights, q8, dev, stream, steps: int, warmup: int, peaks,
             run()
         ms, clocks, stamps = timed_region(moe, run, steps, dev, stream, stamped=True)
         stages, span, gaps = stage_stats(moe, stamps, steps)
+        excl = exclusive_stage_ms(moe, stamps)
         _, _, bytes_step, gu_bytes = algorithmic(c, n_touched)
         dn_bytes = down_bytes(c, n_touched)
         gbs = bytes_step / (ms / 1e3) / 1e9
@@ -996,10 +1016,17 @@ def decode_record(moe, weights, q8, dev, stream, steps: int, warmup: int, peaks,
             "ms_per_step": ms, "tokens_per_s": T / (ms / 1e3), "touched_experts": n_touched,
             "algorithmic_bytes_per_step": bytes_step, "gbs": gbs, "frac_of_hbm": gbs / peaks["hbm_gbs"],
             "gate_up_gemm": {"ms": stages["gate_up_gemm"], "bytes": gu_bytes, "gbs": gu_gbs,
-                             "frac_of_hbm": gu_gbs / peaks["hbm_gbs"]},
+                             "frac_of_hbm": gu_gbs / peaks["hbm_gbs"],
+                             "exclusive_ms": excl["gate_up_gemm"],
+                             "frac_of_hbm_exclusive": gu_bytes / (excl["gate_up_gemm"] / 1e3) / 1e9
+                             / peaks["hbm_gbs"]},
             "down_gemm": {"ms": stages["down_gemm"], "bytes": dn_bytes, "gbs": dn_gbs,
-                          "frac_of_hbm": dn_gbs / peaks["hbm_gbs"]},
+                          "frac_of_hbm": dn_gbs / peaks["hbm_gbs"],
+                          "exclusive_ms": excl["down_gemm"],
+                          "frac_of_hbm_exclusive": dn_bytes / (excl["down_gemm"] / 1e3) / 1e9
+                          / peaks["hbm_gbs"]},
             "stages_ms": {k: round(v, 4) for k, v in stages.items()},
+            "stages_exclusive_ms": {k: round(v, 4) for k, v in excl.items()},
             "launch_gaps_ms": gaps, "clocks": clocks}
         del run
     return out
@@ -1045,6 +1072,7 @@ def run_ours(args):
     # very region and add up to its step time (less launch gaps)
     ms, clocks, stamps = timed_region(moe, run, steps, dev, stream, stamped=True)
     stage_ms, step_span_ms, gaps_ms = stage_stats(moe, stamps, steps)
+    excl_ms = exclusive_stage_ms(moe, stamps)
     y_out = run.y.clone()
     # the same steps through plain moe_forward (no stamps), for comparison
     ms_plain, clocks_plain, _ = timed_region(moe, run, steps, dev, stream, stamped=False)
@@ -1095,8 +1123,12 @@ def run_ours(args):
                                f"{peak_note} ({peak_src}): {why}"}
         dn_ms = stage_ms["down_gemm"]
         dn_flops = T * K * 2 * d * f
+        dn_x = excl_ms["down_gemm"]
         roof["down_gemm"] = {"kernel_ms": dn_ms, "achieved": dn_flops / (dn_ms / 1e3) / 1e12,
-                             "frac": dn_flops / (dn_ms / 1e3) / 1e12 / peak, "algorithmic_flops_per_launch": dn_flops}
+                             "frac": dn_flops / (dn_ms / 1e3) / 1e12 / peak, "algorithmic_flops_per_launch": dn_flops,
+                             "exclusive_ms": dn_x, "frac_exclusive": dn_flops / (dn_x / 1e3) / 1e12 / peak,
+                             "frac_of_burst_exclusive": dn_flops / (dn_x / 1e3) / 1e12
+                             / (peaks["bf16_tflops"] * ratio)}
     line = {
         "metric": METRIC, "value": tokens_per_s, "unit": "tokens/s", "n_gpus": 1, "steps": steps,
         "warmup": warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
@@ -1108,6 +1140,7 @@ def run_ours(args):
         "tflops": flops / (ms / 1e3) / 1e12,
         "hbm_gbs_algorithmic": bytes_step / (ms / 1e3) / 1e9,
         "stages_ms": {k: round(v, 4) for k, v in stage_ms.items()},
+        "stages_exclusive_ms": {k: round(v, 4) for k, v in excl_ms.items()},
         "step_span_ms": step_span_ms, "launch_gaps_ms": gaps_ms,
         "roofline": roof,
         "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,

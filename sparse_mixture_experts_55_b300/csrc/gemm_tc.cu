@@ -55,6 +55,19 @@
 // the same 128 columns of X W3, so one MMA feeds both SwiGLU branches.  The
 // training forward also stores a = X W1 and b = X W3 (save_ab).
 //
+// Launch overlap: the kernel is launched with programmatic dependent launch.
+// Before its grid-dependency wait each producer builds the unit table and
+// issues the weight (B) copies of its first ring stages, which depend on
+// nothing the previous kernel writes; the activation (A) copies follow the
+// wait.
+// Tail split (multicast pairs, unsplit contractions of 8192 or more
+// elements, three or more waves): the units of the last, partial wave run as
+// two halves of the contraction on twice as many clusters.  The first-half
+// CTA stores its fp32 sums into a workspace slot and raises a counter; the
+// second-half CTA waits for it (bounded), adds the slot to its own
+// accumulator in a fixed order and runs the tile's normal epilogue, so the
+// result does not depend on which half finishes first.
+//
 // Every mbarrier wait is bounded (about one second); on expiry the CTA records
 // MOE_ERR_DEVICE_TIMEOUT in the status word, stops issuing work, waits (again
 // bounded) for its own copies and MMAs in flight, frees TMEM and returns.

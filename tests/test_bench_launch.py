@@ -76,3 +76,20 @@ def test_stage_stats_from_stamps():
     assert abs(stages["gate_up_gemm"] - 1.0) < 1e-12 and abs(stages["down_gemm"] - 0.5) < 1e-12
     assert abs(span - 1.528) < 1e-12
     assert abs(gaps - 0.008) < 1e-12
+
+
+def test_exclusive_spans_clip_overlap():
+    n = moe._lib.MOE_NUM_STAGES
+    never = np.iinfo(np.uint64).max
+    b = np.full(n, never, dtype=np.uint64)
+    e = np.zeros(n, dtype=np.uint64)
+    # gather 0-5 us; gate/up starts at 3 us (overlap 2 us) and ends at 100 us;
+    # down starts at 90 us (overlap 10 us) and ends at 150 us
+    for s_, (lo, hi) in {2: (0, 5_000), 3: (3_000, 100_000), 5: (90_000, 150_000)}.items():
+        b[s_], e[s_] = 1_000_000 + lo, 1_000_000 + hi
+    stamps = torch.from_numpy(np.concatenate([b, e]).view(np.int64)[None])
+    stages, span, gaps = bench.stage_stats(moe, stamps, 1)
+    excl = bench.exclusive_stage_ms(moe, stamps)
+    assert abs(stages["down_gemm"] - 0.060) < 1e-12 and abs(excl["down_gemm"] - 0.050) < 1e-12
+    assert abs(excl["gate_up_gemm"] - 0.095) < 1e-12 and abs(excl["gather"] - 0.005) < 1e-12
+    assert abs(sum(excl.values()) - span) < 1e-12 and gaps < 0
