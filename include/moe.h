@@ -214,9 +214,11 @@ MOE_API int moe_block_forward_stamped(void *h, const void *Wg, const void *W1, c
  *   e4m3: 1 sign, 4 exponent bits (bias 7), 3 mantissa bits, no infinities,
  *         largest finite magnitude 448; values round to nearest, ties to the
  *         even code, and saturate at +-448.
- *   weights: one fp32 scale per output column n of each expert bank,
- *         s[e, n] = max_k |W[e, k, n]| / 448 (1 for an all-zero column);
- *         codes q[e, n, k] = e4m3(W[e, k, n] / s[e, n]) (fp32 division),
+ *   weights: from a[e, n] = max_k |W[e, k, n]| per output column n of
+ *         each expert bank, the fp32 scale s[e, n] = a / 448 and the factor
+ *         u[e, n] = 448 / a (fp32 divisions; both 1 for an all-zero column, a
+ *         nonzero a below 2^-100 taken as 2^-100); codes
+ *         q[e, n, k] = e4m3(W[e, k, n] * u[e, n]) (one fp32 product),
  *         stored K-contiguous, i.e. transposed from the bf16 bank.
  *   activations: the same with one scale per row, for each grouped token row
  *         (gate/up input) and for each row of the SwiGLU output H after it is

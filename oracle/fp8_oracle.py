@@ -13,16 +13,20 @@ scheme, so the scheme below is this library's, written out plainly:
     infinities; S.1111.111 is NaN; largest finite magnitude 448; subnormals
     m/8 * 2^-6).  Rounding to e4m3 is to the nearest value, ties to the even
     code, and magnitudes beyond 448 saturate to 448.
-  * expert weights: one fp32 scale per output column of each expert,
-    s = max_k |W[k, n]| / 448 (1 where the column is all zero), codes
-    q = e4m3(W / s), stored K-contiguous ([E, N, K]); W is dequantised as
-    e4m3(q) * s.
+  * expert weights: one fp32 scale per output column of each expert from
+    a = max_k |W[k, n]|: the scale s = a / 448 and its inverse u = 448 / a
+    (both 1 where the column is all zero; a nonzero a below 2^-100 counts
+    as 2^-100, so that u stays finite).  Codes q = e4m3(W * u), stored
+    K-contiguous ([E, N, K]); W is dequantised as e4m3(q) * s.  Scaling by
+    the inverse, one division per column and a product per element, is the
+    usual form of an amax-scaled FP8 cast.
   * activations: one fp32 scale per token row in the same way (x for the
     gate/up projection; the SwiGLU output H, rounded to bf16 first, for the
     down projection).
-  * the divisions that decide a code are float32 operations, as in the CUDA
-    kernels (where floating point decides an integer both sides take that
-    decision in the same precision); everything after decoding is float64.
+  * the divisions giving s and u and the product that decides a code are
+    float32 operations, as in the CUDA kernels (where floating point decides
+    an integer both sides take that decision in the same precision);
+    everything after decoding is float64.
 
 The layer is then the plain definition of ``moe_oracle.moe_layer`` with the
 dequantised operands: y = sum_i G(x)_i E_i(x), G from the unquantised router.
@@ -82,20 +86,36 @@ def _f32(a) -> np.ndarray:
     return np.asarray(a, dtype=np.float32)
 
 
-def scale_of(absmax) -> np.ndarray:
-    """fp32 scale absmax / 448 (a float32 division); 1 where absmax is 0."""
+AMAX_FLOOR = np.float32(2.0 ** -100)
+
+
+def _amax_used(absmax) -> np.ndarray:
+    """The maximum magnitude the scale is taken from: 448 where it is 0 (so
+    that s = u = 1), at least 2^-100 otherwise."""
     absmax = np.asarray(absmax, dtype=np.float32)
-    s = absmax / np.float32(E4M3_MAX)
-    return np.where(absmax > 0, s, np.float32(1.0)).astype(np.float32)
+    return np.where(absmax > 0, np.maximum(absmax, AMAX_FLOOR), np.float32(E4M3_MAX)).astype(np.float32)
+
+
+def scale_of(absmax) -> np.ndarray:
+    """fp32 dequantisation scale absmax / 448 (a float32 division); 1 where
+    absmax is 0."""
+    return (_amax_used(absmax) / np.float32(E4M3_MAX)).astype(np.float32)
+
+
+def inverse_scale_of(absmax) -> np.ndarray:
+    """fp32 quantisation factor 448 / absmax (a float32 division); 1 where
+    absmax is 0."""
+    return (np.float32(E4M3_MAX) / _amax_used(absmax)).astype(np.float32)
 
 
 def quantize_weight_columns(W):
     """Expert bank W [E, K, N] -> (codes [E, N, K] uint8, scales [E, N] fp32):
     one scale per output column n, codes stored K-contiguous."""
     W32 = _f32(W)
-    s = scale_of(np.abs(W32).max(axis=1))                     # [E, N]
-    ratio = W32 / s[:, None, :]                                 # float32 division
-    return np.ascontiguousarray(e4m3_encode(ratio).transpose(0, 2, 1)), s
+    a = np.abs(W32).max(axis=1)                                 # [E, N]
+    s, u = scale_of(a), inverse_scale_of(a)
+    prod = (W32 * u[:, None, :]).astype(np.float32)             # float32 product
+    return np.ascontiguousarray(e4m3_encode(prod).transpose(0, 2, 1)), s
 
 
 def dequantize_weight_columns(codes, scales) -> np.ndarray:
@@ -106,8 +126,9 @@ def dequantize_weight_columns(codes, scales) -> np.ndarray:
 def quantize_rows(X):
     """Rows X [M, K] -> (codes [M, K] uint8, scales [M] fp32), one scale per row."""
     X32 = _f32(X)
-    s = scale_of(np.abs(X32).max(axis=1))
-    return e4m3_encode(X32 / s[:, None]), s
+    a = np.abs(X32).max(axis=1)
+    s, u = scale_of(a), inverse_scale_of(a)
+    return e4m3_encode((X32 * u[:, None]).astype(np.float32)), s
 
 
 def dequantize_rows(codes, scales) -> np.ndarray:

@@ -13,6 +13,7 @@
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <cstdint>
 
 #include "fp8_codec.cuh"
@@ -25,10 +26,11 @@ namespace {
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
-// scales[e, n] = max_k |W[e, k, n]| / 448 (1 for an all-zero column).
+// amax[e, n] = max_k |W[e, k, n]| (written into the scales array, which
+// scales_from_amax_kernel turns into the scales once the codes are out).
 // Block: 64 columns x 4 row phases.
 __global__ void __launch_bounds__(256) weight_absmax_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N,
-                                                            float *__restrict__ scales) {
+                                                            float *__restrict__ amax) {
   __shared__ float red[4][64];
   const int e = blockIdx.y;
   const int j = threadIdx.x & 63, ph = threadIdx.x >> 6;
@@ -42,17 +44,24 @@ __global__ void __launch_bounds__(256) weight_absmax_kernel(const __nv_bfloat16 
   __syncthreads();
   if (ph == 0 && n < N) {
     const float a = fmaxf(fmaxf(red[0][j], red[1][j]), fmaxf(red[2][j], red[3][j]));
-    scales[static_cast<size_t>(e) * N + n] = scale_of(a);
+    amax[static_cast<size_t>(e) * N + n] = a;
   }
 }
 
-// Wq holds e4m3(W[e, k, n] / scales[e, n]) in 128 x 128 tiles: tile (nt, kt)
+// scales[i] = amax[i] / 448 in place (1 for an all-zero column).
+__global__ void __launch_bounds__(256) scales_from_amax_kernel(float *__restrict__ scales, size_t n) {
+  for (size_t i = blockIdx.x * static_cast<size_t>(blockDim.x) + threadIdx.x; i < n;
+       i += static_cast<size_t>(gridDim.x) * blockDim.x)
+    scales[i] = scale_of(scales[i]);
+}
+
+// Wq holds e4m3(W[e, k, n] * u[e, n]) in 128 x 128 tiles, u = 448 / amax[e, n]: tile (nt, kt)
 // of expert e is the contiguous 16 KiB block ((e * Nt + nt) * Kt + kt), inside
 // it row n % 128 holds the 128 codes of k = kt*128 .. kt*128 + 127 (zero past
 // N or K).  64x64 pieces through shared memory so that both the reads (along
 // n) and the writes (along k) coalesce; the grid covers whole tiles.
 __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *__restrict__ W, int K, int N,
-                                                           const float *__restrict__ scales, uint8_t *__restrict__ Wq) {
+                                                           const float *__restrict__ amax, uint8_t *__restrict__ Wq) {
   __shared__ uint8_t tile[64][65];
   const int e = blockIdx.z;
   const int k0 = blockIdx.y * 64, n0 = blockIdx.x * 64;
@@ -60,11 +69,11 @@ __global__ void __launch_bounds__(256) weight_quant_kernel(const __nv_bfloat16 *
   const int Nt = (N + kFp8Tile - 1) / kFp8Tile, Kt = (K + kFp8Tile - 1) / kFp8Tile;
   const __nv_bfloat16 *Wb = W + static_cast<size_t>(e) * K * N;
   const int n = n0 + tx;
-  const float s = n < N ? scales[static_cast<size_t>(e) * N + n] : 1.0f;
+  const float u = n < N ? inverse_scale_of(amax[static_cast<size_t>(e) * N + n]) : 1.0f;
   for (int i = ty; i < 64; i += 4) {
     const int k = k0 + i;
     uint8_t q = 0;
-    if (k < K && n < N) q = to_e4m3(__bfloat162float(Wb[static_cast<size_t>(k) * N + n]) / s);
+    if (k < K && n < N) q = to_e4m3(__fmul_rn(__bfloat162float(Wb[static_cast<size_t>(k) * N + n]), u));
     tile[tx][i] = q;  // [n][k]
   }
   __syncthreads();
@@ -119,7 +128,7 @@ __device__ __forceinline__ float absmax8(uint4 u) {
   return m;
 }
 
-// X_perm8[r, :] = e4m3(x[perm_tok[r], :] / xs[r]) with xs[r] the row's scale;
+// X_perm8[r, :] = e4m3(x[perm_tok[r], :] * u_r) with xs[r] the row's scale;
 // pad rows are zero with scale 0.  One team per grouped row (grid-stride).
 template <bool BLOCK_TEAM>
 __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *__restrict__ x, int T, int d,
@@ -149,16 +158,17 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
     const uint4 *src = reinterpret_cast<const uint4 *>(x + static_cast<size_t>(tok) * d);
     float m = 0.f;
     for (int c = tm.rank; c < nchunk; c += tm.size) m = fmaxf(m, absmax8(__ldg(src + c)));
-    const float s = scale_of(team_max<BLOCK_TEAM>(m, red));
-    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(__ldg(src + c), s);
-    if (tm.rank == 0) xs[r] = s;
+    const float a = team_max<BLOCK_TEAM>(m, red);
+    const float u = inverse_scale_of(a);
+    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(__ldg(src + c), u);
+    if (tm.rank == 0) xs[r] = scale_of(a);
   }
   stamp_end(stamps, ST_GATHER);
 }
 
-// Hq[r, :] = e4m3(H[r, :] / hs[r]) for every real grouped row, with hs[r] =
-// max over the row's n-tiles of the tile maxima habs[r, :] written by the
-// gate/up epilogue (the maxima of the bf16 H values), / 448.  One team per
+// Hq[r, :] = e4m3(H[r, :] * u_r) for every real grouped row, with a_r the
+// largest of the row's tile maxima habs[r, :] written by the gate/up epilogue
+// (the maxima of the bf16 H values), u_r = 448 / a_r and hs[r] = a_r / 448.  One team per
 // row (grid-stride); padding rows are left alone (the down projection drops
 // their output).
 template <bool BLOCK_TEAM>
@@ -181,12 +191,13 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__res
     if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row (uniform over the team)
     float m = 0.f;
     for (int t = tm.rank; t < n_tiles; t += tm.size) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
-    const float s = scale_of(team_max<BLOCK_TEAM>(m, red));
+    const float a = team_max<BLOCK_TEAM>(m, red);
+    const float u = inverse_scale_of(a);
     const uint4 *src = reinterpret_cast<const uint4 *>(H + static_cast<size_t>(r) * f);
     uint8_t *dst = hq + static_cast<size_t>(r) * f;
 #pragma unroll 4
-    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], s);
-    if (tm.rank == 0) hs[r] = s;
+    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], u);
+    if (tm.rank == 0) hs[r] = scale_of(a);
   }
   stamp_end(stamps, ST_QUANT_H);
 }
@@ -203,6 +214,10 @@ cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void
   const dim3 g2(2 * ((N + kFp8Tile - 1) / kFp8Tile), 2 * ((K + kFp8Tile - 1) / kFp8Tile), E);
   weight_quant_kernel<<<g2, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(W), K, N, scales,
                                          static_cast<uint8_t *>(Wq));
+  err = cudaGetLastError();
+  if (err != cudaSuccess) return err;
+  const size_t n = static_cast<size_t>(E) * N;
+  scales_from_amax_kernel<<<static_cast<unsigned>(std::min<size_t>((n + 255) / 256, 4096)), 256, 0, s>>>(scales, n);
   return cudaGetLastError();
 }
 

@@ -227,3 +227,22 @@ def test_column_scales_lose_nothing_to_block_scales_on_these_weights():
     ref = x @ Wt
     rel = lambda q: np.linalg.norm(x @ q - ref) / np.linalg.norm(ref)
     assert abs(rel(col) - rel(blk)) <= 0.02 * rel(blk)
+
+
+def test_zero_and_tiny_rows():
+    """A zero row gets scale 1 and zero codes; a row whose largest magnitude
+    is below 2^-100 is scaled from 2^-100, so its inverse scale stays finite
+    and every code is a number (0 * an infinite inverse would give NaN)."""
+    x = np.zeros((3, 16), dtype=np.float32)
+    x[1, :4] = [1e-38, -3e-39, 0.0, 5e-39]          # tiny: scaled from the 2^-100 floor
+    x[2, :4] = [2.0 ** -90, 0.0, -(2.0 ** -91), 2.0 ** -92]  # above the floor
+    q, s = F8.quantize_rows(x)
+    assert s[0] == 1.0 and np.all(q[0] == 0)
+    assert s[1] == np.float32(2.0 ** -100) / np.float32(448.0)
+    assert np.all((q & 0x7F) != 0x7F)                 # no NaN code
+    assert np.all(q[1] & 0x7F == 0)                   # 1e-38 * 448 * 2^100 is below half the least e4m3 step
+    # above the floor: the largest magnitude maps to 448 and the rest follow within half a step
+    assert (q[2, 0] & 0x7F) == 0x7E
+    back = F8.dequantize_rows(q, s)
+    bound = np.maximum(np.abs(x[2].astype(np.float64)) * 2.0 ** -4, 2.0 ** -10 * float(s[2]))
+    assert np.all(np.abs(back[2] - x[2]) <= bound * (1 + 1e-12))
