@@ -158,11 +158,12 @@ struct GemmArgs {
   // the banks (use_slots; otherwise slot e)
   int use_slots;
   int wslot[kMaxE];
-  // fused combine (down GEMM without splits): y [T, n_out] bf16 gets, per
-  // token and 256-column tile, the sum over its K slot rows of O in slot
-  // order, formed by whichever slot's epilogue arrives last on tok_cnt
+  // fused combine: y [T, n_out] bf16 gets, per token and 256-column tile,
+  // the sum over its K slot rows of O in slot order, formed by whichever
+  // slot's epilogue arrives last on tok_cnt
   __nv_bfloat16 *y;
   int y_accumulate;
+  int keep_o;               // store every slot row of O (the training forward's backward reads them)
   const int32_t *pos;       // [T*K] unpadded grouped row of each (token, slot)
   const int32_t *perm_tok;  // [R] token of each padded grouped row
   int *tok_cnt;             // [T, num_n_tiles], zero at launch
@@ -340,6 +341,20 @@ __device__ __noinline__ bool wait_count(const int *p, int target, int *status) {
       return false;
     }
     __nanosleep(64);
+  }
+  return true;
+}
+
+// Bounded wait until the high 16 bits of *p (the signals of a token's slot
+// rows whose O stores are out) reach target; as wait_count otherwise.
+__device__ __noinline__ bool wait_signals(const int *p, int target, int *status) {
+  const uint64_t t0 = ptx::globaltimer_ns();
+  while ((*reinterpret_cast<const volatile int *>(p) >> 16) < target) {
+    if (ptx::globaltimer_ns() - t0 > kTimeoutNs) {
+      atomicCAS(status, 0, MOE_ERR_DEVICE_TIMEOUT);
+      return false;
+    }
+    __nanosleep(32);
   }
   return true;
 }
@@ -961,32 +976,70 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // e4m3 operands: the gate times the H row's scale; the W2 column scale below
         const float gsc = real ? args.perm_gate[row] * (FP8 ? args.row_scale[row] : 1.f) : 0.f;
         const int n0 = t.nt * BN;
+        // A chunk of 32 accumulator columns of this thread's row: TMEM load
+        // (warp-collective), the tail split's first half, the e4m3 column
+        // scales.  The row's output is this times gsc.
+        auto chunk = [&](int cc, uint32_t(&v)[32]) {
+          ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
+          ptx::tmem_wait_ld();
+          add_part(v, cc * 32);
+          const int col = n0 + cc * 32;
+          if (FP8) {
+            const float *cs2 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
+            // the chunk's 32 column scales, addresses clamped into range so
+            // that all eight loads are in flight together
+            float4 s4s[8];
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4)
+              s4s[j4] = __ldg(reinterpret_cast<const float4 *>(cs2 + min(col + 4 * j4, args.n_out - 4)));
+#pragma unroll
+            for (int j4 = 0; j4 < 8; ++j4) {
+              const float4 s4 = col + 4 * j4 < args.n_out ? s4s[j4] : make_float4(0, 0, 0, 0);
+              v[4 * j4] = __float_as_uint(__uint_as_float(v[4 * j4]) * s4.x);
+              v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) * s4.y);
+              v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) * s4.z);
+              v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) * s4.w);
+            }
+          }
+        };
+        // Fused combine of an unsplit down GEMM: every real row counts its
+        // arrival on its token's n-tile counter (low 16 bits) before storing
+        // anything, so the slot row that arrives last knows it and keeps its
+        // sums out of O (unless keep_o).  The other rows store theirs and then signal (high
+        // 16 bits).  Once all of the warp's stores and signals are out, its
+        // last rows wait (bounded) for the other slot's signal, take their own
+        // sums from TMEM again, add the other slot's row and store y.  A warp
+        // signals before it waits on anything, so no two warps wait on each
+        // other; and two fp32 addends sum the same in either order, so y is
+        // the combine kernel's bit for bit.
+        const bool fused1 = args.y != nullptr && S == 1 && n0 < args.n_out;
+        int tok = -1, other = -1;
+        bool last = false;
+        int *cnt = nullptr;
+        if (fused1 && real) {
+          tok = args.perm_tok[row];
+          if (tok < 0 || tok >= args.T) {
+            atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
+            tok = -1;
+          } else {
+            cnt = args.tok_cnt + static_cast<size_t>(tok) * NT + t.nt;
+            last = (atomicAdd(cnt, 1) & 0xffff) == args.K - 1;
+            if (last && args.K > 1) {
+              const int p0 = args.pos[tok * args.K], p1 = args.pos[tok * args.K + 1];
+              if (p0 < 0 || p0 >= args.tk || p1 < 0 || p1 >= args.tk || (p0 != ru && p1 != ru))
+                atomicCAS(args.status, 0, MOE_ERR_DEVICE_BOUNDS);
+              else
+                other = p0 == ru ? p1 : p0;
+            }
+          }
+        }
         if (n0 < args.n_out && warp_real) {
 #pragma unroll 1
           for (int cc = 0; cc < BN / 32; ++cc) {
             uint32_t v[32];
-            ptx::tmem_ld_32x32b_x32(tbase + cc * 32, v);
-            ptx::tmem_wait_ld();
-            add_part(v, cc * 32);
+            chunk(cc, v);
             const int col = n0 + cc * 32;
-            if (FP8) {
-              const float *cs2 = args.col_scale0 + static_cast<size_t>(t.e) * args.n_out;
-              // the chunk's 32 column scales, addresses clamped into range so
-              // that all eight loads are in flight together
-              float4 s4s[8];
-#pragma unroll
-              for (int j4 = 0; j4 < 8; ++j4)
-                s4s[j4] = __ldg(reinterpret_cast<const float4 *>(cs2 + min(col + 4 * j4, args.n_out - 4)));
-#pragma unroll
-              for (int j4 = 0; j4 < 8; ++j4) {
-                const float4 s4 = col + 4 * j4 < args.n_out ? s4s[j4] : make_float4(0, 0, 0, 0);
-                v[4 * j4] = __float_as_uint(__uint_as_float(v[4 * j4]) * s4.x);
-                v[4 * j4 + 1] = __float_as_uint(__uint_as_float(v[4 * j4 + 1]) * s4.y);
-                v[4 * j4 + 2] = __float_as_uint(__uint_as_float(v[4 * j4 + 2]) * s4.z);
-                v[4 * j4 + 3] = __float_as_uint(__uint_as_float(v[4 * j4 + 3]) * s4.w);
-              }
-            }
-            if (real) {
+            if (real && (!last || args.keep_o)) {
               float *dst = O + static_cast<size_t>(ru) * args.n_out + col;
 #pragma unroll
               for (int j = 0; j < 8; ++j)
@@ -997,12 +1050,65 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
           }
         }
+        if (cnt != nullptr && !last) {
+          __threadfence();  // this row's O stores precede its signal
+          atomicAdd(cnt, 0x10000);
+        }
+        if (fused1 && __ballot_sync(0xffffffffu, last) != 0) {
+          bool ok = last && (args.K == 1 || (other >= 0 && wait_signals(cnt, args.K - 1, args.status)));
+          __threadfence();  // the other slot's O row is visible once its signal is
+          const float *orow = ok && other >= 0 ? O + static_cast<size_t>(other) * args.n_out : nullptr;
+#pragma unroll 1
+          for (int cc = 0; cc < BN / 32; ++cc) {
+            uint32_t v[32];
+            chunk(cc, v);
+            const int col = n0 + cc * 32;
+            if (!ok) continue;
+            float4 o4[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j)
+              o4[j] = orow != nullptr && col + 4 * j < args.n_out
+                          ? __ldcg(reinterpret_cast<const float4 *>(orow + col + 4 * j))
+                          : make_float4(0.f, 0.f, 0.f, 0.f);
+            __nv_bfloat16 *yrow = args.y + static_cast<size_t>(tok) * args.n_out + col;
+#pragma unroll
+            for (int j8 = 0; j8 < 4; ++j8) {
+              if (col + 8 * j8 >= args.n_out) continue;  // n_out is a multiple of 8
+              float f[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) {
+                const float own = __uint_as_float(v[8 * j8 + i]) * gsc;
+                const float4 &o = o4[2 * j8 + (i >> 2)];
+                const float oth = (i & 3) == 0 ? o.x : (i & 3) == 1 ? o.y : (i & 3) == 2 ? o.z : o.w;
+                f[i] = orow != nullptr ? own + oth : own;
+              }
+              uint4 *yp = reinterpret_cast<uint4 *>(yrow + 8 * j8);
+              if (args.y_accumulate) {
+                const uint4 old = *yp;
+                const uint32_t ow[4] = {old.x, old.y, old.z, old.w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                  const float2 f2 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&ow[i]));
+                  f[2 * i] = f2.x + f[2 * i];
+                  f[2 * i + 1] = f2.y + f[2 * i + 1];
+                }
+              }
+              uint32_t yw[4];
+#pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+                yw[i] = *reinterpret_cast<const uint32_t *>(&h);
+              }
+              *yp = make_uint4(yw[0], yw[1], yw[2], yw[3]);
+            }
+          }
+        }
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) ptx::mbar_arrive_cluster(acc ? tempty_at1 : tempty_at0);
-        if (args.y != nullptr && n0 < args.n_out) {
-          // Fused combine: the writer that completes this token's 256 columns
-          // last (of its K slot rows times S splits) adds them -- per slot the
+        if (args.y != nullptr && S > 1 && n0 < args.n_out) {
+          // Fused combine of a split down GEMM: the writer that completes this
+          // token's 256 columns last (of its K slot rows times S splits) adds them -- per slot the
           // splits in order, then the slots in order: the combine kernel's
           // order, so y is the same bit for bit -- and stores y.  The warp
           // finishes its rows that arrived last together, four at a time,
@@ -1296,6 +1402,7 @@ void set_fused_combine(GemmArgs &g, const WsLayout &L, const Ptrs &P, void *y, u
   g.tok_cnt = P.tok_cnt;
   g.T = L.T;
   g.K = L.K;
+  g.keep_o = L.train ? 1 : 0;
 }
 
 }  // namespace
