@@ -15,7 +15,8 @@
 // threads per SM), in one of three forms chosen per call (all compute every
 // tile in the same order, so their results are bitwise identical):
 //
-// Pair MMA (FORM_PAIR; default once experts average 16 or more 128-row tiles):
+// Pair MMA (FORM_PAIR; default once experts average 16 or more 128-row tiles,
+//   8 with e4m3 weights):
 //   the two CTAs run one 256x256 tile together with tcgen05.mma.cta_group::2:
 //   rows 128r..128r+127 come from CTA r's A tile and CTA r holds half of the
 //   256 B columns, so each CTA stages 16 KiB of A and 16 KiB of B per
