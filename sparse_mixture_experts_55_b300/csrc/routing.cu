@@ -545,10 +545,13 @@ __global__ void route_export_kernel(int T, int E, int K, const int32_t *__restri
 }
 
 // out = x / sqrt(mean(x^2) + eps) per row; one block per row, fp32 sums.
+// The general form: any d, any alignment (element loads).
 template <typename T>
 __global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T *__restrict__ out, int d, float eps,
                                                       unsigned long long *stamps) {
   __shared__ float s_red[8];
+  pdl_wait();
+  pdl_trigger();
   stamp_begin(stamps, ST_NORM);
   const T *row = x + static_cast<size_t>(blockIdx.x) * d;
   T *orow = out + static_cast<size_t>(blockIdx.x) * d;
@@ -570,6 +573,82 @@ __global__ void __launch_bounds__(256) rmsnorm_kernel(const T *__restrict__ x, T
     if constexpr (sizeof(T) == 2) orow[j] = __float2bfloat16_rn(v);
     else orow[j] = v;
   }
+  stamp_end(stamps, ST_NORM);
+}
+
+// Sum of squares of one 16-byte chunk (8 bf16 or 4 fp32 values), in order.
+template <typename T>
+__device__ __forceinline__ float chunk_sumsq(uint4 u, float ss) {
+  if constexpr (sizeof(T) == 2) {
+    const __nv_bfloat162 *h = reinterpret_cast<const __nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      ss = fmaf(f.x, f.x, ss);
+      ss = fmaf(f.y, f.y, ss);
+    }
+  } else {
+    const float f[4] = {__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z), __uint_as_float(u.w)};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ss = fmaf(f[i], f[i], ss);
+  }
+  return ss;
+}
+
+template <typename T>
+__device__ __forceinline__ uint4 chunk_scale(uint4 u, float inv) {
+  if constexpr (sizeof(T) == 2) {
+    __nv_bfloat162 *h = reinterpret_cast<__nv_bfloat162 *>(&u);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      h[i] = __floats2bfloat162_rn(f.x * inv, f.y * inv);
+    }
+    return u;
+  } else {
+    return make_uint4(__float_as_uint(__uint_as_float(u.x) * inv), __float_as_uint(__uint_as_float(u.y) * inv),
+                      __float_as_uint(__uint_as_float(u.z) * inv), __float_as_uint(__uint_as_float(u.w) * inv));
+  }
+}
+
+// The same for rows of whole 16-byte chunks at 16-byte aligned addresses:
+// 16-byte loads and stores, and each thread keeps its first kNormRegChunks
+// chunks in registers between the sum and the scaling, so a row of up to
+// 256 * kNormRegChunks chunks (8192 bf16 values) is read from memory once.
+constexpr int kNormRegChunks = 4;
+template <typename T>
+__global__ void __launch_bounds__(256) rmsnorm_vec_kernel(const uint4 *__restrict__ x, uint4 *__restrict__ out,
+                                                          int nch, int d, float eps, unsigned long long *stamps) {
+  __shared__ float s_red[8];
+  pdl_wait();
+  pdl_trigger();
+  stamp_begin(stamps, ST_NORM);
+  const uint4 *row = x + static_cast<size_t>(blockIdx.x) * nch;
+  uint4 *orow = out + static_cast<size_t>(blockIdx.x) * nch;
+  uint4 v[kNormRegChunks];
+#pragma unroll
+  for (int i = 0; i < kNormRegChunks; ++i) {
+    const int c = threadIdx.x + i * 256;
+    v[i] = c < nch ? row[c] : make_uint4(0u, 0u, 0u, 0u);
+  }
+  float ss = 0.f;
+#pragma unroll
+  for (int i = 0; i < kNormRegChunks; ++i) ss = chunk_sumsq<T>(v[i], ss);
+  for (int c = threadIdx.x + kNormRegChunks * 256; c < nch; c += 256) ss = chunk_sumsq<T>(row[c], ss);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, off);
+  if ((threadIdx.x & 31) == 0) s_red[threadIdx.x >> 5] = ss;
+  __syncthreads();
+  float tot = 0.f;
+  for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) tot += s_red[w];
+  const float inv = 1.0f / sqrtf(tot / static_cast<float>(d) + eps);
+  // each thread writes back only the chunks it read, so out may equal x
+#pragma unroll
+  for (int i = 0; i < kNormRegChunks; ++i) {
+    const int c = threadIdx.x + i * 256;
+    if (c < nch) orow[c] = chunk_scale<T>(v[i], inv);
+  }
+  for (int c = threadIdx.x + kNormRegChunks * 256; c < nch; c += 256) orow[c] = chunk_scale<T>(row[c], inv);
   stamp_end(stamps, ST_NORM);
 }
 
@@ -693,12 +772,23 @@ cudaError_t launch_route_export(int T, int E, int K, const Ptrs &P, int32_t *idx
 cudaError_t launch_rmsnorm(const void *x, void *out, int T, int d, float eps, int dtype, cudaStream_t s,
                            unsigned long long *stamps) {
   if (T == 0) return cudaSuccess;
+  // Launched with programmatic dependent launch: each block waits for the
+  // previous kernel in the stream before it reads x.
+  const size_t eb = dtype == MOE_BF16 ? 2 : 4;
+  const bool vec = (d * eb) % 16 == 0 && (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
+  const int nch = static_cast<int>(d * eb / 16);
+  if (vec && dtype == MOE_BF16)
+    return launch_kernel(rmsnorm_vec_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, s, true,
+                         static_cast<const uint4 *>(x), static_cast<uint4 *>(out), nch, d, eps, stamps);
+  if (vec)
+    return launch_kernel(rmsnorm_vec_kernel<float>, dim3(T), dim3(256), 0, s, true, static_cast<const uint4 *>(x),
+                         static_cast<uint4 *>(out), nch, d, eps, stamps);
   if (dtype == MOE_BF16)
-    rmsnorm_kernel<__nv_bfloat16><<<T, 256, 0, s>>>(static_cast<const __nv_bfloat16 *>(x),
-                                                     static_cast<__nv_bfloat16 *>(out), d, eps, stamps);
-  else
-    rmsnorm_kernel<float><<<T, 256, 0, s>>>(static_cast<const float *>(x), static_cast<float *>(out), d, eps, stamps);
-  return cudaGetLastError();
+    return launch_kernel(rmsnorm_kernel<__nv_bfloat16>, dim3(T), dim3(256), 0, s, true,
+                         static_cast<const __nv_bfloat16 *>(x), static_cast<__nv_bfloat16 *>(out), d, eps, stamps);
+  return launch_kernel(rmsnorm_kernel<float>, dim3(T), dim3(256), 0, s, true, static_cast<const float *>(x),
+                       static_cast<float *>(out), d, eps, stamps);
 }
 
 }  // namespace moe

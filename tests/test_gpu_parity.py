@@ -163,10 +163,14 @@ def test_exact_ties_pick_lower_index(moe):
     assert shares[0] > 0.3 and shares[7] < 0.08
 
 
-def test_rmsnorm(moe):
+# rows of whole 16-byte chunks take the vector kernel (d = 4096; d = 10000
+# bf16 also runs its reload loop past the register-held chunks; d = 8 is one
+# chunk); d = 100 bf16 and d = 6 fp32 are not whole chunks: the general kernel
+@pytest.mark.parametrize("T,d", [(33, 4096), (7, 10000), (3, 8), (5, 100), (4, 6)])
+def test_rmsnorm(moe, T, d):
     dev = torch.device("cuda:0")
     for dt, tol in ((torch.bfloat16, 2 ** -7), (torch.float32, 1e-6)):
-        h = W.randn((33, 4096), 3.0, 77, "cpu", dt)
+        h = W.randn((T, d), 3.0, 77, "cpu", dt)
         out = moe.moe_rmsnorm(h.to(dev))
         ref = oracle.rmsnorm(h)
         assert np.abs(_np(out.float()) - ref).max() <= tol * np.abs(ref).max()
