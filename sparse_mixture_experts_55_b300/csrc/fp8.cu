@@ -169,8 +169,10 @@ __global__ void __launch_bounds__(256) gather_quant_kernel(const __nv_bfloat16 *
 // Hq[r, :] = e4m3(H[r, :] * u_r) for every real grouped row, with a_r the
 // largest of the row's tile maxima habs[r, :] written by the gate/up epilogue
 // (the maxima of the bf16 H values), u_r = 448 / a_r and hs[r] = a_r / 448.  One team per
-// row (grid-stride); padding rows are left alone (the down projection drops
-// their output).
+// real row (grid-stride over the T*K real rows, each mapped to its padded
+// position; padding rows are left alone, the down projection drops their
+// output).  With few rows a row's chunks are split over gridDim.y blocks,
+// each taking the row's scale from the tile maxima itself.
 template <bool BLOCK_TEAM>
 __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__restrict__ H, int f,
                                                       const float *__restrict__ habs, int n_tiles,
@@ -183,21 +185,23 @@ __global__ void __launch_bounds__(256) quant_h_kernel(const __nv_bfloat16 *__res
   pdl_trigger();
   stamp_begin(stamps, ST_QUANT_H);
   const Team<BLOCK_TEAM> tm;
-  const int rows = poffsets[E];
+  const int real_rows = offsets[E];
   const int nchunk = f / 8;
-  for (int r = tm.first; r < rows; r += tm.stride) {
+  const int per = (nchunk + gridDim.y - 1) / gridDim.y;
+  const int c0 = blockIdx.y * per, c1 = min(nchunk, c0 + per);
+  for (int u = tm.first; u < real_rows; u += tm.stride) {
     int e = 0;
-    while (e < E - 1 && r >= poffsets[e + 1]) ++e;
-    if (r - poffsets[e] >= offsets[e + 1] - offsets[e]) continue;  // padding row (uniform over the team)
+    while (e < E - 1 && u >= offsets[e + 1]) ++e;
+    const int r = poffsets[e] + (u - offsets[e]);  // padded grouped row
     float m = 0.f;
     for (int t = tm.rank; t < n_tiles; t += tm.size) m = fmaxf(m, habs[static_cast<size_t>(r) * n_tiles + t]);
     const float a = team_max<BLOCK_TEAM>(m, red);
-    const float u = inverse_scale_of(a);
+    const float inv = inverse_scale_of(a);
     const uint4 *src = reinterpret_cast<const uint4 *>(H + static_cast<size_t>(r) * f);
     uint8_t *dst = hq + static_cast<size_t>(r) * f;
 #pragma unroll 4
-    for (int c = tm.rank; c < nchunk; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], u);
-    if (tm.rank == 0) hs[r] = scale_of(a);
+    for (int c = c0 + tm.rank; c < c1; c += tm.size) *reinterpret_cast<uint2 *>(dst + 8 * c) = quant8(src[c], inv);
+    if (tm.rank == 0 && blockIdx.y == 0) hs[r] = scale_of(a);
   }
   stamp_end(stamps, ST_QUANT_H);
 }
@@ -237,12 +241,15 @@ cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const
                        P.status, P.stamps);
 }
 
-cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
-  const bool block_team = R <= num_sms * 32;  // as launch_gather_quant
-  int blocks = block_team ? R : (R + 7) / 8;
+cudaError_t launch_quant_h(int f, int E, int TK, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s) {
+  const bool block_team = TK <= num_sms * 32;  // as launch_gather_quant
+  int blocks = block_team ? TK : (TK + 7) / 8;
   if (blocks > num_sms * 8) blocks = num_sms * 8;
   if (blocks < 1) blocks = 1;
-  return launch_kernel(block_team ? quant_h_kernel<true> : quant_h_kernel<false>, dim3(blocks), dim3(256), 0, s, true,
+  // few rows: split each row over up to 16 blocks, about two blocks per SM in all
+  const int parts = block_team ? std::max(1, std::min(16, (2 * num_sms + blocks - 1) / blocks)) : 1;
+  return launch_kernel(block_team ? quant_h_kernel<true> : quant_h_kernel<false>, dim3(blocks, parts), dim3(256), 0,
+                       s, true,
                        static_cast<const __nv_bfloat16 *>(P.hbuf), f, static_cast<const float *>(P.habs), n_tiles,
                        static_cast<const int32_t *>(P.offsets), static_cast<const int32_t *>(P.poffsets), E,
                        static_cast<uint8_t *>(P.hq), P.hscale, P.stamps);

@@ -1515,7 +1515,7 @@ cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void
   set_tail_split(g1, L, P, form, L.S_gu, 0);
   err = launch_form<MODE_GATE_UP, true>(form, grids, s, true, tm_x, tm_xh, tm_xq, tm_w1, tm_w3, g1);
   // H rows to e4m3 with their own scales
-  if (err == cudaSuccess) err = launch_quant_h(f, E, L.R, g1.num_n_tiles, P, num_sms, s);
+  if (err == cudaSuccess) err = launch_quant_h(f, E, L.T * L.K, g1.num_n_tiles, P, num_sms, s);
   if (err != cudaSuccess) return err;
 
   GemmArgs g2 = g1;

@@ -178,7 +178,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
 cudaError_t launch_quantize_weights_fp8(const void *W, int E, int K, int N, void *Wq, float *scales, cudaStream_t s);
 cudaError_t launch_gather_quant(const void *x, int T, int d, int E, int R, const Ptrs &P, int num_sms,
                                 cudaStream_t s);
-cudaError_t launch_quant_h(int f, int E, int R, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s);
+cudaError_t launch_quant_h(int f, int E, int TK, int n_tiles, const Ptrs &P, int num_sms, cudaStream_t s);
 // gemm_tc.cu, e4m3 operands: gate/up GEMM, H quantisation, down GEMM
 cudaError_t launch_expert_gemms_fp8(const void *W1q, const float *s1, const void *W3q, const float *s3,
                                     const void *W2q, const float *s2, int d, int f, int E, const WsLayout &L,
