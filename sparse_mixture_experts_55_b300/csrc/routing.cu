@@ -194,10 +194,12 @@ __device__ __forceinline__ void select_and_store(const float (&l)[EP], int t, in
 
 // One block routes tpb consecutive tokens.  Thread i owns the i-th 16-byte slice
 // of d (8 bf16 or 4 fp32 columns).  With up to 8 experts it keeps its rows of
-// W_g in registers for all the block's tokens; the x slices of the next group
-// of tokens are loaded while the current group is reduced.  Per token, each
-// warp reduce-scatters its partial logits and the warp sums are added in a
-// fixed order, so the logits are deterministic.
+// W_g in registers for all the block's tokens.  The tokens go by in chunks of
+// CH: every warp runs through a chunk's tokens with the x slices of the next
+// kRouteGroup tokens in flight, reduce-scatters each token's partial logits
+// and parks its warp sums in shared memory; one barrier per chunk, then the
+// warp sums of each logit are added in a fixed order (so the logits are
+// deterministic) and the chunk's tokens are selected.
 template <typename Tin, int EP>
 __device__ __forceinline__ void route_body(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d,
                                            int E, int K, int tpb, unsigned flags, int32_t *__restrict__ idx,
@@ -205,10 +207,11 @@ __device__ __forceinline__ void route_body(const Tin *__restrict__ x, const Tin 
                                            unsigned long long *stamps) {
   constexpr int NV = Vec<Tin>::N;
   constexpr int NW = kRouteThreads / 32;
-  constexpr int G = kRouteGroup;  // tokens per reduction group
+  constexpr int G = kRouteGroup;       // x slices in flight per thread
+  constexpr int CH = EP <= 8 ? 32 : 8;  // tokens per chunk (partials in shared memory)
   constexpr bool kCached = EP == 8;
-  __shared__ float s_red[G][NW][EP];
-  __shared__ float s_log[G][EP];
+  __shared__ float s_red[CH][NW][EP];
+  __shared__ float s_log[CH][EP];
   __shared__ int s_cnt[kMaxE];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * tpb;
@@ -227,30 +230,36 @@ __device__ __forceinline__ void route_body(const Tin *__restrict__ x, const Tin 
 #pragma unroll
   for (int i = 0; i < G; ++i) xr[i] = load_raw(xb + static_cast<size_t>(i) * d, own && i < nt);
 
-  for (int g0 = 0; g0 < nt; g0 += G) {
+  for (int c0 = 0; c0 < nt; c0 += CH) {
+    const int nc = min(CH, nt - c0);  // uniform over the block
+    for (int i0 = 0; i0 < nc; i0 += G) {
 #pragma unroll
-    for (int i = 0; i < G; ++i) {
-      float a[EP];
+      for (int j = 0; j < G; ++j) {
+        const int i = i0 + j;  // token c0 + i of the block
+        if (i < nc) {
+          float a[EP];
 #pragma unroll
-      for (int e = 0; e < EP; ++e) a[e] = 0.f;
-      if constexpr (kCached) {
-        dot_chunk<Tin, EP>(xr[i], w, a);
-      } else {
-        if (own) dot_chunk_streamed<Tin, EP>(xr[i], Wg, tid * NV, E, a);
+          for (int e = 0; e < EP; ++e) a[e] = 0.f;
+          if constexpr (kCached) {
+            dot_chunk<Tin, EP>(xr[j], w, a);
+          } else {
+            if (own) dot_chunk_streamed<Tin, EP>(xr[j], Wg, tid * NV, E, a);
+          }
+          // d wider than one slice per thread: further slices with W_g rows from L1
+          for (int c = tid + kRouteThreads; c < nchunks; c += kRouteThreads)
+            dot_chunk_streamed<Tin, EP>(load_raw(x + static_cast<size_t>(t0 + c0 + i) * d + c * NV, true), Wg,
+                                        c * NV, E, a);
+          int e;
+          const float v = warp_reduce_scatter<EP>(a, lane, e);
+          if ((lane & (32 / EP - 1)) == 0) s_red[i][warp][e] = v;
+        }
+        // the slice kRouteGroup tokens ahead (across chunk ends)
+        const int nxt = c0 + i + G;
+        xr[j] = load_raw(xb + static_cast<size_t>(nxt) * d, own && nxt < nt);
       }
-      // d wider than one slice per thread: further slices with W_g rows from L1
-      for (int c = tid + kRouteThreads; c < nchunks && g0 + i < nt; c += kRouteThreads)
-        dot_chunk_streamed<Tin, EP>(load_raw(x + static_cast<size_t>(t0 + g0 + i) * d + c * NV, true), Wg, c * NV, E,
-                                    a);
-      int e;
-      const float v = warp_reduce_scatter<EP>(a, lane, e);
-      if ((lane & (32 / EP - 1)) == 0) s_red[i][warp][e] = v;
     }
-    // the next group's x slices load while this group is reduced
-#pragma unroll
-    for (int i = 0; i < G; ++i) xr[i] = load_raw(xb + static_cast<size_t>(g0 + G + i) * d, own && g0 + G + i < nt);
     __syncthreads();
-    if (tid < G * EP) {
+    if (tid < nc * EP) {
       const int i = tid / EP, e = tid % EP;
       float sum = 0.f;
 #pragma unroll
@@ -258,7 +267,7 @@ __device__ __forceinline__ void route_body(const Tin *__restrict__ x, const Tin 
       s_log[i][e] = sum;
     }
     __syncthreads();
-    if (tid < G && g0 + tid < nt) select_and_store<EP>(s_log[tid], t0 + g0 + tid, E, K, flags, idx, gate, s_cnt, status);
+    if (tid < nc) select_and_store<EP>(s_log[tid], t0 + c0 + tid, E, K, flags, idx, gate, s_cnt, status);
   }
   __syncthreads();
   if (tid < E) blockcounts[blockIdx.x * E + tid] = s_cnt[tid];
