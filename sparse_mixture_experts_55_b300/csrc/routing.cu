@@ -364,6 +364,62 @@ __device__ __forceinline__ void group_body(int b, int nb, int T, int E, int K, i
   }
 }
 
+// Grouping of at most 32 (token, slot) entries (T * K <= 32) by the block
+// that has just routed them: one warp ranks the entries with
+// __match_any_sync in flat t*K + k order within each expert -- the order of
+// group_body, so the permutation is the same -- reading idx and gate back
+// from this block's own stores; then the block marks the padding rows.
+__device__ __forceinline__ void group_tiny(int T, int E, int K, const int32_t *idx, const float *gate,
+                                           int32_t *offsets, int32_t *poffsets, int32_t *pos, int32_t *perm_tok,
+                                           float *perm_gate, int *status) {
+  __shared__ int s_cnt[kMaxE], s_off[kMaxE + 1], s_poff[kMaxE + 1];
+  const int tid = threadIdx.x, lane = tid & 31;
+  const int n = T * K;
+  for (int i = tid; i < E; i += blockDim.x) s_cnt[i] = 0;
+  __syncthreads();
+  if (tid < 32) {
+    bool active = lane < n;
+    int e = active ? idx[lane] : -1;
+    if (active && (e < 0 || e >= E)) {
+      set_status(status, MOE_ERR_DEVICE_BOUNDS);
+      active = false;
+      e = -1;
+    }
+    const unsigned peers = __match_any_sync(0xffffffffu, e);
+    const int rank = __popc(peers & ((1u << lane) - 1u));
+    if (active && rank == 0) s_cnt[e] = __popc(peers);
+    __syncwarp();
+    if (lane == 0) {
+      int off = 0, poff = 0;
+      for (int ee = 0; ee < E; ++ee) {
+        s_off[ee] = off;
+        s_poff[ee] = poff;
+        off += s_cnt[ee];
+        poff += (s_cnt[ee] + kSegPad - 1) / kSegPad * kSegPad;
+      }
+      s_off[E] = off;
+      s_poff[E] = poff;
+    }
+    __syncwarp();
+    for (int i = lane; i <= E; i += 32) {
+      offsets[i] = s_off[i];
+      poffsets[i] = s_poff[i];
+    }
+    if (active) {
+      const int rp = s_poff[e] + rank;
+      perm_tok[rp] = lane / K;
+      perm_gate[rp] = gate[lane];
+      pos[lane] = s_off[e] + rank;  // unpadded grouped row
+    }
+  }
+  __syncthreads();
+  for (int ee = 0; ee < E; ++ee)
+    for (int r = s_poff[ee] + s_cnt[ee] + tid; r < s_poff[ee + 1]; r += blockDim.x) {
+      perm_tok[r] = -1;
+      perm_gate[r] = 0.f;
+    }
+}
+
 __global__ void __launch_bounds__(kGroupTokens *kMaxK)
     group_kernel(int T, int E, int K, int nb_route, int tpb, unsigned flags, const int32_t *__restrict__ idx,
                  const float *__restrict__ gate, const int32_t *__restrict__ blockcounts, int32_t *offsets,
@@ -410,7 +466,7 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
 // previous work in the stream to finish, then clears the call's status words
 // and split / slot counters (n_zero ints from `status`, which that work may
 // have been using), then routes every token as route_kernel does (same
-// arithmetic) and groups them.
+// arithmetic) and groups them in one warp (group_tiny).
 template <typename Tin, int EP>
 __global__ void __launch_bounds__(kRouteThreads, 1)
     route_single_kernel(const Tin *__restrict__ x, const Tin *__restrict__ Wg, int T, int d, int E, int K, int tpb,
@@ -424,7 +480,8 @@ __global__ void __launch_bounds__(kRouteThreads, 1)
   __syncthreads();
   __threadfence_block();
   stamp_begin(stamps, ST_GROUP);
-  group_body(0, 1, T, E, K, 1, tpb, idx, gate, blockcounts, offsets, poffsets, pos, perm_tok, perm_gate, status);
+  static_assert(kSingleRouteT * kMaxK <= 32, "group_tiny ranks all entries in one warp");
+  group_tiny(T, E, K, idx, gate, offsets, poffsets, pos, perm_tok, perm_gate, status);
   stamp_end(stamps, ST_GROUP);
 }
 
