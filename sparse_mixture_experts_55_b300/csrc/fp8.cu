@@ -5,10 +5,11 @@
 //
 // Scheme (the pages name FP8 only as deployment work -- paper-graph-ui
 // summary, "Inference and Deployment Infrastructure" -- so it is this
-// library's): scale = max |v| / 448 over the column (weights) or row
-// (activations), 1 where that maximum is 0; code = e4m3(v / scale) rounded to
-// nearest, ties to even, saturating at 448; the division is an fp32 IEEE
-// division.
+// library's): from a = max |v| over the column (weights) or row
+// (activations), the dequantisation scale a / 448 and the quantisation factor
+// u = 448 / a (both 1 where a is 0, a nonzero a below 2^-100 taken as
+// 2^-100); code = e4m3(v * u) rounded to nearest, ties to even, saturating at
+// 448 (fp8_codec.cuh).
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 #include <cuda_runtime.h>

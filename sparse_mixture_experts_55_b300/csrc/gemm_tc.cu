@@ -294,11 +294,6 @@ __device__ __forceinline__ Tile decode_unit(int u, const Ctrl &c, int NT, int S,
   return t;
 }
 
-// SiLU(g) = g / (1 + e^-g) with CUDA's fast exponential and fast division
-// intrinsics (a few ulp of fp32; the result is rounded to bf16 next).  An
-// IEEE division's longer dependent chain made this the epilogue's cost at
-// decode sizes, where one warp holds a tile's real rows.  For g below about
-// -88, e^-g is infinite and the quotient is 0, SiLU's limit.
 // Work item `it` of the persistent schedule: a whole unit, or (the tail
 // split) one k-half of one of the last wave's units.  Items before tail_base
 // are units; item tail_base + j is half (j & 1) of unit tail_base + (j >> 1),
@@ -360,6 +355,11 @@ __device__ __noinline__ bool wait_signals(const int *p, int target, int *status)
   return true;
 }
 
+// SiLU(g) = g / (1 + e^-g) with CUDA's fast exponential and fast division
+// intrinsics (a few ulp of fp32; the result is rounded to bf16 next).  An
+// IEEE division's longer dependent chain made this the epilogue's cost at
+// decode sizes, where one warp holds a tile's real rows.  For g below about
+// -88, e^-g is infinite and the quotient is 0, SiLU's limit.
 __device__ __forceinline__ float silu_f(float g) { return __fdividef(g, 1.0f + __expf(-g)); }
 
 template <int MODE, int FORM, bool FP8>
