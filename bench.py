@@ -874,20 +874,45 @@ def run_ours_train(args):
 
     # end to end with host buffers: x and dy copied in from pinned memory,
     # dx copied out, every step (the weight gradients stay on the device for
-    # the optimiser)
+    # the optimiser).  As moe.HostPipeline does for the forward: two device
+    # buffer sets, the next step's copies in and the previous step's dx out on
+    # their own streams, ordered by events against the steps, which run in
+    # order on the compute stream (the workspace holds one step's activations).
     x_h, dy_h = inp.x.cpu().pin_memory(), dy.cpu().pin_memory()
-    dx_h = torch.empty(T, d, dtype=torch.float32).pin_memory()
-    xd, dyd = torch.empty_like(inp.x), torch.empty_like(dy)
+    dx_h = [torch.empty(T, d, dtype=torch.float32).pin_memory() for _ in range(2)]
+    xs = [torch.empty_like(inp.x) for _ in range(2)]
+    dys = [torch.empty_like(dy) for _ in range(2)]
+    gbuf = [grads, moe.LayerGrads(torch.empty(T, d, **z), grads.dWg, grads.dW1, grads.dW3, grads.dW2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    in_done, run_done, out_done = ([torch.cuda.Event() for _ in range(2)] for _ in range(3))
+
+    def submit(n):
+        b = n & 1
+        if n >= 2:
+            s_in.wait_event(run_done[b])      # xs[b], dys[b] were read by the step two batches ago
+        with torch.cuda.stream(s_in):
+            xs[b].copy_(x_h, non_blocking=True)
+            dys[b].copy_(dy_h, non_blocking=True)
+            in_done[b].record(s_in)
+        stream.wait_event(in_done[b])
+        if n >= 2:
+            stream.wait_event(out_done[b])    # dx[b] was copied out two batches ago
+        step(xs[b], gbuf[b], dys[b])
+        run_done[b].record(stream)
+        s_out.wait_event(run_done[b])
+        with torch.cuda.stream(s_out):
+            dx_h[b].copy_(gbuf[b].dx, non_blocking=True)
+            out_done[b].record(s_out)
+
     e2e_steps = max(3, min(steps, 20))
-    for i in range(e2e_steps + 2):
-        if i == 2:
-            torch.cuda.synchronize(dev)
-            t0 = time.perf_counter()
-        xd.copy_(x_h, non_blocking=True)
-        dyd.copy_(dy_h, non_blocking=True)
-        step(xd, grads, dyd)
-        dx_h.copy_(grads.dx, non_blocking=True)
-        torch.cuda.synchronize(dev)
+    for n in range(2):
+        submit(n)
+    torch.cuda.synchronize(dev)
+    t0 = time.perf_counter()
+    for n in range(2, 2 + e2e_steps):
+        submit(n)
+    for sx in (s_in, stream, s_out):
+        sx.synchronize()
     e2e_ms = 1e3 * (time.perf_counter() - t0) / e2e_steps
 
     peaks, peak_src = load_peaks()
@@ -920,7 +945,7 @@ def run_ours_train(args):
         "roofline": roof,
         "e2e": {"value": T / (e2e_ms / 1e3), "unit": "tokens/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": x_h.numel() * x_h.element_size() + dy_h.numel() * dy_h.element_size(),
-                "d2h_bytes_per_step": dx_h.numel() * dx_h.element_size()},
+                "d2h_bytes_per_step": dx_h[0].numel() * dx_h[0].element_size()},
         "gpu_launches": (moe._lib.load().moe_forward_launches(T, d, f, E, K, moe.MOE_BF16) + 8) * steps,
         "stage_timing": "shares from a separate pass of the same steps with library-recorded backward stage "
                         "events, scaled to the headline step",
