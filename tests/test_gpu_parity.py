@@ -92,6 +92,8 @@ def _bf16_inputs(T, d, f, E, K, seed):
     (33, 256, 256, 5, 2),       # 5 experts (scalar router path)
     (1, 512, 1024, 8, 2),       # decode: one token, split-K down projection
     (8, 512, 1024, 8, 2),
+    (8, 256, 384, 32, 2),       # one-block routing: 16 entries over 32 experts, most segments empty
+    (5, 256, 256, 5, 1),        # one-block routing, scalar router path, top-1
     (128, 512, 1024, 8, 2),
     (3000, 256, 256, 8, 2),     # 6 m-tiles per expert, many tiles per CTA
     # decode-like shapes whose gate/up contraction is split (fp32 partials,
