@@ -43,9 +43,9 @@
 //   loading half of both.
 // Roles per CTA:
 //   warp 0      TMA producer (one elected thread), shared-memory ring
-//               (A 128x64 K-major; bf16 B in 64x64 N-major boxes since the
-//               weights are stored [E, K, N], e4m3 B K-major; 128-byte
-//               swizzle); weight banks are addressed by slot (wslot[e]) so
+//               (A 128x64 K-major; bf16 B in 64x64 N-major blocks since the
+//               weights are stored [E, K, N], two blocks per copy when N is a
+//               multiple of 128; e4m3 B K-major; 128-byte swizzle); weight banks are addressed by slot (wslot[e]) so
 //               that an expert cache can hold them in any order;
 //   warp 1      TMEM allocator + MMA issuer (one thread) into one of two
 //               256-column accumulators;
@@ -165,6 +165,7 @@ struct GemmArgs {
   __nv_bfloat16 *y;
   int y_accumulate;
   int keep_o;               // store every slot row of O (the training forward's backward reads them)
+  int b4d;                  // bf16 weights through the 4-D map: one copy per 128 columns
   const int32_t *pos;       // [T*K] unpadded grouped row of each (token, slot)
   const int32_t *perm_tok;  // [R] token of each padded grouped row
   int *tok_cnt;             // [T, num_n_tiles], zero at launch
@@ -492,6 +493,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       if (FP8) {
         // e4m3 banks are stored in 128 x 128 tiles: one contiguous 16 KiB box
         ptx::tma_load_2d_pair(b_dst, mb, bar, 0, fp8_tile_row(wz, nb, k0), pol_b);
+      } else if (args.b4d) {
+        ptx::tma_load_4d_pair(b_dst, mb, bar, 0, k0, nb / 64, wz, pol_b);
       } else {
         ptx::tma_load_3d_pair(b_dst, mb, bar, nb, k0, wz, pol_b);
         ptx::tma_load_3d_pair(b_dst + B_CHUNK, mb, bar, nb + 64, k0, wz, pol_b);
@@ -509,6 +512,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int row = fp8_tile_row(wz, nb, k0);
         if (mask) ptx::tma_load_2d_mc(dst, mb, bar, 0, row, mask, pol_b);
         else ptx::tma_load_2d(dst, mb, bar, 0, row, pol_b);
+      } else if (args.b4d) {
+        if (mask) ptx::tma_load_4d_mc(dst, mb, bar, 0, k0, nb / 64, wz, mask, pol_b);
+        else ptx::tma_load_4d(dst, mb, bar, 0, k0, nb / 64, wz, pol_b);
       } else {
         if (mask) {
           ptx::tma_load_3d_mc(dst, mb, bar, nb, k0, wz, mask, pol_b);
@@ -1417,11 +1423,16 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   const int form = pick_form(L, grids);
   const int banks = slot_of ? n_slots : E;  // matrices held by each weight bank
   CUtensorMap tm_x, tm_xh, tm_xq, tm_w1, tm_w3, tm_h, tm_hh, tm_hq, tm_w2;
+  // weights whose column count is a multiple of 128 go through the 4-D view:
+  // one copy per 128-column half tile instead of two (2.3% per prefill layer)
+  const bool w13_4d = f % 128 == 0, w2_4d = d % 128 == 0;
   if (!tmap_2d(&tm_x, P.xperm, d, L.R, BM) || !tmap_2d(&tm_xh, P.xperm, d, L.R, BM / 2) ||
-      !tmap_2d(&tm_xq, P.xperm, d, L.R, BM / 4) || !tmap_3d(&tm_w1, W1, f, d, banks) ||
-      !tmap_3d(&tm_w3, W3, f, d, banks) || !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) ||
+      !tmap_2d(&tm_xq, P.xperm, d, L.R, BM / 4) ||
+      !(w13_4d ? tmap_4d_w(&tm_w1, W1, f, d, banks) : tmap_3d(&tm_w1, W1, f, d, banks)) ||
+      !(w13_4d ? tmap_4d_w(&tm_w3, W3, f, d, banks) : tmap_3d(&tm_w3, W3, f, d, banks)) ||
+      !tmap_2d(&tm_h, P.hbuf, f, L.R, BM) ||
       !tmap_2d(&tm_hh, P.hbuf, f, L.R, BM / 2) || !tmap_2d(&tm_hq, P.hbuf, f, L.R, BM / 4) ||
-      !tmap_3d(&tm_w2, W2, d, f, banks))
+      !(w2_4d ? tmap_4d_w(&tm_w2, W2, d, f, banks) : tmap_3d(&tm_w2, W2, d, f, banks)))
     return cudaErrorInvalidValue;
 
   GemmArgs g1{};
@@ -1438,6 +1449,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g1.n_out = f;
   g1.num_n_tiles = (f + BN / 2 - 1) / (BN / 2);
   g1.num_kb = (d + BK - 1) / BK;
+  g1.b4d = w13_4d ? 1 : 0;
   g1.splits = L.S_gu;
   g1.kb_per_split = L.kb_per_split_gu;
   g1.force_timeout = (flags & MOE_DEBUG_FORCE_TIMEOUT) ? 1 : 0;
@@ -1461,6 +1473,7 @@ cudaError_t launch_expert_gemms_bf16(const void *W1, const void *W3, const void 
   g2.n_out = d;
   g2.num_n_tiles = (d + BN - 1) / BN;
   g2.num_kb = (f + BK - 1) / BK;
+  g2.b4d = w2_4d ? 1 : 0;
   g2.splits = L.S;
   g2.kb_per_split = L.kb_per_split;
   set_tail_split(g2, L, P, form, L.S, 1);

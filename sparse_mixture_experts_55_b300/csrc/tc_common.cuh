@@ -43,5 +43,8 @@ __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, C &c, 
 bool tmap_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
 bool tmap_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E, uint32_t box_rows = 64);
 bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
+// bf16 bank [E, rows, cols] with cols a multiple of 128, viewed as [E, cols/64, rows, 64]:
+// one box is 64 x 64 x 2 blocks, i.e. 128 columns x 64 rows in two 8 KiB swizzled blocks.
+bool tmap_4d_w(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E);
 
 }  // namespace moe

@@ -53,6 +53,22 @@ bool tmap_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The same bank viewed as [E, cols/64, rows, 64] (strides: a row, 64 columns,
+// a matrix), for cols a multiple of 128: one box of 64 columns x 64 rows x 2
+// column blocks fills the two 8 KiB swizzled blocks that a 128-column half
+// of a weight tile occupies in shared memory, in one copy instead of two.
+bool tmap_4d_w(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E) {
+  auto fn = encode_fn();
+  if (!fn || cols % 128 != 0) return false;
+  cuuint64_t dims[4] = {64, rows, cols / 64, E};
+  cuuint64_t strides[3] = {cols * 2, 128, cols * rows * 2};
+  cuuint32_t box[4] = {64, 64, 2, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D e4m3 matrix [rows, cols] (cols contiguous), box = 128 columns (128
 // bytes) x box_rows rows, 128-byte swizzle.
 bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
