@@ -329,10 +329,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           } else {
             const int krow = t.krow0 + kb * BK;
             const int m0 = t.mt * BM, n0 = t.nt * BN;
-            ptx::tma_load_2d(a_dst, &tmA, bar, m0, krow, pol);
-            ptx::tma_load_2d(a_dst + BOX_BYTES, &tmA, bar, m0 + 64, krow, pol);
-#pragma unroll
-            for (int j = 0; j < 4; ++j) ptx::tma_load_2d(b_dst + j * BOX_BYTES, &tmB0, bar, n0 + 64 * j, krow, pol);
+            // column-block views: the two 64-column blocks of A and the four
+            // of B each in one copy
+            ptx::tma_load_3d(a_dst, &tmA, bar, 0, krow, m0 / 64, pol);
+            ptx::tma_load_3d(b_dst, &tmB0, bar, 0, krow, n0 / 64, pol);
           }
           issued |= 1u << p_stage;
           last_par = (last_par & ~(1u << p_stage)) | (p_phase << p_stage);
@@ -556,9 +556,9 @@ cudaError_t launch_bwd_gemms(const void *W1, const void *W3, const void *W2, voi
   const uint64_t R = static_cast<uint64_t>(L.R);
   if (!tmap_2d(&tm_dye_k, P.dye, d, R, BM) || !tmap_3d(&tm_w2_k, W2, d, f, E, BN) ||
       !tmap_2d(&tm_dab_k, P.dab, 2 * static_cast<uint64_t>(f), R, BM) || !tmap_3d(&tm_w1_k, W1, f, d, E, BN) ||
-      !tmap_3d(&tm_w3_k, W3, f, d, E, BN) || !tmap_2d(&tm_h_mn, P.hbuf, f, R, 64) ||
-      !tmap_2d(&tm_dye_mn, P.dye, d, R, 64) || !tmap_2d(&tm_x_mn, P.xperm, d, R, 64) ||
-      !tmap_2d(&tm_dab_mn, P.dab, 2 * static_cast<uint64_t>(f), R, 64))
+      !tmap_3d(&tm_w3_k, W3, f, d, E, BN) || !tmap_blocks_2d(&tm_h_mn, P.hbuf, f, R, BM / 64) ||
+      !tmap_blocks_2d(&tm_dye_mn, P.dye, d, R, BN / 64) || !tmap_blocks_2d(&tm_x_mn, P.xperm, d, R, BM / 64) ||
+      !tmap_blocks_2d(&tm_dab_mn, P.dab, 2 * static_cast<uint64_t>(f), R, BN / 64))
     return cudaErrorInvalidValue;
 
   BwdArgs a{};

@@ -46,5 +46,8 @@ bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, u
 // bf16 bank [E, rows, cols] with cols a multiple of 128, viewed as [E, cols/64, rows, 64]:
 // one box is 64 x 64 x 2 blocks, i.e. 128 columns x 64 rows in two 8 KiB swizzled blocks.
 bool tmap_4d_w(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E);
+// bf16 matrix [rows, cols] with cols a multiple of 64, viewed as [cols/64, rows, 64]:
+// one box is 64 columns x 64 rows x nblk column blocks (nblk 8 KiB swizzled blocks).
+bool tmap_blocks_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t nblk);
 
 }  // namespace moe

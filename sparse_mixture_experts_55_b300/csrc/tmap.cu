@@ -69,6 +69,21 @@ bool tmap_4d_w(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, ui
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// A row-major bf16 matrix viewed as [cols/64, rows, 64] (strides: a row, 64
+// columns): one box of 64 columns x 64 rows x nblk column blocks fills nblk
+// consecutive 8 KiB swizzled blocks of shared memory in one copy.
+bool tmap_blocks_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t nblk) {
+  auto fn = encode_fn();
+  if (!fn || cols % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, rows, cols / 64};
+  cuuint64_t strides[2] = {cols * 2, 128};
+  cuuint32_t box[3] = {64, 64, nblk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(ptr), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 // 2-D e4m3 matrix [rows, cols] (cols contiguous), box = 128 columns (128
 // bytes) x box_rows rows, 128-byte swizzle.
 bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows) {
