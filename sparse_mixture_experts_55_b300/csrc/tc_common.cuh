@@ -40,6 +40,8 @@ __device__ __noinline__ bool wait_bounded(uint64_t *bar, uint32_t parity, C &c, 
 //   tmap_2d      bf16 [rows, cols] (cols contiguous), box 64 cols x box_rows rows
 //   tmap_3d      bf16 bank [E, rows, cols], box 64 cols x box_rows rows x 1
 //   tmap_2d_u8   e4m3 [rows, cols], box 128 cols x box_rows rows
+//   tmap_4d_w    bf16 bank viewed in 64-column blocks, box 128 cols x 64 rows
+//   tmap_blocks_2d  bf16 [rows, cols] viewed in 64-column blocks, box nblk blocks x 64 rows
 bool tmap_2d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
 bool tmap_3d(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint64_t E, uint32_t box_rows = 64);
 bool tmap_2d_u8(CUtensorMap *m, const void *ptr, uint64_t cols, uint64_t rows, uint32_t box_rows);
